@@ -1,0 +1,105 @@
+/*
+ * tee_ops.h -- per-step entry points of the encoder pass (same library as tee.h).
+ *
+ * Each call runs ONE step of the pass on caller-provided DEVICE buffers,
+ * asynchronously on `stream` (a cudaStream_t, NULL = legacy default stream),
+ * using the weights already loaded into `ctx`.  They exist so each step can
+ * be checked against the CPU oracle and timed on its own; tee_encode_device
+ * runs exactly these steps in this order.
+ *
+ * Activation buffers use the context's activation type ACT:
+ *   TEE_F32 and TEE_W8A8 contexts: float;  TEE_BF16 contexts: bfloat16
+ *   (uint16 bit patterns).  The residual stream x is always float.
+ * Shapes: T = rows (tokens), H = hidden, I = intermediate, row-major.
+ * Return codes as in tee.h.  Buffers are borrowed for the duration of the
+ * stream work only.
+ *
+ * Steps (tensai page "テキスト埋め込み", §何が動くか):
+ *   embed       x[t] = E[id[t]]                                   (token embedding)
+ *   positions   pos[t] = t - cu[j] for t in text j                 (packing paragraph: positions restart per text)
+ *   layernorm   y = (x - mean) / sqrt(var + eps) * gamma           (エンコーダ: bias-free LayerNorm)
+ *   qkv         qkv = RoPE(y Wqkv^T)  (RoPE on q and k, base by layer)   (エンコーダ: RoPE attention)
+ *   attention   o = softmax(q k^T / sqrt(d) + mask) v per head     (エンコーダ: whole text / +-64 window)
+ *   out_proj    x += o Wo^T
+ *   ffn_in      z = GELU(u[:, :I]) * u[:, I:],  u = y Wi^T         (エンコーダ: GeGLU feed-forward)
+ *   ffn_out     x += z Wo_ffn^T
+ *   pool_l2     out[j] = mean_{t in j} x[t] / || . ||              (プーリング)
+ */
+#ifndef TEE_OPS_H
+#define TEE_OPS_H
+
+#include <stdint.h>
+#include "tee.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TEE_LN_ATTN 0
+#define TEE_LN_MLP  1
+
+#define TEE_W_QKV    0
+#define TEE_W_OUT    1
+#define TEE_W_FFN_IN 2
+#define TEE_W_FFN_OUT 3
+
+/* x float[T*H] <- E[ids]; ids int32[T].  Out-of-range ids give a zero row and
+ * set the context's device status (see tee_device_status). */
+int tee_op_embed(tee_ctx* ctx, const int32_t* d_ids, int T, float* d_x, void* stream);
+
+/* pos int32[T] from cu int32[n+1] (device) and its host copy h_cu. */
+int tee_op_positions(tee_ctx* ctx, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int32_t* d_pos,
+                     void* stream);
+
+/* y ACT[T*H] = LayerNorm(x float[T*H]) with the gain of (layer, which). */
+int tee_op_layernorm(tee_ctx* ctx, int layer, int which, const float* d_x, void* d_y, int T, void* stream);
+
+/* qkv ACT[T*3H] = y Wqkv^T with RoPE applied to the q and k thirds;
+ * pos int32[T] are the per-text positions. */
+int tee_op_qkv(tee_ctx* ctx, int layer, const void* d_y, const int32_t* d_pos, void* d_qkv, int T, void* stream);
+
+/* o ACT[T*H] = varlen attention of layer `layer` over qkv ACT[T*3H]
+ * (global if layer % global_every == 0, else the window); texts given by
+ * cu (device) and h_cu (host copy). */
+int tee_op_attention(tee_ctx* ctx, int layer, const void* d_qkv, const int32_t* d_cu, const int32_t* h_cu,
+                     int n_texts, void* d_o, void* stream);
+
+/* x float[T*H] += o ACT[T*H] Wo^T */
+int tee_op_out_proj(tee_ctx* ctx, int layer, const void* d_o, float* d_x, int T, void* stream);
+
+/* z ACT[T*I] = GeGLU(y ACT[T*H] Wi^T) */
+int tee_op_ffn_in(tee_ctx* ctx, int layer, const void* d_y, void* d_z, int T, void* stream);
+
+/* x float[T*H] += z ACT[T*I] Wo_ffn^T */
+int tee_op_ffn_out(tee_ctx* ctx, int layer, const void* d_z, float* d_x, int T, void* stream);
+
+/* out float[n*H] = L2-normalised per-text mean of x float[T*H]. */
+int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts,
+                   float* d_out, void* stream);
+
+/* ---- W8A8 pieces (TEE_W8A8 contexts) ----------------------------------- */
+
+/* Per-row 7-bit quantiser: s[m] = max|x[m,:]| / 63 (IEEE fp32 division),
+ * q = clamp(rint(x / s), -63, 63) (ties to even); zero rows give s = 0, q = 0.
+ * x float[M*K] -> q int8[M*K], s float[M]. */
+int tee_op_quant_rows7(tee_ctx* ctx, const float* d_x, int M, int K, int8_t* d_q, float* d_s, void* stream);
+
+/* Exact integer block sums I[m, n, b] = sum_{k in block b} q[m,k] * Wq[n,k]
+ * (blocks of 32 along K) for projection `which` of `layer`:
+ * q int8[M*K] -> partials int32[M*N*(K/32)], laid out [m][n][b]. */
+int tee_op_w8a8_partials(tee_ctx* ctx, int layer, int which, const int8_t* d_q, int M, int32_t* d_partials,
+                         void* stream);
+
+/* Copy the device-resident int8 codes int8[N*K] and block scales float[N*K/32]
+ * of projection `which` of `layer` to host buffers.  Synchronous. */
+int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d);
+
+/* Synchronise the context's device status word: TEE_OK, or TEE_EINVAL if a
+ * kernel met an out-of-range token id since the last call (the word is then
+ * cleared), or TEE_ETIMEOUT if a bounded device wait gave up. */
+int tee_device_status(tee_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TEE_OPS_H */

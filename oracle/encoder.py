@@ -87,15 +87,18 @@ def attention_text(q, k, v, is_global: bool, window: int, q_chunk: int = 256) ->
             k0, k1 = 0, L
         else:
             k0, k1 = max(0, q0 - window), min(L, q1 - 1 + window + 1)
-        s = np.einsum("qhd,khd->hqk", q[q0:q1], k[k0:k1]) * scale
         if not is_global:
             qi = np.arange(q0, q1)[:, None]
             kj = np.arange(k0, k1)[None, :]
-            s = np.where((np.abs(qi - kj) <= window)[None, :, :], s, -np.inf)
-        s = s - s.max(axis=-1, keepdims=True)
-        p = np.exp(s)
-        p /= p.sum(axis=-1, keepdims=True)
-        out[q0:q1] = np.einsum("hqk,khd->qhd", p, v[k0:k1])
+            allowed = np.abs(qi - kj) <= window
+        for h in range(nh):
+            s = (q[q0:q1, h, :] @ k[k0:k1, h, :].T) * scale
+            if not is_global:
+                s = np.where(allowed, s, -np.inf)
+            s = s - s.max(axis=-1, keepdims=True)
+            p = np.exp(s)
+            p /= p.sum(axis=-1, keepdims=True)
+            out[q0:q1, h, :] = p @ v[k0:k1, h, :]
     return out
 
 

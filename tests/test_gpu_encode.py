@@ -1,0 +1,169 @@
+"""End-to-end encoder passes through the C ABI on the GPU, against the oracle.
+
+Covers the five workloads (tiny fp32; the 310m shape in bf16 on the
+7-text accuracy batch; sampled texts of a full 32768-token sweep batch and of
+the 8 x 8192 long-document batch; the W8A8 path with outlier channels), the
+packing invariance the method states (a text's vector does not depend on the
+other texts packed with it), edge lengths around the tile and window sizes,
+and host-side rejection of malformed input.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from text_embedding_encoder_gb300 import binding, synth
+
+torch = pytest.importorskip("torch")
+from gpu_util import assert_embeddings_close, dev, make_encoder, to_np  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny_weights():
+    return synth.make_weights(synth.TINY, seed=0)
+
+
+@pytest.fixture(scope="module")
+def ruri_weights():
+    return synth.make_weights(synth.RURI_310M, seed=0)
+
+
+@pytest.fixture(scope="module")
+def ruri_bf16(lib, ruri_weights):
+    enc = make_encoder(synth.RURI_310M, "bf16", ruri_weights, max_tokens=65536, max_texts=1024)
+    yield enc
+    enc.close()
+
+
+@pytest.fixture(scope="module")
+def ruri_oracle_bf16(ruri_weights):
+    return oracle.OracleModel(ruri_weights, synth.RURI_310M, "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_tiny_config(lib, tiny_weights, dtype):
+    ids, cu = synth.make_batch(synth.TINY_LENGTHS, synth.TINY.vocab, seed=0)
+    enc = make_encoder(synth.TINY, dtype, tiny_weights, max_tokens=512, max_texts=16)
+    got = enc.encode(ids, cu)
+    ref = oracle.encode_packed(ids, cu, oracle.OracleModel(tiny_weights, synth.TINY, dtype))
+    err = assert_embeddings_close(got, ref, dtype)
+    print(f"tiny {dtype}: max abs err {err:.2e}")
+    np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
+    enc.close()
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("lengths", [[1], [2], [127, 128, 129], [65, 66, 130], [300], [1, 1, 1]])
+def test_tiny_edge_lengths(lib, tiny_weights, dtype, lengths):
+    ids, cu = synth.make_batch(lengths, synth.TINY.vocab, seed=sum(lengths))
+    enc = make_encoder(synth.TINY, dtype, tiny_weights, max_tokens=sum(lengths), max_texts=len(lengths))
+    got = enc.encode(ids, cu)
+    ref = oracle.encode_packed(ids, cu, oracle.OracleModel(tiny_weights, synth.TINY, dtype))
+    assert_embeddings_close(got, ref, dtype)
+    enc.close()
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_packing_invariance(lib, tiny_weights, dtype):
+    lengths = [37, 150, 8, 64, 129]
+    ids, cu = synth.make_batch(lengths, synth.TINY.vocab, seed=9)
+    enc = make_encoder(synth.TINY, dtype, tiny_weights, max_tokens=512, max_texts=16)
+    packed = enc.encode(ids, cu)
+    alone = np.stack([enc.encode(ids[a:b], np.array([0, b - a], np.int32)) [0] for a, b in zip(cu[:-1], cu[1:])])
+    # reversed packing order
+    order = list(range(len(lengths)))[::-1]
+    ids_r = np.concatenate([ids[cu[j]:cu[j + 1]] for j in order])
+    cu_r = np.concatenate([[0], np.cumsum([lengths[j] for j in order])]).astype(np.int32)
+    rev = enc.encode(ids_r, cu_r)[::-1]
+    tol = 0.0 if dtype == "fp32" else 1e-6
+    np.testing.assert_allclose(packed, alone, atol=tol, rtol=0)
+    np.testing.assert_allclose(packed, rev, atol=tol, rtol=0)
+    sim = packed @ packed.T
+    np.testing.assert_allclose(np.diag(sim), 1.0, atol=2e-6)
+    np.testing.assert_allclose(sim, sim.T, atol=1e-6)
+    enc.close()
+
+
+def test_ruri_accuracy_batch_bf16(ruri_bf16, ruri_oracle_bf16):
+    ids, cu = synth.make_batch(synth.ACCURACY_LENGTHS, synth.RURI_310M.vocab, seed=0)
+    got = ruri_bf16.encode(ids, cu)
+    ref = oracle.encode_packed(ids, cu, ruri_oracle_bf16)
+    err = assert_embeddings_close(got, ref, "bf16")
+    cos = np.sum(got * ref, axis=1)
+    print(f"310m bf16 accuracy batch: max abs {err:.2e}, min cos {cos.min():.6f}")
+
+
+def test_ruri_sweep_32k_sampled(ruri_bf16, ruri_oracle_bf16):
+    """Full 32768-token sweep batch in the bench's launch configuration
+    (device buffers, tee_encode_device); sampled texts checked by the oracle."""
+    ids, cu = synth.sweep_batch(32768, 0, synth.RURI_310M.vocab)
+    n = len(cu) - 1
+    out = torch.empty(n, synth.RURI_310M.hidden, device="cuda")
+    ruri_bf16.encode_device(dev(ids), dev(cu), cu, out, 0)
+    torch.cuda.synchronize()
+    got = to_np(out)
+    lens = np.diff(cu)
+    sample = sorted({int(np.argmin(lens)), int(np.argmax(lens)), int(np.argsort(lens)[n // 2]), n - 1})
+    ref = oracle.encode_packed(ids, cu, ruri_oracle_bf16, texts=sample)
+    assert_embeddings_close(got[sample], ref[sample], "bf16")
+    np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
+
+
+def test_ruri_long_docs_sampled(ruri_bf16, ruri_oracle_bf16):
+    ids, cu = synth.make_batch(synth.LONG_DOC_LENGTHS, synth.RURI_310M.vocab, seed=0)
+    got = ruri_bf16.encode(ids, cu)
+    ref = oracle.encode_packed(ids, cu, ruri_oracle_bf16, texts=[5])
+    assert_embeddings_close(got[[5]], ref[[5]], "bf16")
+    np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
+
+
+def test_ruri_w8a8_outliers(lib):
+    shape = synth.RURI_310M
+    w = synth.make_weights(shape, seed=0, outliers=True)
+    ids, cu = synth.make_batch(synth.ACCURACY_LENGTHS, shape.vocab, seed=0)
+    enc = make_encoder(shape, "w8a8", w, max_tokens=2048, max_texts=16)
+    got = enc.encode(ids, cu)
+    enc.close()
+    ref_int = oracle.encode_packed(ids, cu, oracle.OracleModel(w, shape, "w8a8"))
+    ref_f = oracle.encode_packed(ids, cu, oracle.OracleModel(w, shape, "fp32"))
+    cos_int = np.sum(got * ref_int, axis=1)
+    cos_f = np.sum(got * ref_f, axis=1)
+    cos_oracles = np.sum(ref_int * ref_f, axis=1)
+    print(f"w8a8: min cos vs W8A8 oracle {cos_int.min():.6f}; vs fp32 oracle {cos_f.min():.6f} "
+          f"(oracle W8A8 vs fp32: {cos_oracles.min():.6f})")
+    assert cos_int.min() >= 0.9999
+    np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
+
+
+def test_host_validation_and_recovery(lib, tiny_weights):
+    enc = binding.Encoder(synth.TINY, "fp32", max_tokens=64, max_texts=4)
+    ids, cu = synth.make_batch([5, 7], synth.TINY.vocab, seed=1)
+    with pytest.raises(binding.TeeError) as e:
+        enc.encode(ids, cu)
+    assert e.value.code == binding.TEE_ENOTLOADED
+    enc.load_weights(tiny_weights)
+    bad = [
+        (ids, np.array([1, 5, 12], np.int32), binding.TEE_EINVAL),          # cu[0] != 0
+        (ids, np.array([0, 5, 5], np.int32), binding.TEE_EINVAL),           # empty text
+        (ids, np.array([0, 7, 5], np.int32), binding.TEE_EINVAL),           # decreasing
+        (np.zeros(65, np.int32), np.array([0, 65], np.int32), binding.TEE_ETOOLONG),
+        (np.array([1, 5000, 2], np.int32), np.array([0, 3], np.int32), binding.TEE_EINVAL),   # id >= vocab
+        (np.array([1, -3, 2], np.int32), np.array([0, 3], np.int32), binding.TEE_EINVAL),
+        (ids, np.array([0], np.int32), binding.TEE_EINVAL),                 # no texts
+        (np.zeros(10, np.int32), np.arange(6, dtype=np.int32) * 2, binding.TEE_ETOOLONG),   # 5 texts > 4
+    ]
+    for bi, bc, code in bad:
+        with pytest.raises(binding.TeeError) as e:
+            enc.encode(bi, bc)
+        assert e.value.code == code, (bc, e.value)
+    good = enc.encode(ids, cu)   # still usable
+    ref = oracle.encode_packed(ids, cu, oracle.OracleModel(tiny_weights, synth.TINY, "fp32"))
+    assert_embeddings_close(good, ref, "fp32")
+    # device path: an out-of-range id is reported through the status word
+    out = torch.empty(1, synth.TINY.hidden, device="cuda")
+    enc.encode_device(dev(np.array([1, 99999, 2], np.int32)), dev(np.array([0, 3], np.int32)),
+                      np.array([0, 3], np.int32), out, 0)
+    assert enc.device_status() == binding.TEE_EINVAL
+    assert enc.device_status() == 0
+    enc.close()

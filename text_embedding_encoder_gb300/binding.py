@@ -1,0 +1,219 @@
+"""Thin ctypes binding of the C ABI (include/tee.h, include/tee_ops.h).
+
+Argument marshalling only: every step of the encoder runs in the CUDA
+library.  There is no fallback: if the compiled library is missing, loading
+raises.  Device buffers are passed as raw pointers (``tensor.data_ptr()``),
+streams as ``torch.cuda.Stream.cuda_stream`` integers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+TEE_OK = 0
+TEE_EINVAL = -1
+TEE_ENOTLOADED = -2
+TEE_ENOMEM = -3
+TEE_ECUDA = -4
+TEE_ETOOLONG = -5
+TEE_ETIMEOUT = -6
+
+TEE_F32, TEE_BF16, TEE_W8A8 = 0, 1, 2
+DTYPES = {"fp32": TEE_F32, "bf16": TEE_BF16, "w8a8": TEE_W8A8}
+
+TEE_LN_ATTN, TEE_LN_MLP = 0, 1
+TEE_W_QKV, TEE_W_OUT, TEE_W_FFN_IN, TEE_W_FFN_OUT = 0, 1, 2, 3
+
+KERNEL_CLASSES = ["embed", "layernorm", "gemm", "attention", "elementwise", "pool", "quant"]
+
+
+class TeeConfig(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("n_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int), ("intermediate", ctypes.c_int), ("vocab", ctypes.c_int),
+        ("global_every", ctypes.c_int), ("window", ctypes.c_int),
+        ("rope_base_global", ctypes.c_float), ("rope_base_local", ctypes.c_float), ("ln_eps", ctypes.c_float),
+        ("dtype", ctypes.c_int), ("max_tokens", ctypes.c_int), ("max_texts", ctypes.c_int),
+    ]
+
+
+_FP = ctypes.POINTER(ctypes.c_float)
+_FPP = ctypes.POINTER(_FP)
+
+
+class TeeWeights(ctypes.Structure):
+    _fields_ = [("tok_emb", _FP), ("ln_attn", _FPP), ("wqkv", _FPP), ("wo", _FPP),
+                ("ln_mlp", _FPP), ("wi", _FPP), ("wo_ffn", _FPP)]
+
+
+class TeeKernelStat(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int64), ("total_ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_ctx = ctypes.c_void_p
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+# name -> (restype, argtypes), for every function declared in include/*.h
+SIGNATURES = {
+    "tee_create": (_i, [ctypes.POINTER(TeeConfig), _i, ctypes.POINTER(_ctx)]),
+    "tee_load_weights": (_i, [_ctx, ctypes.POINTER(TeeWeights)]),
+    "tee_encode": (_i, [_ctx, _vp, _vp, _i, _vp]),
+    "tee_encode_device": (_i, [_ctx, _vp, _vp, _vp, _i, _vp, _vp]),
+    "tee_last_error": (ctypes.c_char_p, [_ctx]),
+    "tee_destroy": (None, [_ctx]),
+    "tee_profile_enable": (_i, [_ctx, _i]),
+    "tee_profile_read": (_i, [_ctx, ctypes.POINTER(TeeKernelStat)]),
+    "tee_op_embed": (_i, [_ctx, _vp, _i, _vp, _vp]),
+    "tee_op_positions": (_i, [_ctx, _vp, _vp, _i, _vp, _vp]),
+    "tee_op_layernorm": (_i, [_ctx, _i, _i, _vp, _vp, _i, _vp]),
+    "tee_op_qkv": (_i, [_ctx, _i, _vp, _vp, _vp, _i, _vp]),
+    "tee_op_attention": (_i, [_ctx, _i, _vp, _vp, _vp, _i, _vp, _vp]),
+    "tee_op_out_proj": (_i, [_ctx, _i, _vp, _vp, _i, _vp]),
+    "tee_op_ffn_in": (_i, [_ctx, _i, _vp, _vp, _i, _vp]),
+    "tee_op_ffn_out": (_i, [_ctx, _i, _vp, _vp, _i, _vp]),
+    "tee_op_pool_l2": (_i, [_ctx, _vp, _vp, _vp, _i, _vp, _vp]),
+    "tee_op_quant_rows7": (_i, [_ctx, _vp, _i, _i, _vp, _vp, _vp]),
+    "tee_op_w8a8_partials": (_i, [_ctx, _i, _i, _vp, _i, _vp, _vp]),
+    "tee_weight_codes": (_i, [_ctx, _i, _i, _vp, _vp]),
+    "tee_device_status": (_i, [_ctx]),
+}
+
+_LIB = None
+
+
+class TeeError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"tee error {code}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the compiled library (built by ``__graft_entry__.build()``).  Raises if absent."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _ptr(a) -> int:
+    """Device or host pointer of a torch tensor / numpy array / int."""
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    if hasattr(a, "data_ptr"):
+        return a.data_ptr()
+    if isinstance(a, np.ndarray):
+        if not a.flags.c_contiguous:
+            raise ValueError("array must be C-contiguous")
+        return a.ctypes.data
+    raise TypeError(type(a))
+
+
+def config_from_shape(shape, dtype: str, max_tokens: int, max_texts: int) -> TeeConfig:
+    return TeeConfig(shape.n_layers, shape.hidden, shape.n_heads, shape.head_dim, shape.intermediate, shape.vocab,
+                     shape.global_every, shape.window, shape.rope_base_global, shape.rope_base_local,
+                     shape.ln_eps, DTYPES[dtype], int(max_tokens), int(max_texts))
+
+
+class Encoder:
+    """One library context: owns device weights and workspace."""
+
+    def __init__(self, shape, dtype: str = "bf16", max_tokens: int = 32768, max_texts: int = 4096, device: int = 0):
+        self.lib = load()
+        self.shape = shape
+        self.dtype = dtype
+        self.cfg = config_from_shape(shape, dtype, max_tokens, max_texts)
+        ctx = ctypes.c_void_p()
+        rc = self.lib.tee_create(ctypes.byref(self.cfg), device, ctypes.byref(ctx))
+        if rc != TEE_OK:
+            raise TeeError(rc, self.lib.tee_last_error(None).decode())
+        self.ctx = ctx
+
+    # -- helpers --------------------------------------------------------
+    def check(self, rc):
+        if rc != TEE_OK:
+            raise TeeError(rc, self.lib.tee_last_error(self.ctx).decode())
+        return rc
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            self.lib.tee_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- public API -------------------------------------------------------
+    def load_weights(self, w):
+        L = self.shape.n_layers
+        keep = []
+
+        def f32(a):
+            a = np.ascontiguousarray(a, dtype=np.float32)
+            keep.append(a)
+            return a.ctypes.data_as(_FP)
+
+        def arr(lst):
+            ptrs = (_FP * L)(*[f32(a) for a in lst])
+            keep.append(ptrs)
+            return ctypes.cast(ptrs, _FPP)
+
+        tw = TeeWeights(f32(w.tok_emb), arr(w.ln_attn), arr(w.wqkv), arr(w.wo), arr(w.ln_mlp), arr(w.wi),
+                        arr(w.wo_ffn))
+        self.check(self.lib.tee_load_weights(self.ctx, ctypes.byref(tw)))
+
+    def encode(self, ids, cu_seqlens) -> np.ndarray:
+        """Host arrays in, host fp32 [n, H] out (synchronous)."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        n = cu.shape[0] - 1
+        out = np.empty((max(n, 0), self.shape.hidden), dtype=np.float32)
+        self.check(self.lib.tee_encode(self.ctx, ids.ctypes.data, cu.ctypes.data, n, out.ctypes.data))
+        return out
+
+    def encode_device(self, d_ids, d_cu, h_cu, d_out, stream=0):
+        h_cu = np.ascontiguousarray(h_cu, dtype=np.int32)
+        self.check(self.lib.tee_encode_device(self.ctx, _ptr(d_ids), _ptr(d_cu), h_cu.ctypes.data,
+                                              h_cu.shape[0] - 1, _ptr(d_out), stream))
+
+    def profile_enable(self, on=True):
+        self.check(self.lib.tee_profile_enable(self.ctx, 1 if on else 0))
+
+    def profile_read(self) -> dict:
+        stats = (TeeKernelStat * len(KERNEL_CLASSES))()
+        self.check(self.lib.tee_profile_read(self.ctx, stats))
+        return {name: {"launches": s.launches, "total_ms": s.total_ms, "flops": s.flops, "bytes": s.bytes}
+                for name, s in zip(KERNEL_CLASSES, stats)}
+
+    def device_status(self) -> int:
+        return self.lib.tee_device_status(self.ctx)
+
+    # -- per-step entry points (tee_ops.h) ------------------------------
+    def op(self, name, *args):
+        return self.check(getattr(self.lib, name)(self.ctx, *[_ptr(a) if not isinstance(a, (int, float)) else a
+                                                              for a in args]))

@@ -1,0 +1,268 @@
+// Memory-bound steps of the pass: embedding gather, per-text positions,
+// bias-free LayerNorm, RoPE, GeGLU gate, and mean-pool + L2 normalisation.
+//
+// Method: tensai page "テキスト埋め込み", §何が動くか (エンコーダ, プーリング,
+// packing paragraph).  All of these are bandwidth-bound: rows are read with
+// 16-byte vector loads, one warp (LayerNorm) or one block (pool) per row /
+// text, reductions by warp shuffles.
+#include "tee_internal.cuh"
+
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Index of the text containing token t: the largest j with cu[j] <= t.
+__device__ __forceinline__ int text_of(const int32_t* cu, int n_texts, int t) {
+    int lo = 0, hi = n_texts - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void convert_f32_bf16_kernel(const float* __restrict__ src, bf16* __restrict__ dst, size_t n) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (; i < n; i += stride) dst[i] = __float2bfloat16_rn(src[i]);
+}
+
+// x[t, :] = E[id[t], :]; one block of H/4 threads per token, 16-byte loads.
+template <typename TE>
+__global__ void embed_kernel(const TE* __restrict__ emb, const int32_t* __restrict__ ids, int T, int H, int V,
+                             float* __restrict__ x, unsigned int* status) {
+    int t = blockIdx.x;
+    if (t >= T) return;
+    int id = ids[t];
+    bool ok = (id >= 0 && id < V);
+    if (!ok && threadIdx.x == 0 && status) atomicOr(status, TEE_STATUS_BAD_ID);
+    float4* dst = reinterpret_cast<float4*>(x + (size_t)t * H);
+    for (int c4 = threadIdx.x; c4 < H / 4; c4 += blockDim.x) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ok) {
+            if constexpr (sizeof(TE) == 4) {
+                v = reinterpret_cast<const float4*>(emb + (size_t)id * H)[c4];
+            } else {
+                const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(emb + (size_t)id * H) + 2 * c4;
+                float2 a = __bfloat1622float2(p[0]);
+                float2 b = __bfloat1622float2(p[1]);
+                v = make_float4(a.x, a.y, b.x, b.y);
+            }
+        }
+        dst[c4] = v;
+    }
+}
+
+// pos[t] = t - cu[text(t)]
+__global__ void positions_kernel(const int32_t* __restrict__ cu, int n_texts, int T, int32_t* __restrict__ pos) {
+    int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    pos[t] = t - cu[text_of(cu, n_texts, t)];
+}
+
+// One warp per row; H a multiple of 128 and <= 1024 (at most 8 float4 per lane).
+template <typename TY>
+__global__ void layernorm_kernel(const float* __restrict__ x, const float* __restrict__ gamma, TY* __restrict__ y,
+                                 int T, int H, float eps) {
+    int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    int lane = threadIdx.x & 31;
+    if (warp >= T) return;
+    const float4* row = reinterpret_cast<const float4*>(x + (size_t)warp * H);
+    const int nv = H / 128;   // float4 per lane
+    float4 v[8];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i < nv) {
+            v[i] = row[i * 32 + lane];
+            s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+        }
+    }
+    const float mean = warp_sum(s) / (float)H;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i < nv) {
+            float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, d = v[i].w - mean;
+            ss += (a * a + b * b) + (c * c + d * d);
+        }
+    }
+    const float var = warp_sum(ss) / (float)H;
+    const float rstd = 1.0f / sqrtf(var + eps);
+    const float4* g4 = reinterpret_cast<const float4*>(gamma);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i < nv) {
+            int c4 = i * 32 + lane;
+            float4 g = g4[c4];
+            float o0 = (v[i].x - mean) * rstd * g.x, o1 = (v[i].y - mean) * rstd * g.y;
+            float o2 = (v[i].z - mean) * rstd * g.z, o3 = (v[i].w - mean) * rstd * g.w;
+            if constexpr (sizeof(TY) == 4) {
+                reinterpret_cast<float4*>(y + (size_t)warp * H)[c4] = make_float4(o0, o1, o2, o3);
+            } else {
+                __nv_bfloat162 p0 = __floats2bfloat162_rn(o0, o1);
+                __nv_bfloat162 p1 = __floats2bfloat162_rn(o2, o3);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&p0);
+                pk.y = *reinterpret_cast<uint32_t*>(&p1);
+                reinterpret_cast<uint2*>(y + (size_t)warp * H)[c4] = pk;
+            }
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v) {
+    if constexpr (sizeof(T) == 4) return v; else return __bfloat162float(v);
+}
+template <typename T>
+__device__ __forceinline__ T from_f(float v) {
+    if constexpr (sizeof(T) == 4) return v; else return __float2bfloat16_rn(v);
+}
+
+// Rotate-half RoPE on the q and k thirds of qkv [T, 3H]; one thread per
+// (token, head, pair j < 32), applied to q and k.
+template <typename TA>
+__global__ void rope_kernel(TA* __restrict__ qkv, const int32_t* __restrict__ pos, const float* __restrict__ cos_t,
+                            const float* __restrict__ sin_t, int T, int H, int n_heads) {
+    int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    int j = idx & 31;
+    int h = (idx >> 5) % n_heads;
+    int t = (idx >> 5) / n_heads;
+    if (t >= T) return;
+    int p = pos[t];
+    float c = cos_t[(size_t)p * 32 + j], s = sin_t[(size_t)p * 32 + j];
+    TA* row = qkv + (size_t)t * 3 * H + h * 64;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+        TA* r = row + part * H;
+        float lo = to_f(r[j]), hi = to_f(r[j + 32]);
+        r[j] = from_f<TA>(lo * c - hi * s);
+        r[j + 32] = from_f<TA>(hi * c + lo * s);
+    }
+}
+
+__device__ __forceinline__ float gelu_erf(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
+
+// z[t, c] = GELU(u[t, c]) * u[t, I + c]
+template <typename TA>
+__global__ void geglu_kernel(const TA* __restrict__ u, TA* __restrict__ z, int T, int I) {
+    size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    size_t n = (size_t)T * I;
+    if (idx >= n) return;
+    size_t t = idx / I, c = idx % I;
+    float a = to_f(u[t * 2 * I + c]);
+    float g = to_f(u[t * 2 * I + I + c]);
+    z[idx] = from_f<TA>(gelu_erf(a) * g);
+}
+
+// One block per text: column sums over the text's rows, then L2 scaling.
+__global__ void pool_l2_kernel(const float* __restrict__ x, const int32_t* __restrict__ cu, int H,
+                               float* __restrict__ out) {
+    __shared__ float red[32];
+    int j = blockIdx.x;
+    int t0 = cu[j], t1 = cu[j + 1];
+    float inv_len = 1.0f / (float)(t1 - t0);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};   // H <= 4 * blockDim.x
+    for (int t = t0; t < t1; ++t) {
+        const float* row = x + (size_t)t * H;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            int c = threadIdx.x + i * blockDim.x;
+            if (c < H) acc[i] += row[c];
+        }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[i] *= inv_len;
+        int c = threadIdx.x + i * blockDim.x;
+        if (c < H) ss += acc[i] * acc[i];
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        v = warp_sum(v);
+        if (threadIdx.x == 0) red[0] = v;
+    }
+    __syncthreads();
+    float scale = 1.0f / fmaxf(sqrtf(red[0]), 1e-12f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int c = threadIdx.x + i * blockDim.x;
+        if (c < H) out[(size_t)j * H + c] = acc[i] * scale;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_convert_f32_bf16(const float* src, bf16* dst, size_t n, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    size_t blocks = (n + 255) / 256;
+    if (blocks > 152 * 64) blocks = 152 * 64;
+    convert_f32_bf16_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, dst, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_embed(const void* emb, bool emb_bf16, const int32_t* ids, int T, int H, int V, float* x,
+                         unsigned int* status, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    int threads = H / 4 < 256 ? H / 4 : 256;
+    if (emb_bf16)
+        embed_kernel<bf16><<<T, threads, 0, s>>>((const bf16*)emb, ids, T, H, V, x, status);
+    else
+        embed_kernel<float><<<T, threads, 0, s>>>((const float*)emb, ids, T, H, V, x, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_positions(const int32_t* cu, int n_texts, int T, int32_t* pos, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    positions_kernel<<<(T + 255) / 256, 256, 0, s>>>(cu, n_texts, T, pos);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_layernorm(const float* x, const float* gamma, void* y, bool y_bf16, int T, int H, float eps,
+                             cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    int blocks = (T + 7) / 8;   // 8 warps per block, one row per warp
+    if (y_bf16)
+        layernorm_kernel<bf16><<<blocks, 256, 0, s>>>(x, gamma, (bf16*)y, T, H, eps);
+    else
+        layernorm_kernel<float><<<blocks, 256, 0, s>>>(x, gamma, (float*)y, T, H, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope(void* qkv, bool bf16_act, const int32_t* pos, const float* cos_t, const float* sin_t, int T,
+                        int H, int n_heads, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    size_t threads = (size_t)T * n_heads * 32;
+    unsigned blocks = (unsigned)((threads + 255) / 256);
+    if (bf16_act)
+        rope_kernel<bf16><<<blocks, 256, 0, s>>>((bf16*)qkv, pos, cos_t, sin_t, T, H, n_heads);
+    else
+        rope_kernel<float><<<blocks, 256, 0, s>>>((float*)qkv, pos, cos_t, sin_t, T, H, n_heads);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_geglu(const void* u, void* z, bool bf16_act, int T, int I, cudaStream_t s) {
+    size_t n = (size_t)T * I;
+    if (n == 0) return cudaSuccess;
+    unsigned blocks = (unsigned)((n + 255) / 256);
+    if (bf16_act)
+        geglu_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)u, (bf16*)z, T, I);
+    else
+        geglu_kernel<float><<<blocks, 256, 0, s>>>((const float*)u, (float*)z, T, I);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pool_l2(const float* x, const int32_t* cu, int n_texts, int H, float* out, cudaStream_t s) {
+    if (n_texts == 0) return cudaSuccess;
+    pool_l2_kernel<<<n_texts, 256, 0, s>>>(x, cu, H, out);
+    return cudaGetLastError();
+}

@@ -1,0 +1,468 @@
+// bf16 projection GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// The four projections of every layer (QKV, attention output, GeGLU input,
+// feed-forward output; tensai page "テキスト埋め込み", §何が動くか / エンコーダ)
+// are the only dense contractions of the pass.  C = A W^T with A [M, K] the
+// token activations and W [N, K] the weights, both bf16 and K-contiguous.
+//
+// Design (one CTA per SM, persistent over output tiles):
+//   * tile 128 x BN (BN = 256, or 128 when N is not a multiple of 256), K step 64
+//     (one 128-byte swizzle atom); 4-stage shared-memory ring filled by TMA
+//     (cp.async.bulk.tensor, 128B swizzle, out-of-range rows zero-filled).
+//   * warp 0 lane 0: TMA producer.  warp 1: TMEM allocator, lane 0 issues
+//     tcgen05.mma (M=128, N=BN, K=16) and commits to mbarriers.  warps 2-5:
+//     epilogue, each reading its 32-lane TMEM quadrant with tcgen05.ld.
+//   * two TMEM accumulators (2 x BN fp32 columns) so the epilogue of one tile
+//     overlaps the MMAs of the next.
+//   * tiles are ordered with the N index fastest, so CTAs running at the same
+//     time share their A rows in L2.
+//   * epilogues fused into the store: bf16 store, fp32 residual add, RoPE on
+//     the q/k columns (positions restart per text), GeGLU gate.
+//   * every mbarrier wait is bounded: after ~2 s the CTA raises an abort flag,
+//     drains its in-flight copies and MMAs, frees TMEM, sets the timeout bit
+//     of the status word and returns.
+#include "tee_internal.cuh"
+#include "gemm_tc.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int NUM_THREADS = 192;
+constexpr long long WAIT_CYCLES = 4000000000LL;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase of `parity` to complete.  Gives up (returning false) when
+// another role raised the abort flag or after WAIT_CYCLES, raising it.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > WAIT_CYCLES) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+// Bounded wait that ignores the abort flag (used to drain in-flight work).
+__device__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > WAIT_CYCLES) return false;
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane; waits for completion.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte
+// swizzle layout that TMA writes: rows of 128 bytes (64 bf16), 8-row atoms of
+// 1024 bytes (stride byte offset), 1024-byte aligned base.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= (uint64_t)1 << 16;                     // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset
+    d |= (uint64_t)1 << 46;                     // descriptor version
+    d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16 with bf16 A/B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float gelu_erf(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ void store_bf16x32(bf16* dst, const float (&v)[32]) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 q;
+        q.x = pack_bf16(v[8 * i + 0], v[8 * i + 1]);
+        q.y = pack_bf16(v[8 * i + 2], v[8 * i + 3]);
+        q.z = pack_bf16(v[8 * i + 4], v[8 * i + 5]);
+        q.w = pack_bf16(v[8 * i + 6], v[8 * i + 7]);
+        d[i] = q;
+    }
+}
+
+struct Params {
+    void* C;
+    int M, N, K;
+    const int32_t* pos;
+    const float* rope_cos;
+    const float* rope_sin;
+    int hidden;
+    unsigned int* status;
+};
+
+template <int BN>
+struct Smem {
+    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr uint32_t N_BARS = 2 * STAGES + 5;
+    static constexpr uint32_t TOTAL = BAR_OFF + N_BARS * 8 + 16 + 1024;   // + alignment slack
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+};
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+    using S = Smem<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::N_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+    // barrier indices
+    const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, TEMPTY = 2 * STAGES + 2, MMA_DONE = 2 * STAGES + 4;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_m = (p.M + BM - 1) / BM, num_n = p.N / BN, num_k = p.K / BK;
+    const int num_tiles = num_m * num_n;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar(FULL + s), 1);
+            mbar_init(bar(EMPTY + s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar(TFULL + a), 1);
+            mbar_init(bar(TEMPTY + a), 128);
+        }
+        mbar_init(bar(MMA_DONE), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(S::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            uint32_t g = 0;
+            uint32_t armed_parity[STAGES];
+            bool armed[STAGES];
+            for (int s = 0; s < STAGES; ++s) armed[s] = false, armed_parity[s] = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const int n_t = tile % num_n, m_t = tile / num_n;
+                for (int kb = 0; kb < num_k; ++kb, ++g) {
+                    const int s = g % STAGES;
+                    const uint32_t r = g / STAGES;
+                    if (!mbar_wait(bar(EMPTY + s), (r & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + s * S::STAGE_BYTES;
+                    const uint32_t sb = sa + A_BYTES;
+                    mbar_expect_tx(bar(FULL + s), S::STAGE_BYTES);
+                    tma_load_2d(sa, &tmA, kb * BK, m_t * BM, bar(FULL + s));
+                    tma_load_2d(sb, &tmB, kb * BK, n_t * BN, bar(FULL + s));
+                    armed[s] = true;
+                    armed_parity[s] = r & 1;
+                }
+            }
+            // no copy may still be landing in shared memory when the CTA exits
+            for (int s = 0; s < STAGES; ++s)
+                if (armed[s]) mbar_wait_drain(bar(FULL + s), armed_parity[s]);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(BM, BN);
+            uint32_t g = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+                const int acc = it & 1, use = it >> 1;
+                if (!mbar_wait(bar(TEMPTY + acc), (use & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < num_k; ++kb, ++g) {
+                    const int s = g % STAGES;
+                    const uint32_t r = g / STAGES;
+                    if (!mbar_wait(bar(FULL + s), r & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + s * S::STAGE_BYTES;
+                    const uint64_t adesc = sw128_desc(sa);
+                    const uint64_t bdesc = sw128_desc(sa + A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                    mma_commit(bar(EMPTY + s));
+                }
+                if (!ok) break;
+                mma_commit(bar(TFULL + acc));
+            }
+            // every MMA issued must be finished before TMEM is freed
+            mma_commit(bar(MMA_DONE));
+            mbar_wait_drain(bar(MMA_DONE), 0);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quad = warp & 3;
+        const int row_local = quad * 32 + lane;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            const int acc = it & 1, use = it >> 1;
+            if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
+            tc_fence_after();
+            const int n_t = tile % num_n, m_t = tile / num_n;
+            const int gr = m_t * BM + row_local;
+            const bool valid = gr < p.M;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
+            if constexpr (EPI == GEMM_EPI_STORE_BF16) {
+                bf16* C = reinterpret_cast<bf16*>(p.C) + (size_t)gr * p.N + n_t * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    if (valid) store_bf16x32(C + c * 32, v);
+                }
+            } else if constexpr (EPI == GEMM_EPI_ADD_F32) {
+                float* C = reinterpret_cast<float*>(p.C) + (size_t)gr * p.N + n_t * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    if (valid) {
+                        float4* d = reinterpret_cast<float4*>(C + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            float4 o = d[i];
+                            o.x += v[4 * i + 0];
+                            o.y += v[4 * i + 1];
+                            o.z += v[4 * i + 2];
+                            o.w += v[4 * i + 3];
+                            d[i] = o;
+                        }
+                    }
+                }
+            } else if constexpr (EPI == GEMM_EPI_ROPE_BF16) {
+                bf16* C = reinterpret_cast<bf16*>(p.C) + (size_t)gr * p.N + n_t * BN;
+                const int pos = valid ? p.pos[gr] : 0;
+                const float* cs = p.rope_cos + (size_t)pos * 32;
+                const float* sn = p.rope_sin + (size_t)pos * 32;
+#pragma unroll 1
+                for (int hh = 0; hh < BN / 64; ++hh) {
+                    float lo[32], hi[32];
+                    tmem_ld32(taddr + hh * 64, lo);
+                    tmem_ld32(taddr + hh * 64 + 32, hi);
+                    if (valid) {
+                        if (n_t * BN + hh * 64 < 2 * p.hidden) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const float c = cs[j], s = sn[j];
+                                const float a = lo[j] * c - hi[j] * s;
+                                const float b = hi[j] * c + lo[j] * s;
+                                lo[j] = a;
+                                hi[j] = b;
+                            }
+                        }
+                        store_bf16x32(C + hh * 64, lo);
+                        store_bf16x32(C + hh * 64 + 32, hi);
+                    }
+                }
+            } else {   // GEMM_EPI_GEGLU (BN == 256)
+                bf16* C = reinterpret_cast<bf16*>(p.C) + (size_t)gr * (p.N / 2) + n_t * (BN / 2);
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    float a[32], g[32];
+                    tmem_ld32(taddr + c * 32, a);
+                    tmem_ld32(taddr + BN / 2 + c * 32, g);
+                    if (valid) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) a[j] = gelu_erf(a[j]) * g[j];
+                        store_bf16x32(C + c * 32, a);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(TEMPTY + acc));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(S::TMEM_COLS)
+                     : "memory");
+    }
+    if (threadIdx.x == 0 && *abort_flag && p.status) atomicOr(p.status, TEE_STATUS_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_num_sms = 0;
+std::once_flag g_once;
+cudaError_t g_init_err = cudaSuccess;
+
+void init_once() {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        g_init_err = e != cudaSuccess ? e : cudaErrorNotSupported;
+        return;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) g_init_err = e;
+}
+
+bool make_map(CUtensorMap* map, const void* ptr, int rows, int K, int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid, cudaStream_t s) {
+    static bool attr_set = false;
+    constexpr uint32_t smem = Smem<BN>::TOTAL;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    gemm_tc_kernel<BN, EPI><<<grid, NUM_THREADS, smem, s>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
+    std::call_once(g_once, init_once);
+    if (g_init_err != cudaSuccess) return g_init_err;
+    if (a.M < 0 || a.N <= 0 || a.K <= 0 || a.N % 128 || a.K % BK) return cudaErrorInvalidValue;
+    if (a.epi == GEMM_EPI_GEGLU && a.N % 256) return cudaErrorInvalidValue;
+    if (a.epi < GEMM_EPI_STORE_BF16 || a.epi > GEMM_EPI_GEGLU) return cudaErrorInvalidValue;
+    if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.W) | reinterpret_cast<uintptr_t>(a.C)) & 15)
+        return cudaErrorMisalignedAddress;
+    if (a.M == 0) return cudaSuccess;
+    const int BN = (a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, BN)) return cudaErrorInvalidValue;
+    Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status};
+    const int tiles = ((a.M + BM - 1) / BM) * (a.N / BN);
+    const int grid = tiles < g_num_sms ? tiles : g_num_sms;
+    if (BN == 256) {
+        switch (a.epi) {
+            case GEMM_EPI_STORE_BF16: return launch_t<256, GEMM_EPI_STORE_BF16>(ma, mb, p, grid, s);
+            case GEMM_EPI_ADD_F32: return launch_t<256, GEMM_EPI_ADD_F32>(ma, mb, p, grid, s);
+            case GEMM_EPI_ROPE_BF16: return launch_t<256, GEMM_EPI_ROPE_BF16>(ma, mb, p, grid, s);
+            default: return launch_t<256, GEMM_EPI_GEGLU>(ma, mb, p, grid, s);
+        }
+    }
+    switch (a.epi) {
+        case GEMM_EPI_STORE_BF16: return launch_t<128, GEMM_EPI_STORE_BF16>(ma, mb, p, grid, s);
+        case GEMM_EPI_ADD_F32: return launch_t<128, GEMM_EPI_ADD_F32>(ma, mb, p, grid, s);
+        default: return launch_t<128, GEMM_EPI_ROPE_BF16>(ma, mb, p, grid, s);
+    }
+}

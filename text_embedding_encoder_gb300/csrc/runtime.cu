@@ -1,0 +1,673 @@
+// C ABI runtime: context, weight ingestion, workspace, validation, the launch
+// sequence of one encoder pass, per-step entry points and the profiling hook.
+//
+// The pass follows the tensai page "テキスト埋め込み", §何が動くか: token
+// embedding; per layer a bias-free LayerNorm, QKV projection with RoPE
+// (positions restart per text), attention confined to each text (whole text
+// on layer 0 and every third layer, +-64 tokens otherwise), the output
+// projection with the residual, a second bias-free LayerNorm and the GeGLU
+// feed-forward with the residual; finally the per-text mean and L2 scaling.
+#include "tee_internal.cuh"
+#include "gemm_tc.cuh"
+
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+
+namespace {
+
+std::string g_create_error;
+
+int fail(tee_ctx* c, int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (c) c->err = buf; else g_create_error = buf;
+    return code;
+}
+
+int cuda_fail(tee_ctx* c, cudaError_t e, const char* what) {
+    return fail(c, e == cudaErrorMemoryAllocation ? TEE_ENOMEM : TEE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CK(call)                                                   \
+    do {                                                           \
+        cudaError_t _e = (call);                                   \
+        if (_e != cudaSuccess) return cuda_fail(ctx, _e, #call);   \
+    } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Sub-allocator over one device allocation (offsets aligned to 256 bytes).
+struct Carve {
+    char* base;
+    size_t off = 0;
+    explicit Carve(void* b) : base((char*)b) {}
+    template <typename T>
+    T* take(size_t count, size_t elem = sizeof(T)) {
+        T* p = (T*)(base ? base + off : nullptr);
+        off = align_up(off + count * elem, 256);
+        return p;
+    }
+};
+
+int wshape(const tee_config& c, int which, int* N, int* K) {
+    const int H = c.hidden, I = c.intermediate;
+    switch (which) {
+        case TEE_W_QKV: *N = 3 * H; *K = H; return 0;
+        case TEE_W_OUT: *N = H; *K = H; return 0;
+        case TEE_W_FFN_IN: *N = 2 * I; *K = H; return 0;
+        case TEE_W_FFN_OUT: *N = H; *K = I; return 0;
+    }
+    return -1;
+}
+
+int validate_config(const tee_config* c) {
+    if (!c) return fail(nullptr, TEE_EINVAL, "config is NULL");
+    if (c->n_layers < 1) return fail(nullptr, TEE_EINVAL, "n_layers must be >= 1");
+    if (c->head_dim != 64) return fail(nullptr, TEE_EINVAL, "head_dim must be 64");
+    if (c->n_heads < 1 || c->hidden != c->n_heads * c->head_dim)
+        return fail(nullptr, TEE_EINVAL, "hidden must equal n_heads * head_dim");
+    if (c->hidden % 128 || c->hidden > 1024) return fail(nullptr, TEE_EINVAL, "hidden must be a multiple of 128, <= 1024");
+    if (c->intermediate < 128 || c->intermediate % 128) return fail(nullptr, TEE_EINVAL, "intermediate must be a multiple of 128");
+    if (c->vocab < 1) return fail(nullptr, TEE_EINVAL, "vocab must be >= 1");
+    if (c->global_every < 1) return fail(nullptr, TEE_EINVAL, "global_every must be >= 1");
+    if (c->window < 0) return fail(nullptr, TEE_EINVAL, "window must be >= 0");
+    if (!(c->rope_base_global > 0.f) || !(c->rope_base_local > 0.f)) return fail(nullptr, TEE_EINVAL, "RoPE bases must be > 0");
+    if (!(c->ln_eps >= 0.f)) return fail(nullptr, TEE_EINVAL, "ln_eps must be >= 0");
+    if (c->dtype != TEE_F32 && c->dtype != TEE_BF16 && c->dtype != TEE_W8A8) return fail(nullptr, TEE_EINVAL, "unknown dtype");
+    if (c->max_tokens < 1 || c->max_texts < 1) return fail(nullptr, TEE_EINVAL, "max_tokens and max_texts must be >= 1");
+    if (c->max_tokens > (1 << 24)) return fail(nullptr, TEE_EINVAL, "max_tokens must be <= 2^24");
+    return TEE_OK;
+}
+
+// Workspace layout (also used to size the allocation: base == nullptr).
+size_t carve_workspace(tee_ctx* c, void* base) {
+    const tee_config& g = c->cfg;
+    const size_t T = g.max_tokens, H = g.hidden, I = g.intermediate, A = act_size(c);
+    Carve cv(base);
+    c->d_ids = cv.take<int32_t>(T);
+    c->d_cu = cv.take<int32_t>(g.max_texts + 1);
+    c->d_pos = cv.take<int32_t>(T);
+    c->x = cv.take<float>(T * H);
+    c->y = cv.take<char>(T * H, A);
+    c->qkv = cv.take<char>(T * 3 * H, A);
+    c->o = cv.take<char>(T * H, A);
+    c->u = cv.take<char>(T * 2 * I, A);
+    c->z = cv.take<char>(T * I, A);
+    c->out = cv.take<float>((size_t)g.max_texts * H);
+    if (g.dtype == TEE_W8A8) {
+        c->qa = cv.take<int8_t>(T * std::max(H, I));
+        c->qs = cv.take<float>(T);
+    } else {
+        c->qa = nullptr;
+        c->qs = nullptr;
+    }
+    for (int b = 0; b < 2; ++b) {
+        c->rope_cos[b] = cv.take<float>(T * 32);
+        c->rope_sin[b] = cv.take<float>(T * 32);
+    }
+    c->d_status = cv.take<unsigned int>(4);
+    return cv.off;
+}
+
+// Per-layer weight layout inside the weight arena.
+size_t carve_weights(tee_ctx* c, void* base) {
+    const tee_config& g = c->cfg;
+    const size_t H = g.hidden;
+    Carve cv(base);
+    const size_t esz = g.dtype == TEE_BF16 ? 2 : (g.dtype == TEE_F32 ? 4 : 1);
+    c->emb = cv.take<char>((size_t)g.vocab * H, g.dtype == TEE_BF16 ? 2 : 4);
+    c->layers.assign(g.n_layers, LayerWeights{});
+    for (int l = 0; l < g.n_layers; ++l) {
+        LayerWeights& L = c->layers[l];
+        L.ln_attn = cv.take<float>(H);
+        L.ln_mlp = cv.take<float>(H);
+        for (int w = 0; w < 4; ++w) {
+            int N, K;
+            wshape(g, w, &N, &K);
+            L.w[w] = cv.take<char>((size_t)N * K, esz);
+            L.wd[w] = g.dtype == TEE_W8A8 ? cv.take<float>((size_t)N * K / 32) : nullptr;
+        }
+    }
+    return cv.off;
+}
+
+// RoPE cos/sin tables for positions 0..max_tokens-1 (fp64 angles, fp32 storage).
+int build_rope_tables(tee_ctx* ctx) {
+    const tee_config& g = ctx->cfg;
+    const size_t T = g.max_tokens;
+    std::vector<float> cs(T * 32), sn(T * 32);
+    for (int b = 0; b < 2; ++b) {
+        const double base = b == 0 ? g.rope_base_global : g.rope_base_local;
+        double inv_freq[32];
+        for (int j = 0; j < 32; ++j) inv_freq[j] = pow(base, -2.0 * j / 64.0);
+        for (size_t p = 0; p < T; ++p)
+            for (int j = 0; j < 32; ++j) {
+                const double a = (double)p * inv_freq[j];
+                cs[p * 32 + j] = (float)cos(a);
+                sn[p * 32 + j] = (float)sin(a);
+            }
+        CK(cudaMemcpy(ctx->rope_cos[b], cs.data(), T * 32 * sizeof(float), cudaMemcpyHostToDevice));
+        CK(cudaMemcpy(ctx->rope_sin[b], sn.data(), T * 32 * sizeof(float), cudaMemcpyHostToDevice));
+    }
+    return TEE_OK;
+}
+
+// Validate a host cu_seqlens array; returns total tokens via *T.
+int check_cu(tee_ctx* ctx, const int32_t* h_cu, int n_texts, int* T) {
+    if (!h_cu) return fail(ctx, TEE_EINVAL, "cu_seqlens is NULL");
+    if (n_texts < 1) return fail(ctx, TEE_EINVAL, "n_texts must be >= 1 (got %d)", n_texts);
+    if (n_texts > ctx->cfg.max_texts) return fail(ctx, TEE_ETOOLONG, "n_texts %d > max_texts %d", n_texts, ctx->cfg.max_texts);
+    if (h_cu[0] != 0) return fail(ctx, TEE_EINVAL, "cu_seqlens[0] must be 0 (got %d)", h_cu[0]);
+    for (int j = 0; j < n_texts; ++j)
+        if (h_cu[j + 1] <= h_cu[j])
+            return fail(ctx, TEE_EINVAL, "cu_seqlens must be strictly increasing (text %d is empty or negative)", j);
+    if (h_cu[n_texts] > ctx->cfg.max_tokens)
+        return fail(ctx, TEE_ETOOLONG, "total tokens %d > max_tokens %d", h_cu[n_texts], ctx->cfg.max_tokens);
+    *T = h_cu[n_texts];
+    return TEE_OK;
+}
+
+// Algorithmic attention work: (query, allowed key) pairs summed over texts.
+double attention_pairs(const int32_t* h_cu, int n_texts, bool is_global, int w) {
+    double pairs = 0;
+    for (int j = 0; j < n_texts; ++j) {
+        const long long L = h_cu[j + 1] - h_cu[j];
+        if (is_global) {
+            pairs += (double)L * (double)L;
+            continue;
+        }
+        for (long long i = 0; i < L; ++i) pairs += (double)(std::min(L - 1, i + w) - std::max(0LL, i - w) + 1);
+    }
+    return pairs;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// profiling
+// ---------------------------------------------------------------------------
+int prof_begin(tee_ctx* c, cudaStream_t s, int kclass, double flops, double bytes) {
+    if (!c->profiling) return -1;
+    if (c->prof_used == c->prof_slots.size()) {
+        ProfileSlot slot{};
+        if (cudaEventCreate(&slot.start) != cudaSuccess) return -1;
+        if (cudaEventCreate(&slot.stop) != cudaSuccess) {
+            cudaEventDestroy(slot.start);
+            return -1;
+        }
+        c->prof_slots.push_back(slot);
+    }
+    ProfileSlot& slot = c->prof_slots[c->prof_used];
+    slot.kclass = kclass;
+    slot.flops = flops;
+    slot.bytes = bytes;
+    cudaEventRecord(slot.start, s);
+    return (int)c->prof_used++;
+}
+
+void prof_end(tee_ctx* c, cudaStream_t s, int slot) {
+    if (slot >= 0) cudaEventRecord(c->prof_slots[slot].stop, s);
+}
+
+#define LAUNCH(kclass, flops, bytes, expr)                                    \
+    do {                                                                      \
+        int _slot = prof_begin(ctx, s, (kclass), (flops), (bytes));           \
+        cudaError_t _e = (expr);                                              \
+        prof_end(ctx, s, _slot);                                              \
+        if (_e != cudaSuccess) return cuda_fail(ctx, _e, #expr);              \
+    } while (0)
+
+// ---------------------------------------------------------------------------
+// steps (shared by the pass and the per-step entry points)
+// ---------------------------------------------------------------------------
+namespace {
+
+int step_layernorm(tee_ctx* ctx, int layer, int which, const float* x, void* y, int T, cudaStream_t s) {
+    const tee_config& g = ctx->cfg;
+    const float* gamma = which == TEE_LN_ATTN ? ctx->layers[layer].ln_attn : ctx->layers[layer].ln_mlp;
+    const double bytes = (double)T * g.hidden * (4 + act_size(ctx)) + g.hidden * 4.0;
+    LAUNCH(TEE_K_LAYERNORM, 0, bytes,
+           launch_layernorm(x, gamma, y, act_is_bf16(ctx), T, g.hidden, g.ln_eps, s));
+    return TEE_OK;
+}
+
+// A (ACT [T*K]) times weight `which` of `layer`; epi 0 stores into C (ACT), epi 1 adds into float C.
+int step_linear(tee_ctx* ctx, int layer, int which, const void* A, void* C, int T, int epi, int tc_epi,
+                const int32_t* pos, cudaStream_t s) {
+    const tee_config& g = ctx->cfg;
+    int N, K;
+    wshape(g, which, &N, &K);
+    const LayerWeights& L = ctx->layers[layer];
+    const double flops = 2.0 * T * N * K;
+    if (g.dtype == TEE_W8A8) {
+        LAUNCH(TEE_K_QUANT, 0, (double)T * K * 5 + T * 4.0,
+               launch_quant_rows7((const float*)A, T, K, ctx->qa, ctx->qs, s));
+        LAUNCH(TEE_K_GEMM, flops, (double)T * K + (double)N * K + (double)T * N * 4 * (epi ? 2 : 1),
+               launch_gemm_w8a8(ctx->qa, ctx->qs, (const int8_t*)L.w[which], L.wd[which], (float*)C, nullptr, T, N,
+                                K, epi, s));
+        return TEE_OK;
+    }
+    if (g.dtype == TEE_BF16) {
+        const int is_g = layer_is_global(ctx, layer);
+        GemmTcArgs a{};
+        a.A = A;
+        a.W = L.w[which];
+        a.C = C;
+        a.M = T;
+        a.N = N;
+        a.K = K;
+        a.epi = tc_epi;
+        a.pos = pos;
+        a.rope_cos = ctx->rope_cos[is_g ? 0 : 1];
+        a.rope_sin = ctx->rope_sin[is_g ? 0 : 1];
+        a.hidden = g.hidden;
+        a.status = ctx->d_status;
+        const double out_b = tc_epi == GEMM_EPI_GEGLU ? (double)T * (N / 2) * 2
+                            : (tc_epi == GEMM_EPI_ADD_F32 ? (double)T * N * 8 : (double)T * N * 2);
+        LAUNCH(TEE_K_GEMM, flops, (double)T * K * 2 + (double)N * K * 2 + out_b, launch_gemm_tc(a, s));
+        return TEE_OK;
+    }
+    LAUNCH(TEE_K_GEMM, flops, (double)T * K * 4 + (double)N * K * 4 + (double)T * N * 4 * (epi ? 2 : 1),
+           launch_gemm_simt(A, L.w[which], C, false, T, N, K, epi, s));
+    return TEE_OK;
+}
+
+int step_qkv(tee_ctx* ctx, int layer, const void* y, const int32_t* pos, void* qkv, int T, cudaStream_t s) {
+    const tee_config& g = ctx->cfg;
+    if (g.dtype == TEE_BF16) return step_linear(ctx, layer, TEE_W_QKV, y, qkv, T, 0, GEMM_EPI_ROPE_BF16, pos, s);
+    int rc = step_linear(ctx, layer, TEE_W_QKV, y, qkv, T, 0, 0, pos, s);
+    if (rc) return rc;
+    const int b = layer_is_global(ctx, layer) ? 0 : 1;
+    LAUNCH(TEE_K_ELEMENTWISE, 0, (double)T * 2 * g.hidden * act_size(ctx) * 2,
+           launch_rope(qkv, act_is_bf16(ctx), pos, ctx->rope_cos[b], ctx->rope_sin[b], T, g.hidden, g.n_heads, s));
+    return TEE_OK;
+}
+
+int step_attention(tee_ctx* ctx, int layer, const void* qkv, const int32_t* d_cu, const int32_t* h_cu, int n_texts,
+                   int T, void* o, cudaStream_t s) {
+    const tee_config& g = ctx->cfg;
+    const bool is_g = layer_is_global(ctx, layer);
+    const double pairs = ctx->profiling ? attention_pairs(h_cu, n_texts, is_g, g.window) : 0.0;
+    const double flops = 4.0 * g.head_dim * g.n_heads * pairs;
+    const double bytes = (double)T * g.hidden * act_size(ctx) * 4;
+    LAUNCH(TEE_K_ATTENTION, flops, bytes,
+           launch_attention_simple(qkv, act_is_bf16(ctx), d_cu, n_texts, T, g.hidden, g.n_heads, is_g, g.window, o, s));
+    return TEE_OK;
+}
+
+int step_ffn_in(tee_ctx* ctx, int layer, const void* y, void* z, int T, cudaStream_t s) {
+    const tee_config& g = ctx->cfg;
+    if (g.dtype == TEE_BF16) return step_linear(ctx, layer, TEE_W_FFN_IN, y, z, T, 0, GEMM_EPI_GEGLU, nullptr, s);
+    int rc = step_linear(ctx, layer, TEE_W_FFN_IN, y, ctx->u, T, 0, 0, nullptr, s);
+    if (rc) return rc;
+    LAUNCH(TEE_K_ELEMENTWISE, 0, (double)T * 3 * g.intermediate * act_size(ctx),
+           launch_geglu(ctx->u, z, act_is_bf16(ctx), T, g.intermediate, s));
+    return TEE_OK;
+}
+
+int step_pool(tee_ctx* ctx, const float* x, const int32_t* d_cu, int n_texts, int T, float* out, cudaStream_t s) {
+    const tee_config& g = ctx->cfg;
+    LAUNCH(TEE_K_POOL, 0, (double)T * g.hidden * 4 + (double)n_texts * g.hidden * 4,
+           launch_pool_l2(x, d_cu, n_texts, g.hidden, out, s));
+    return TEE_OK;
+}
+
+int run_pass(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int T,
+             float* d_out, cudaStream_t s) {
+    const tee_config& g = ctx->cfg;
+    LAUNCH(TEE_K_EMBED, 0, (double)T * 4 * 2, launch_positions(d_cu, n_texts, T, ctx->d_pos, s));
+    LAUNCH(TEE_K_EMBED, 0, (double)T * g.hidden * (4.0 + (act_is_bf16(ctx) ? 2 : 4)) + T * 4.0,
+           launch_embed(ctx->emb, act_is_bf16(ctx), d_ids, T, g.hidden, g.vocab, ctx->x, ctx->d_status, s));
+    int rc;
+    for (int l = 0; l < g.n_layers; ++l) {
+        if ((rc = step_layernorm(ctx, l, TEE_LN_ATTN, ctx->x, ctx->y, T, s))) return rc;
+        if ((rc = step_qkv(ctx, l, ctx->y, ctx->d_pos, ctx->qkv, T, s))) return rc;
+        if ((rc = step_attention(ctx, l, ctx->qkv, d_cu, h_cu, n_texts, T, ctx->o, s))) return rc;
+        if ((rc = step_linear(ctx, l, TEE_W_OUT, ctx->o, ctx->x, T, 1, GEMM_EPI_ADD_F32, nullptr, s))) return rc;
+        if ((rc = step_layernorm(ctx, l, TEE_LN_MLP, ctx->x, ctx->y, T, s))) return rc;
+        if ((rc = step_ffn_in(ctx, l, ctx->y, ctx->z, T, s))) return rc;
+        if ((rc = step_linear(ctx, l, TEE_W_FFN_OUT, ctx->z, ctx->x, T, 1, GEMM_EPI_ADD_F32, nullptr, s))) return rc;
+    }
+    return step_pool(ctx, ctx->x, d_cu, n_texts, T, d_out, s);
+}
+
+int check_ready(tee_ctx* ctx) {
+    if (!ctx) return TEE_EINVAL;
+    if (!ctx->loaded) return fail(ctx, TEE_ENOTLOADED, "weights are not loaded");
+    return TEE_OK;
+}
+
+int check_layer(tee_ctx* ctx, int layer) {
+    if (layer < 0 || layer >= ctx->cfg.n_layers) return fail(ctx, TEE_EINVAL, "layer %d out of range", layer);
+    return TEE_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// public C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+int tee_create(const tee_config* cfg, int device, tee_ctx** out) {
+    if (!out) return fail(nullptr, TEE_EINVAL, "out is NULL");
+    *out = nullptr;
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    tee_ctx* ctx = new (std::nothrow) tee_ctx();
+    if (!ctx) return fail(nullptr, TEE_ENOMEM, "host allocation failed");
+    ctx->cfg = *cfg;
+    ctx->device = device;
+    auto bail = [&](int code) {
+        g_create_error = ctx->err;
+        tee_destroy(ctx);
+        return code;
+    };
+    cudaError_t e = cudaSetDevice(device);
+    if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaSetDevice"));
+    ctx->ws_bytes = carve_workspace(ctx, nullptr);
+    e = cudaMalloc(&ctx->ws_arena, ctx->ws_bytes);
+    if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaMalloc(workspace)"));
+    carve_workspace(ctx, ctx->ws_arena);
+    e = cudaMemset(ctx->d_status, 0, 4 * sizeof(unsigned int));
+    if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaMemset(status)"));
+    if ((rc = build_rope_tables(ctx))) return bail(rc);
+    e = cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaStreamCreate"));
+    memset(ctx->prof_acc, 0, sizeof ctx->prof_acc);
+    *out = ctx;
+    return TEE_OK;
+}
+
+int tee_load_weights(tee_ctx* ctx, const tee_weights* w) {
+    if (!ctx) return TEE_EINVAL;
+    const tee_config& g = ctx->cfg;
+    if (!w || !w->tok_emb || !w->ln_attn || !w->wqkv || !w->wo || !w->ln_mlp || !w->wi || !w->wo_ffn)
+        return fail(ctx, TEE_EINVAL, "weights struct has NULL members");
+    for (int l = 0; l < g.n_layers; ++l)
+        if (!w->ln_attn[l] || !w->wqkv[l] || !w->wo[l] || !w->ln_mlp[l] || !w->wi[l] || !w->wo_ffn[l])
+            return fail(ctx, TEE_EINVAL, "layer %d has a NULL weight pointer", l);
+    CK(cudaSetDevice(ctx->device));
+    ctx->loaded = false;
+    if (ctx->weight_arena) {
+        CK(cudaFree(ctx->weight_arena));
+        ctx->weight_arena = nullptr;
+    }
+    ctx->weight_bytes = carve_weights(ctx, nullptr);
+    CK(cudaMalloc(&ctx->weight_arena, ctx->weight_bytes));
+    carve_weights(ctx, ctx->weight_arena);
+
+    const size_t H = g.hidden, V = g.vocab;
+    size_t stage_elems = std::max(V * H, (size_t)2 * g.intermediate * H);
+    float* stage = nullptr;
+    if (g.dtype != TEE_F32) CK(cudaMalloc(&stage, stage_elems * sizeof(float)));
+    cudaStream_t s = ctx->stream;
+    int rc = TEE_OK;
+    auto put = [&](void* dst, const float* src, size_t n, int kind, int N, int K, float* dscale) -> int {
+        // kind 0: fp32 copy; 1: bf16 convert; 2: int8 block quantise
+        if (kind == 0) {
+            CK(cudaMemcpy(dst, src, n * sizeof(float), cudaMemcpyHostToDevice));
+            return TEE_OK;
+        }
+        CK(cudaMemcpyAsync(stage, src, n * sizeof(float), cudaMemcpyHostToDevice, s));
+        if (kind == 1) CK(launch_convert_f32_bf16(stage, (bf16*)dst, n, s));
+        else CK(launch_quant_weight_blocks(stage, (int8_t*)dst, dscale, N, K, s));
+        CK(cudaStreamSynchronize(s));
+        return TEE_OK;
+    };
+    const int lin_kind = g.dtype == TEE_F32 ? 0 : (g.dtype == TEE_BF16 ? 1 : 2);
+    const int emb_kind = g.dtype == TEE_BF16 ? 1 : 0;
+    if ((rc = put(ctx->emb, w->tok_emb, V * H, emb_kind, 0, 0, nullptr))) goto done;
+    for (int l = 0; l < g.n_layers && rc == TEE_OK; ++l) {
+        LayerWeights& L = ctx->layers[l];
+        const float* ln_a = w->ln_attn[l];
+        const float* ln_m = w->ln_mlp[l];
+        // LayerNorm gains are stored as fp32 in every variant; the bf16 variant
+        // keeps their bf16-rounded values.
+        if (g.dtype == TEE_BF16) {
+            std::vector<float> tmp(H);
+            for (int which = 0; which < 2 && rc == TEE_OK; ++which) {
+                const float* src = which ? ln_m : ln_a;
+                for (size_t i = 0; i < H; ++i) {
+                    uint32_t u;
+                    memcpy(&u, &src[i], 4);
+                    u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+                    memcpy(&tmp[i], &u, 4);
+                }
+                rc = put(which ? L.ln_mlp : L.ln_attn, tmp.data(), H, 0, 0, 0, nullptr);
+            }
+        } else {
+            if ((rc = put(L.ln_attn, ln_a, H, 0, 0, 0, nullptr))) break;
+            if ((rc = put(L.ln_mlp, ln_m, H, 0, 0, 0, nullptr))) break;
+        }
+        const float* srcs[4] = {w->wqkv[l], w->wo[l], w->wi[l], w->wo_ffn[l]};
+        for (int which = 0; which < 4 && rc == TEE_OK; ++which) {
+            int N, K;
+            wshape(g, which, &N, &K);
+            const float* src = srcs[which];
+            std::vector<float> perm;
+            if (g.dtype == TEE_BF16 && which == TEE_W_FFN_IN) {
+                // the tensor-core GEMM fuses the GeGLU gate: each 256-row tile holds
+                // 128 GELU-input rows followed by the 128 matching gate rows
+                perm.resize((size_t)N * K);
+                for (int r = 0; r < N; ++r)
+                    memcpy(&perm[(size_t)r * K], src + (size_t)geglu_source_row(r, g.intermediate) * K,
+                           (size_t)K * sizeof(float));
+                src = perm.data();
+            }
+            rc = put(L.w[which], src, (size_t)N * K, lin_kind, N, K, L.wd[which]);
+        }
+    }
+done:
+    if (stage) cudaFree(stage);
+    if (rc) return rc;
+    ctx->loaded = true;
+    return TEE_OK;
+}
+
+int tee_encode(tee_ctx* ctx, const int32_t* token_ids, const int32_t* cu_seqlens, int n_texts, float* out) {
+    int rc = check_ready(ctx);
+    if (rc) return rc;
+    if (!token_ids || !out) return fail(ctx, TEE_EINVAL, "token_ids / out is NULL");
+    int T = 0;
+    if ((rc = check_cu(ctx, cu_seqlens, n_texts, &T))) return rc;
+    for (int t = 0; t < T; ++t)
+        if (token_ids[t] < 0 || token_ids[t] >= ctx->cfg.vocab)
+            return fail(ctx, TEE_EINVAL, "token id %d at position %d is outside [0, %d)", token_ids[t], t,
+                        ctx->cfg.vocab);
+    CK(cudaSetDevice(ctx->device));
+    cudaStream_t s = ctx->stream;
+    CK(cudaMemcpyAsync(ctx->d_ids, token_ids, (size_t)T * 4, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(ctx->d_cu, cu_seqlens, (size_t)(n_texts + 1) * 4, cudaMemcpyHostToDevice, s));
+    if ((rc = run_pass(ctx, ctx->d_ids, ctx->d_cu, cu_seqlens, n_texts, T, ctx->out, s))) return rc;
+    CK(cudaMemcpyAsync(out, ctx->out, (size_t)n_texts * ctx->cfg.hidden * 4, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    return TEE_OK;
+}
+
+int tee_encode_device(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu, int n_texts,
+                      float* d_out, void* stream) {
+    int rc = check_ready(ctx);
+    if (rc) return rc;
+    if (!d_ids || !d_cu || !d_out) return fail(ctx, TEE_EINVAL, "device pointer is NULL");
+    int T = 0;
+    if ((rc = check_cu(ctx, h_cu, n_texts, &T))) return rc;
+    CK(cudaSetDevice(ctx->device));
+    return run_pass(ctx, d_ids, d_cu, h_cu, n_texts, T, d_out, (cudaStream_t)stream);
+}
+
+const char* tee_last_error(const tee_ctx* ctx) { return ctx ? ctx->err.c_str() : g_create_error.c_str(); }
+
+void tee_destroy(tee_ctx* ctx) {
+    if (!ctx) return;
+    cudaSetDevice(ctx->device);
+    if (ctx->stream) cudaStreamSynchronize(ctx->stream);
+    for (auto& sl : ctx->prof_slots) {
+        cudaEventDestroy(sl.start);
+        cudaEventDestroy(sl.stop);
+    }
+    if (ctx->weight_arena) cudaFree(ctx->weight_arena);
+    if (ctx->ws_arena) cudaFree(ctx->ws_arena);
+    if (ctx->stream) cudaStreamDestroy(ctx->stream);
+    delete ctx;
+}
+
+int tee_profile_enable(tee_ctx* ctx, int on) {
+    if (!ctx) return TEE_EINVAL;
+    ctx->profiling = on != 0;
+    ctx->prof_used = 0;
+    memset(ctx->prof_acc, 0, sizeof ctx->prof_acc);
+    return TEE_OK;
+}
+
+int tee_profile_read(tee_ctx* ctx, tee_kernel_stat* stats) {
+    if (!ctx || !stats) return TEE_EINVAL;
+    CK(cudaSetDevice(ctx->device));
+    for (size_t i = 0; i < ctx->prof_used; ++i) {
+        ProfileSlot& sl = ctx->prof_slots[i];
+        CK(cudaEventSynchronize(sl.stop));
+        float ms = 0.f;
+        CK(cudaEventElapsedTime(&ms, sl.start, sl.stop));
+        tee_kernel_stat& a = ctx->prof_acc[sl.kclass];
+        a.launches += 1;
+        a.total_ms += ms;
+        a.flops += sl.flops;
+        a.bytes += sl.bytes;
+    }
+    ctx->prof_used = 0;
+    memcpy(stats, ctx->prof_acc, sizeof ctx->prof_acc);
+    return TEE_OK;
+}
+
+// ---- per-step entry points ------------------------------------------------
+
+int tee_op_embed(tee_ctx* ctx, const int32_t* d_ids, int T, float* d_x, void* stream) {
+    int rc = check_ready(ctx);
+    if (rc) return rc;
+    if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    cudaStream_t s = (cudaStream_t)stream;
+    LAUNCH(TEE_K_EMBED, 0, 0,
+           launch_embed(ctx->emb, act_is_bf16(ctx), d_ids, T, ctx->cfg.hidden, ctx->cfg.vocab, d_x, ctx->d_status, s));
+    return TEE_OK;
+}
+
+int tee_op_positions(tee_ctx* ctx, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int32_t* d_pos,
+                     void* stream) {
+    if (!ctx) return TEE_EINVAL;
+    int T = 0, rc = check_cu(ctx, h_cu, n_texts, &T);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    LAUNCH(TEE_K_EMBED, 0, 0, launch_positions(d_cu, n_texts, T, d_pos, s));
+    return TEE_OK;
+}
+
+int tee_op_layernorm(tee_ctx* ctx, int layer, int which, const float* d_x, void* d_y, int T, void* stream) {
+    int rc = check_ready(ctx);
+    if (rc || (rc = check_layer(ctx, layer))) return rc;
+    if (which != TEE_LN_ATTN && which != TEE_LN_MLP) return fail(ctx, TEE_EINVAL, "bad LayerNorm selector");
+    if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    return step_layernorm(ctx, layer, which, d_x, d_y, T, (cudaStream_t)stream);
+}
+
+int tee_op_qkv(tee_ctx* ctx, int layer, const void* d_y, const int32_t* d_pos, void* d_qkv, int T, void* stream) {
+    int rc = check_ready(ctx);
+    if (rc || (rc = check_layer(ctx, layer))) return rc;
+    if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    return step_qkv(ctx, layer, d_y, d_pos, d_qkv, T, (cudaStream_t)stream);
+}
+
+int tee_op_attention(tee_ctx* ctx, int layer, const void* d_qkv, const int32_t* d_cu, const int32_t* h_cu,
+                     int n_texts, void* d_o, void* stream) {
+    int rc = check_ready(ctx);
+    if (rc || (rc = check_layer(ctx, layer))) return rc;
+    int T = 0;
+    if ((rc = check_cu(ctx, h_cu, n_texts, &T))) return rc;
+    return step_attention(ctx, layer, d_qkv, d_cu, h_cu, n_texts, T, d_o, (cudaStream_t)stream);
+}
+
+int tee_op_out_proj(tee_ctx* ctx, int layer, const void* d_o, float* d_x, int T, void* stream) {
+    int rc = check_ready(ctx);
+    if (rc || (rc = check_layer(ctx, layer))) return rc;
+    if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    return step_linear(ctx, layer, TEE_W_OUT, d_o, d_x, T, 1, GEMM_EPI_ADD_F32, nullptr, (cudaStream_t)stream);
+}
+
+int tee_op_ffn_in(tee_ctx* ctx, int layer, const void* d_y, void* d_z, int T, void* stream) {
+    int rc = check_ready(ctx);
+    if (rc || (rc = check_layer(ctx, layer))) return rc;
+    if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    return step_ffn_in(ctx, layer, d_y, d_z, T, (cudaStream_t)stream);
+}
+
+int tee_op_ffn_out(tee_ctx* ctx, int layer, const void* d_z, float* d_x, int T, void* stream) {
+    int rc = check_ready(ctx);
+    if (rc || (rc = check_layer(ctx, layer))) return rc;
+    if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    return step_linear(ctx, layer, TEE_W_FFN_OUT, d_z, d_x, T, 1, GEMM_EPI_ADD_F32, nullptr, (cudaStream_t)stream);
+}
+
+int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts,
+                   float* d_out, void* stream) {
+    if (!ctx) return TEE_EINVAL;
+    int T = 0, rc = check_cu(ctx, h_cu, n_texts, &T);
+    if (rc) return rc;
+    return step_pool(ctx, d_x, d_cu, n_texts, T, d_out, (cudaStream_t)stream);
+}
+
+int tee_op_quant_rows7(tee_ctx* ctx, const float* d_x, int M, int K, int8_t* d_q, float* d_s, void* stream) {
+    if (!ctx) return TEE_EINVAL;
+    if (M < 0 || K < 1) return fail(ctx, TEE_EINVAL, "bad M/K");
+    cudaStream_t s = (cudaStream_t)stream;
+    LAUNCH(TEE_K_QUANT, 0, 0, launch_quant_rows7(d_x, M, K, d_q, d_s, s));
+    return TEE_OK;
+}
+
+int tee_op_w8a8_partials(tee_ctx* ctx, int layer, int which, const int8_t* d_q, int M, int32_t* d_partials,
+                         void* stream) {
+    int rc = check_ready(ctx);
+    if (rc || (rc = check_layer(ctx, layer))) return rc;
+    if (ctx->cfg.dtype != TEE_W8A8) return fail(ctx, TEE_EINVAL, "context is not W8A8");
+    int N, K;
+    if (wshape(ctx->cfg, which, &N, &K)) return fail(ctx, TEE_EINVAL, "bad projection selector");
+    if (M < 0) return fail(ctx, TEE_EINVAL, "bad M");
+    const LayerWeights& L = ctx->layers[layer];
+    cudaStream_t s = (cudaStream_t)stream;
+    LAUNCH(TEE_K_GEMM, 0, 0,
+           launch_gemm_w8a8(d_q, nullptr, (const int8_t*)L.w[which], L.wd[which], nullptr, d_partials, M, N, K, 0, s));
+    return TEE_OK;
+}
+
+int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d) {
+    int rc = check_ready(ctx);
+    if (rc || (rc = check_layer(ctx, layer))) return rc;
+    if (ctx->cfg.dtype != TEE_W8A8) return fail(ctx, TEE_EINVAL, "context is not W8A8");
+    int N, K;
+    if (wshape(ctx->cfg, which, &N, &K)) return fail(ctx, TEE_EINVAL, "bad projection selector");
+    if (!h_q || !h_d) return fail(ctx, TEE_EINVAL, "NULL output");
+    CK(cudaSetDevice(ctx->device));
+    CK(cudaMemcpy(h_q, ctx->layers[layer].w[which], (size_t)N * K, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(h_d, ctx->layers[layer].wd[which], (size_t)N * K / 32 * 4, cudaMemcpyDeviceToHost));
+    return TEE_OK;
+}
+
+int tee_device_status(tee_ctx* ctx) {
+    if (!ctx) return TEE_EINVAL;
+    CK(cudaSetDevice(ctx->device));
+    unsigned int st = 0;
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(&st, ctx->d_status, 4, cudaMemcpyDeviceToHost));
+    CK(cudaMemset(ctx->d_status, 0, 4));
+    if (st & TEE_STATUS_TIMEOUT) return fail(ctx, TEE_ETIMEOUT, "a device-side wait gave up (status 0x%x)", st);
+    if (st & TEE_STATUS_BAD_ID) return fail(ctx, TEE_EINVAL, "a token id was outside [0, vocab)");
+    return TEE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <string>
+#include <vector>
+
+#include "tee.h"
+#include "tee_ops.h"
+
+typedef __nv_bfloat16 bf16;
+
+// Device status word bits (ctx->d_status).
+#define TEE_STATUS_BAD_ID   1u
+#define TEE_STATUS_TIMEOUT  2u
+
+struct LayerWeights {
+    float* ln_attn = nullptr;      // fp32 [H]
+    float* ln_mlp = nullptr;       // fp32 [H]
+    void* w[4] = {nullptr, nullptr, nullptr, nullptr};      // fp32 / bf16 / int8, [N*K]
+    float* wd[4] = {nullptr, nullptr, nullptr, nullptr};    // W8A8 block scales [N*K/32]
+};
+
+struct ProfileSlot {
+    cudaEvent_t start, stop;
+    int kclass;
+    double flops, bytes;
+};
+
+struct tee_ctx {
+    tee_config cfg{};
+    int device = 0;
+    bool loaded = false;
+    std::string err;
+
+    // weights
+    void* weight_arena = nullptr;
+    size_t weight_bytes = 0;
+    void* emb = nullptr;                // fp32 [V*H] (F32, W8A8) or bf16 (BF16)
+    std::vector<LayerWeights> layers;
+
+    // RoPE tables, index 0 = global base, 1 = window base: float [max_tokens][head_dim/2]
+    float* rope_cos[2] = {nullptr, nullptr};
+    float* rope_sin[2] = {nullptr, nullptr};
+
+    // workspace (sized by max_tokens / max_texts)
+    void* ws_arena = nullptr;
+    size_t ws_bytes = 0;
+    int32_t* d_ids = nullptr;
+    int32_t* d_cu = nullptr;
+    int32_t* d_pos = nullptr;
+    float* x = nullptr;                 // residual stream, float [T*H]
+    void* y = nullptr;                  // LayerNorm output, ACT [T*H]
+    void* qkv = nullptr;                // ACT [T*3H]
+    void* o = nullptr;                  // attention output, ACT [T*H]
+    void* u = nullptr;                  // Wi output, ACT [T*2I] (unfused GeGLU only)
+    void* z = nullptr;                  // GeGLU output, ACT [T*I]
+    float* out = nullptr;               // float [max_texts*H]
+    int8_t* qa = nullptr;               // W8A8 activation codes [T*max(H,I)]
+    float* qs = nullptr;                // W8A8 activation scales [T]
+    unsigned int* d_status = nullptr;   // device status word
+
+    cudaStream_t stream = nullptr;      // the context's own stream (tee_encode)
+    std::vector<int32_t> h_cu_scratch;
+
+    // profiling
+    bool profiling = false;
+    std::vector<ProfileSlot> prof_slots;
+    size_t prof_used = 0;
+    tee_kernel_stat prof_acc[TEE_K_COUNT];
+};
+
+// ---- helpers ------------------------------------------------------------
+inline bool act_is_bf16(const tee_ctx* c) { return c->cfg.dtype == TEE_BF16; }
+inline size_t act_size(const tee_ctx* c) { return act_is_bf16(c) ? 2 : 4; }
+inline int layer_is_global(const tee_ctx* c, int l) { return (l % c->cfg.global_every) == 0; }
+
+// Profiling brackets: record events around one launch when profiling is on.
+int prof_begin(tee_ctx* c, cudaStream_t s, int kclass, double flops, double bytes);
+void prof_end(tee_ctx* c, cudaStream_t s, int slot);
+
+// ---- kernel launchers (each returns cudaGetLastError()) -------------------
+cudaError_t launch_convert_f32_bf16(const float* src, bf16* dst, size_t n, cudaStream_t s);
+cudaError_t launch_embed(const void* emb, bool emb_bf16, const int32_t* ids, int T, int H, int V, float* x,
+                         unsigned int* status, cudaStream_t s);
+cudaError_t launch_positions(const int32_t* cu, int n_texts, int T, int32_t* pos, cudaStream_t s);
+cudaError_t launch_layernorm(const float* x, const float* gamma, void* y, bool y_bf16, int T, int H, float eps,
+                             cudaStream_t s);
+cudaError_t launch_rope(void* qkv, bool bf16_act, const int32_t* pos, const float* cos_t, const float* sin_t, int T,
+                        int H, int n_heads, cudaStream_t s);
+cudaError_t launch_geglu(const void* u, void* z, bool bf16_act, int T, int I, cudaStream_t s);
+cudaError_t launch_pool_l2(const float* x, const int32_t* cu, int n_texts, int H, float* out, cudaStream_t s);
+cudaError_t launch_attention_simple(const void* qkv, bool bf16_act, const int32_t* cu, int n_texts, int T, int H,
+                                    int n_heads, bool is_global, int window, void* o, cudaStream_t s);
+
+// SIMT GEMM, C = A W^T.  epi 0: store C in A's type; epi 1: add into float C.
+cudaError_t launch_gemm_simt(const void* A, const void* W, void* C, bool bf16_in, int M, int N, int K, int epi,
+                             cudaStream_t s);
+
+// W8A8
+cudaError_t launch_quant_weight_blocks(const float* w, int8_t* q, float* d, int N, int K, cudaStream_t s);
+cudaError_t launch_quant_rows7(const float* x, int M, int K, int8_t* q, float* scale, cudaStream_t s);
+// y = s_m * sum_b d[n,b] * I[m,n,b]; epi 0 store float, 1 add into float; partials (optional) int32 [M][N][K/32]
+cudaError_t launch_gemm_w8a8(const int8_t* qa, const float* sa, const int8_t* qw, const float* dw, float* C,
+                             int32_t* partials, int M, int N, int K, int epi, cudaStream_t s);
