@@ -114,6 +114,8 @@ size_t carve_workspace(tee_ctx* c, void* base) {
         c->rope_sin[b] = cv.take<float>(T * 32);
     }
     c->d_status = cv.take<unsigned int>(4);
+    c->max_items = (int)(T / 128 + g.max_texts + 1);
+    for (int b = 0; b < 2; ++b) c->d_items[b] = cv.take<int4>(c->max_items);
     return cv.off;
 }
 
@@ -187,6 +189,34 @@ double attention_pairs(const int32_t* h_cu, int n_texts, bool is_global, int w) 
         for (long long i = 0; i < L; ++i) pairs += (double)(std::min(L - 1, i + w) - std::max(0LL, i - w) + 1);
     }
     return pairs;
+}
+
+// Attention work items of one pass: one per (text, 128-query tile), with the
+// key range the queries of that tile may see.  List 0 (global layers): the
+// whole text, longest texts first so the heavy CTAs start early; list 1
+// (window layers): the window around the tile, clipped to the text.
+int prepare_attention_items(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cudaStream_t s) {
+    const int w = ctx->cfg.window;
+    for (int b = 0; b < 2; ++b) ctx->h_items[b].clear();
+    for (int j = 0; j < n_texts; ++j) {
+        const int s0 = h_cu[j], s1 = h_cu[j + 1];
+        for (int q0 = s0; q0 < s1; q0 += 128) {
+            const int ql = std::min(128, s1 - q0);
+            ctx->h_items[0].push_back(make_int4(q0, ql, s0, s1));
+            ctx->h_items[1].push_back(make_int4(q0, ql, std::max(s0, q0 - w), std::min(s1, q0 + ql + w)));
+        }
+    }
+    std::stable_sort(ctx->h_items[0].begin(), ctx->h_items[0].end(), [](const int4& a, const int4& b) {
+        const long long ca = (long long)a.y * (a.w - a.z), cb = (long long)b.y * (b.w - b.z);
+        return ca > cb;
+    });
+    for (int b = 0; b < 2; ++b) {
+        if ((int)ctx->h_items[b].size() > ctx->max_items)
+            return fail(ctx, TEE_ETOOLONG, "too many attention work items");
+        CK(cudaMemcpyAsync(ctx->d_items[b], ctx->h_items[b].data(), ctx->h_items[b].size() * sizeof(int4),
+                           cudaMemcpyHostToDevice, s));
+    }
+    return TEE_OK;
 }
 
 }  // namespace
@@ -298,6 +328,13 @@ int step_attention(tee_ctx* ctx, int layer, const void* qkv, const int32_t* d_cu
     const double pairs = ctx->profiling ? attention_pairs(h_cu, n_texts, is_g, g.window) : 0.0;
     const double flops = 4.0 * g.head_dim * g.n_heads * pairs;
     const double bytes = (double)T * g.hidden * act_size(ctx) * 4;
+    if (g.dtype == TEE_BF16) {
+        const int b = is_g ? 0 : 1;
+        LAUNCH(TEE_K_ATTENTION, flops, bytes,
+               launch_attention_tc(qkv, T, g.hidden, g.n_heads, ctx->d_items[b], (int)ctx->h_items[b].size(), is_g,
+                                   g.window, o, ctx->d_status, s));
+        return TEE_OK;
+    }
     LAUNCH(TEE_K_ATTENTION, flops, bytes,
            launch_attention_simple(qkv, act_is_bf16(ctx), d_cu, n_texts, T, g.hidden, g.n_heads, is_g, g.window, o, s));
     return TEE_OK;
@@ -323,10 +360,11 @@ int step_pool(tee_ctx* ctx, const float* x, const int32_t* d_cu, int n_texts, in
 int run_pass(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int T,
              float* d_out, cudaStream_t s) {
     const tee_config& g = ctx->cfg;
+    int rc;
+    if (g.dtype == TEE_BF16 && (rc = prepare_attention_items(ctx, h_cu, n_texts, s))) return rc;
     LAUNCH(TEE_K_EMBED, 0, (double)T * 4 * 2, launch_positions(d_cu, n_texts, T, ctx->d_pos, s));
     LAUNCH(TEE_K_EMBED, 0, (double)T * g.hidden * (4.0 + (act_is_bf16(ctx) ? 2 : 4)) + T * 4.0,
            launch_embed(ctx->emb, act_is_bf16(ctx), d_ids, T, g.hidden, g.vocab, ctx->x, ctx->d_status, s));
-    int rc;
     for (int l = 0; l < g.n_layers; ++l) {
         if ((rc = step_layernorm(ctx, l, TEE_LN_ATTN, ctx->x, ctx->y, T, s))) return rc;
         if ((rc = step_qkv(ctx, l, ctx->y, ctx->d_pos, ctx->qkv, T, s))) return rc;
@@ -590,6 +628,8 @@ int tee_op_attention(tee_ctx* ctx, int layer, const void* d_qkv, const int32_t* 
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     int T = 0;
     if ((rc = check_cu(ctx, h_cu, n_texts, &T))) return rc;
+    if (ctx->cfg.dtype == TEE_BF16 && (rc = prepare_attention_items(ctx, h_cu, n_texts, (cudaStream_t)stream)))
+        return rc;
     return step_attention(ctx, layer, d_qkv, d_cu, h_cu, n_texts, T, d_o, (cudaStream_t)stream);
 }
 

@@ -61,6 +61,9 @@ struct tee_ctx {
     int8_t* qa = nullptr;               // W8A8 activation codes [T*max(H,I)]
     float* qs = nullptr;                // W8A8 activation scales [T]
     unsigned int* d_status = nullptr;   // device status word
+    int4* d_items[2] = {nullptr, nullptr};   // attention work items (global, window layers)
+    int max_items = 0;
+    std::vector<int4> h_items[2];
 
     cudaStream_t stream = nullptr;      // the context's own stream (tee_encode)
     std::vector<int32_t> h_cu_scratch;
@@ -94,6 +97,11 @@ cudaError_t launch_geglu(const void* u, void* z, bool bf16_act, int T, int I, cu
 cudaError_t launch_pool_l2(const float* x, const int32_t* cu, int n_texts, int H, float* out, cudaStream_t s);
 cudaError_t launch_attention_simple(const void* qkv, bool bf16_act, const int32_t* cu, int n_texts, int T, int H,
                                     int n_heads, bool is_global, int window, void* o, cudaStream_t s);
+
+// tcgen05 varlen attention over bf16 qkv [T, 3H]; items {q_start, q_len, k_lo, k_hi} per
+// (text, 128-query tile), one CTA per item and head.
+cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, const int4* d_items, int n_items,
+                                bool is_global, int window, void* o, unsigned int* status, cudaStream_t s);
 
 // SIMT GEMM, C = A W^T.  epi 0: store C in A's type; epi 1: add into float C.
 cudaError_t launch_gemm_simt(const void* A, const void* W, void* C, bool bf16_in, int M, int N, int K, int epi,
