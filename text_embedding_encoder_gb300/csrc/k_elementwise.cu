@@ -160,27 +160,52 @@ __global__ void geglu_kernel(const TA* __restrict__ u, TA* __restrict__ z, int T
     z[idx] = from_f<TA>(gelu_erf(a) * g);
 }
 
-// One block per text: column sums over the text's rows, then L2 scaling.
-__global__ void pool_l2_kernel(const float* __restrict__ x, const int32_t* __restrict__ cu, int H,
-                               float* __restrict__ out) {
+// Pass 1 of mean-pool + L2: one block per chunk of up to POOL_CHUNK rows of one
+// text; thread c4 sums float4 column group c4 over the chunk's rows and writes
+// the partial sum.  chunk_off[j] is the first chunk of text j (chunk_off[n] =
+// total chunks).
+__global__ void pool_partial_kernel(const float* __restrict__ x, const int32_t* __restrict__ cu,
+                                    const int32_t* __restrict__ chunk_off, int n_texts, int H,
+                                    float* __restrict__ partial) {
+    const int chunk = blockIdx.x;
+    const int j = text_of(chunk_off, n_texts, chunk);
+    const int r0 = cu[j] + (chunk - chunk_off[j]) * POOL_CHUNK;
+    const int r1 = min(cu[j + 1], r0 + POOL_CHUNK);
+    for (int c4 = threadIdx.x; c4 < H / 4; c4 += blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = r0; r < r1; ++r) {
+            const float4 v = reinterpret_cast<const float4*>(x + (size_t)r * H)[c4];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        reinterpret_cast<float4*>(partial + (size_t)chunk * H)[c4] = acc;
+    }
+}
+
+// Pass 2: one block per text sums its chunks' partials in chunk order (so the
+// result is deterministic), divides by the length and scales to unit norm
+// (norm floored at 1e-12).  H <= 4 * blockDim.x.
+__global__ void pool_finish_kernel(const float* __restrict__ partial, const int32_t* __restrict__ cu,
+                                   const int32_t* __restrict__ chunk_off, int H, float* __restrict__ out) {
     __shared__ float red[32];
-    int j = blockIdx.x;
-    int t0 = cu[j], t1 = cu[j + 1];
-    float inv_len = 1.0f / (float)(t1 - t0);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};   // H <= 4 * blockDim.x
-    for (int t = t0; t < t1; ++t) {
-        const float* row = x + (size_t)t * H;
+    const int j = blockIdx.x;
+    const int k0 = chunk_off[j], k1 = chunk_off[j + 1];
+    const float inv_len = 1.0f / (float)(cu[j + 1] - cu[j]);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = k0; k < k1; ++k) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            int c = threadIdx.x + i * blockDim.x;
-            if (c < H) acc[i] += row[c];
+            const int c = threadIdx.x + i * blockDim.x;
+            if (c < H) acc[i] += partial[(size_t)k * H + c];
         }
     }
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         acc[i] *= inv_len;
-        int c = threadIdx.x + i * blockDim.x;
+        const int c = threadIdx.x + i * blockDim.x;
         if (c < H) ss += acc[i] * acc[i];
     }
     ss = warp_sum(ss);
@@ -192,10 +217,10 @@ __global__ void pool_l2_kernel(const float* __restrict__ x, const int32_t* __res
         if (threadIdx.x == 0) red[0] = v;
     }
     __syncthreads();
-    float scale = 1.0f / fmaxf(sqrtf(red[0]), 1e-12f);
+    const float scale = 1.0f / fmaxf(sqrtf(red[0]), 1e-12f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        int c = threadIdx.x + i * blockDim.x;
+        const int c = threadIdx.x + i * blockDim.x;
         if (c < H) out[(size_t)j * H + c] = acc[i] * scale;
     }
 }
@@ -261,8 +286,13 @@ cudaError_t launch_geglu(const void* u, void* z, bool bf16_act, int T, int I, cu
     return cudaGetLastError();
 }
 
-cudaError_t launch_pool_l2(const float* x, const int32_t* cu, int n_texts, int H, float* out, cudaStream_t s) {
+cudaError_t launch_pool_l2(const float* x, const int32_t* cu, const int32_t* chunk_off, int n_texts, int n_chunks,
+                           int H, float* partial, float* out, cudaStream_t s) {
     if (n_texts == 0) return cudaSuccess;
-    pool_l2_kernel<<<n_texts, 256, 0, s>>>(x, cu, H, out);
+    const int threads = H / 4 < 256 ? H / 4 : 256;
+    pool_partial_kernel<<<n_chunks, threads, 0, s>>>(x, cu, chunk_off, n_texts, H, partial);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    pool_finish_kernel<<<n_texts, 256, 0, s>>>(partial, cu, chunk_off, H, out);
     return cudaGetLastError();
 }

@@ -181,13 +181,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
             const int acc = it & 1, use = it >> 1;
-            if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
-            tc_fence_after();
             const int n_t = tile % num_n, m_t = tile / num_n;
             const int gr = m_t * BM + row_local;
             const bool valid = gr < p.M;
             const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
             if constexpr (EPI == GEMM_EPI_STORE_BF16) {
+                if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
+                tc_fence_after();
                 bf16* C = reinterpret_cast<bf16*>(p.C) + (size_t)gr * p.N + n_t * BN;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
@@ -196,16 +196,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (valid) store_bf16x32(C + c * 32, v);
                 }
             } else if constexpr (EPI == GEMM_EPI_ADD_F32) {
+                // the residual chunk is fetched one chunk ahead (the first one
+                // while the tile's MMAs still run) to keep loads in flight
                 float* C = reinterpret_cast<float*>(p.C) + (size_t)gr * p.N + n_t * BN;
+                float4 cur[8], nxt[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    cur[i] = valid ? reinterpret_cast<const float4*>(C)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
+                tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
+                    if (c + 1 < BN / 32) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            nxt[i] = valid ? reinterpret_cast<const float4*>(C + (c + 1) * 32)[i]
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                     float v[32];
                     tmem_ld32(taddr + c * 32, v);
                     if (valid) {
                         float4* d = reinterpret_cast<float4*>(C + c * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            float4 o = d[i];
+                            float4 o = cur[i];
                             o.x += v[4 * i + 0];
                             o.y += v[4 * i + 1];
                             o.z += v[4 * i + 2];
@@ -213,33 +227,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             d[i] = o;
                         }
                     }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
                 }
             } else if constexpr (EPI == GEMM_EPI_ROPE_BF16) {
+                // q and k tiles (columns < 2*hidden; 2*hidden is a multiple of
+                // the tile width) rotate every head with the row's cos/sin,
+                // fetched once per tile before the accumulator is ready
                 bf16* C = reinterpret_cast<bf16*>(p.C) + (size_t)gr * p.N + n_t * BN;
-                const int pos = valid ? p.pos[gr] : 0;
-                const float* cs = p.rope_cos + (size_t)pos * 32;
-                const float* sn = p.rope_sin + (size_t)pos * 32;
+                const bool rope = n_t * BN < 2 * p.hidden;
+                float cs[32], sn[32];
+                if (rope) {
+                    const int pos = valid ? p.pos[gr] : 0;
+                    const float4* c4 = reinterpret_cast<const float4*>(p.rope_cos + (size_t)pos * 32);
+                    const float4* s4 = reinterpret_cast<const float4*>(p.rope_sin + (size_t)pos * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 a = c4[i], b = s4[i];
+                        cs[4 * i] = a.x, cs[4 * i + 1] = a.y, cs[4 * i + 2] = a.z, cs[4 * i + 3] = a.w;
+                        sn[4 * i] = b.x, sn[4 * i + 1] = b.y, sn[4 * i + 2] = b.z, sn[4 * i + 3] = b.w;
+                    }
+                }
+                if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
+                tc_fence_after();
 #pragma unroll 1
                 for (int hh = 0; hh < BN / 64; ++hh) {
                     float lo[32], hi[32];
                     tmem_ld32(taddr + hh * 64, lo);
                     tmem_ld32(taddr + hh * 64 + 32, hi);
-                    if (valid) {
-                        if (n_t * BN + hh * 64 < 2 * p.hidden) {
+                    if (rope) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const float c = cs[j], s = sn[j];
-                                const float a = lo[j] * c - hi[j] * s;
-                                const float b = hi[j] * c + lo[j] * s;
-                                lo[j] = a;
-                                hi[j] = b;
-                            }
+                        for (int j = 0; j < 32; ++j) {
+                            const float a = lo[j] * cs[j] - hi[j] * sn[j];
+                            const float b = hi[j] * cs[j] + lo[j] * sn[j];
+                            lo[j] = a;
+                            hi[j] = b;
                         }
+                    }
+                    if (valid) {
                         store_bf16x32(C + hh * 64, lo);
                         store_bf16x32(C + hh * 64 + 32, hi);
                     }
                 }
             } else {   // GEMM_EPI_GEGLU (BN == 256)
+                if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
+                tc_fence_after();
                 bf16* C = reinterpret_cast<bf16*>(p.C) + (size_t)gr * (p.N / 2) + n_t * (BN / 2);
 #pragma unroll 1
                 for (int c = 0; c < BN / 64; ++c) {

@@ -116,6 +116,9 @@ size_t carve_workspace(tee_ctx* c, void* base) {
     c->d_status = cv.take<unsigned int>(4);
     c->max_items = (int)(T / 128 + g.max_texts + 1);
     for (int b = 0; b < 2; ++b) c->d_items[b] = cv.take<int4>(c->max_items);
+    c->max_chunks = (int)(T / POOL_CHUNK + g.max_texts + 1);
+    c->d_chunk_off = cv.take<int32_t>(g.max_texts + 1);
+    c->pool_partial = cv.take<float>((size_t)c->max_chunks * H);
     return cv.off;
 }
 
@@ -350,10 +353,29 @@ int step_ffn_in(tee_ctx* ctx, int layer, const void* y, void* z, int T, cudaStre
     return TEE_OK;
 }
 
-int step_pool(tee_ctx* ctx, const float* x, const int32_t* d_cu, int n_texts, int T, float* out, cudaStream_t s) {
+// Chunk offsets of the two-pass pool: text j owns ceil(len_j / POOL_CHUNK) chunks.
+int prepare_pool_chunks(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cudaStream_t s) {
+    ctx->h_chunk_off.resize(n_texts + 1);
+    int total = 0;
+    for (int j = 0; j < n_texts; ++j) {
+        ctx->h_chunk_off[j] = total;
+        total += (h_cu[j + 1] - h_cu[j] + POOL_CHUNK - 1) / POOL_CHUNK;
+    }
+    ctx->h_chunk_off[n_texts] = total;
+    if (total > ctx->max_chunks) return fail(ctx, TEE_ETOOLONG, "too many pooling chunks");
+    CK(cudaMemcpyAsync(ctx->d_chunk_off, ctx->h_chunk_off.data(), (n_texts + 1) * sizeof(int32_t),
+                       cudaMemcpyHostToDevice, s));
+    return TEE_OK;
+}
+
+int step_pool(tee_ctx* ctx, const float* x, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int T, float* out,
+              cudaStream_t s) {
     const tee_config& g = ctx->cfg;
+    int rc = prepare_pool_chunks(ctx, h_cu, n_texts, s);
+    if (rc) return rc;
+    const int n_chunks = ctx->h_chunk_off[n_texts];
     LAUNCH(TEE_K_POOL, 0, (double)T * g.hidden * 4 + (double)n_texts * g.hidden * 4,
-           launch_pool_l2(x, d_cu, n_texts, g.hidden, out, s));
+           launch_pool_l2(x, d_cu, ctx->d_chunk_off, n_texts, n_chunks, g.hidden, ctx->pool_partial, out, s));
     return TEE_OK;
 }
 
@@ -374,7 +396,7 @@ int run_pass(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int3
         if ((rc = step_ffn_in(ctx, l, ctx->y, ctx->z, T, s))) return rc;
         if ((rc = step_linear(ctx, l, TEE_W_FFN_OUT, ctx->z, ctx->x, T, 1, GEMM_EPI_ADD_F32, nullptr, s))) return rc;
     }
-    return step_pool(ctx, ctx->x, d_cu, n_texts, T, d_out, s);
+    return step_pool(ctx, ctx->x, d_cu, h_cu, n_texts, T, d_out, s);
 }
 
 int check_ready(tee_ctx* ctx) {
@@ -659,7 +681,7 @@ int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const in
     if (!ctx) return TEE_EINVAL;
     int T = 0, rc = check_cu(ctx, h_cu, n_texts, &T);
     if (rc) return rc;
-    return step_pool(ctx, d_x, d_cu, n_texts, T, d_out, (cudaStream_t)stream);
+    return step_pool(ctx, d_x, d_cu, h_cu, n_texts, T, d_out, (cudaStream_t)stream);
 }
 
 int tee_op_quant_rows7(tee_ctx* ctx, const float* d_x, int M, int K, int8_t* d_q, float* d_s, void* stream) {

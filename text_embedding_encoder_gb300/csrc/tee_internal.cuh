@@ -62,6 +62,10 @@ struct tee_ctx {
     float* qs = nullptr;                // W8A8 activation scales [T]
     unsigned int* d_status = nullptr;   // device status word
     int4* d_items[2] = {nullptr, nullptr};   // attention work items (global, window layers)
+    int32_t* d_chunk_off = nullptr;     // pool: first chunk of each text [max_texts + 1]
+    float* pool_partial = nullptr;      // pool: partial sums [max_chunks * H]
+    int max_chunks = 0;
+    std::vector<int32_t> h_chunk_off;
     int max_items = 0;
     std::vector<int4> h_items[2];
 
@@ -94,7 +98,12 @@ cudaError_t launch_layernorm(const float* x, const float* gamma, void* y, bool y
 cudaError_t launch_rope(void* qkv, bool bf16_act, const int32_t* pos, const float* cos_t, const float* sin_t, int T,
                         int H, int n_heads, cudaStream_t s);
 cudaError_t launch_geglu(const void* u, void* z, bool bf16_act, int T, int I, cudaStream_t s);
-cudaError_t launch_pool_l2(const float* x, const int32_t* cu, int n_texts, int H, float* out, cudaStream_t s);
+// Mean-pool + L2 in two passes: partial column sums of POOL_CHUNK-row chunks
+// (chunk_off[j] = first chunk of text j, device int32[n+1]) into `partial`
+// (float [n_chunks * H]), then per text the ordered sum, mean and scaling.
+#define POOL_CHUNK 64
+cudaError_t launch_pool_l2(const float* x, const int32_t* cu, const int32_t* chunk_off, int n_texts, int n_chunks,
+                           int H, float* partial, float* out, cudaStream_t s);
 cudaError_t launch_attention_simple(const void* qkv, bool bf16_act, const int32_t* cu, int n_texts, int T, int H,
                                     int n_heads, bool is_global, int window, void* o, cudaStream_t s);
 
