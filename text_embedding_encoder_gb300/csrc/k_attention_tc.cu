@@ -5,22 +5,26 @@
 // the global layers (layer 0 and every third), |i - j| <= 64 on the others --
 // with scores q.k / sqrt(64) and a softmax over the allowed keys.
 //
-// Work item = (text, 128-query tile) x head; the host lists the items with
-// their key range [k_lo, k_hi) (whole text, or the window clipped to the
-// text), longest first.  One CTA per item, 6 warps:
-//   warp 0 lane 0   TMA: the Q tile once, then K and V tiles (128 keys) into a
-//                   3-stage ring, straight from the packed qkv rows;
+// Work unit = (text, 128-query tile) x head; the host lists the (text, tile)
+// items with their key range [k_lo, k_hi) (whole text, or the window clipped to
+// the text), longest first.  The kernel is persistent: one CTA per SM walks
+// the units u = blockIdx.x, blockIdx.x + gridDim.x, ...  Six warps:
+//   warp 0 lane 0   TMA: each unit's Q tile (double-buffered, so the next
+//                   unit's Q arrives early), then its K and V tiles (128 keys)
+//                   into a 3-stage ring, straight from the packed qkv rows;
 //   warp 1          TMEM allocation; lane 0 issues S = Q K^T (M=128, N=128,
-//                   K=64) into one of two TMEM S buffers, and O_j = P_j V_j
+//                   K=64) into one of two TMEM S buffers, and O_t = P_t V_t
 //                   (M=128, N=64, K=128; V read as an MN-major operand, no
-//                   transpose) into one of two TMEM O buffers;
-//   warps 2-5       one query row per thread: read S from TMEM, mask, online
-//                   softmax in fp32 (exp2 with the scale folded in), write P
-//                   as bf16 into shared memory in the 128-byte swizzle layout,
-//                   accumulate O = O * corr + P_j V_j in registers, and store
-//                   O / l as bf16.
-// The MMA issuer runs S for tile j+1 before P_j V_j so the softmax of one tile
-// overlaps the tensor-core work of the next.  All waits are bounded.
+//                   transpose) into one of two TMEM O buffers.  S of tile t+1
+//                   is issued before P_t V_t, across unit boundaries too, so
+//                   the softmax of one tile overlaps the QK^T of the next;
+//   warps 2-5       one query row per thread: one 128-column TMEM load of S,
+//                   the mask (skipped when the whole tile is visible to the
+//                   row), the online softmax in fp32 with exp2 (scale folded
+//                   into one FMA), P as bf16 into shared memory in the 128-byte
+//                   swizzle layout, O = O * corr + P_t V_t in registers, and
+//                   O / l stored as bf16.
+// Pipeline counters run across units; every wait is bounded.
 #include "tee_internal.cuh"
 
 #include <cuda.h>
@@ -41,13 +45,13 @@ constexpr int KV_STAGES = 3;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TILE_BYTES = BQ * HD * 2;        // Q, K or V tile: 16 KB
 constexpr uint32_t P_BYTES = BQ * BKV * 2;          // 32 KB
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
+constexpr uint32_t OFF_Q = 0;                       // 2 Q buffers
+constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + KV_STAGES * TILE_BYTES;
 constexpr uint32_t OFF_P = OFF_V + KV_STAGES * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
 // barrier indices
-constexpr int B_Q = 0, B_KVF = 1, B_KVE = B_KVF + KV_STAGES, B_SF = B_KVE + KV_STAGES, B_SE = B_SF + 2,
+constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = B_KVF + KV_STAGES, B_SF = B_KVE + KV_STAGES, B_SE = B_SF + 2,
               B_PF = B_SE + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_DONE = B_OE + 2, N_BARS = B_DONE + 1;
 constexpr uint32_t SMEM_TOTAL = OFF_BAR + N_BARS * 8 + 16 + 1024;
 constexpr uint32_t TMEM_COLS = 512;                 // S: 2 x 128 columns, O: 2 x 64 columns
@@ -55,6 +59,7 @@ constexpr uint32_t TM_S = 0, TM_O = 256;
 
 struct AttnParams {
     const int4* items;      // {q_start, q_len, k_lo, k_hi} per (text, query tile)
+    int n_units;            // items x heads
     int n_heads;
     int hidden;
     int is_global;
@@ -63,6 +68,8 @@ struct AttnParams {
     bf16* o;                // [T, hidden]
     unsigned int* status;
 };
+
+__device__ __forceinline__ int n_kv_tiles(const int4& it) { return (it.w - it.z + BKV - 1) / BKV; }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm, AttnParams p) {
@@ -75,23 +82,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto bar = [&](int i) { return smem_u32(bars + i); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int head = blockIdx.x % p.n_heads;
-    const int4 item = p.items[blockIdx.x / p.n_heads];
-    const int q_start = item.x, q_len = item.y, k_lo = item.z, k_hi = item.w;
-    const int nk = (k_hi - k_lo + BKV - 1) / BKV;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(B_Q), 1);
-        for (int s = 0; s < KV_STAGES; ++s) {
-            mbar_init(bar(B_KVF + s), 1);
-            mbar_init(bar(B_KVE + s), 1);
-        }
         for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_QF + b), 1);
+            mbar_init(bar(B_QE + b), 1);
             mbar_init(bar(B_SF + b), 1);
             mbar_init(bar(B_SE + b), 128);
             mbar_init(bar(B_PF + b), 128);
             mbar_init(bar(B_OF + b), 1);
             mbar_init(bar(B_OE + b), 128);
+        }
+        for (int s = 0; s < KV_STAGES; ++s) {
+            mbar_init(bar(B_KVF + s), 1);
+            mbar_init(bar(B_KVE + s), 1);
         }
         mbar_init(bar(B_DONE), 1);
         *abort_flag = 0;
@@ -112,25 +116,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            const int xq = head * HD, xk = p.hidden + head * HD, xv = 2 * p.hidden + head * HD;
-            mbar_expect_tx(bar(B_Q), TILE_BYTES);
-            tma_load_2d(sbase + OFF_Q, &tm, xq, q_start, bar(B_Q));
-            bool armed[KV_STAGES] = {false, false, false};
-            uint32_t armed_parity[KV_STAGES] = {0, 0, 0};
-            for (int kt = 0; kt < nk; ++kt) {
-                const int s = kt % KV_STAGES;
-                const uint32_t r = kt / KV_STAGES;
-                if (!mbar_wait(bar(B_KVE + s), (r & 1) ^ 1, abort_flag)) break;
-                const int y = k_lo + kt * BKV;
-                mbar_expect_tx(bar(B_KVF + s), 2 * TILE_BYTES);
-                tma_load_2d(sbase + OFF_K + s * TILE_BYTES, &tm, xk, y, bar(B_KVF + s));
-                tma_load_2d(sbase + OFF_V + s * TILE_BYTES, &tm, xv, y, bar(B_KVF + s));
-                armed[s] = true;
-                armed_parity[s] = r & 1;
+            bool q_armed[2] = {false, false}, kv_armed[KV_STAGES] = {false, false, false};
+            uint32_t q_par[2] = {0, 0}, kv_par[KV_STAGES] = {0, 0, 0};
+            uint32_t g = 0;   // KV tiles issued
+            int ui = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
+                const int4 it = p.items[u / p.n_heads];
+                const int head = u % p.n_heads;
+                const int nk = n_kv_tiles(it);
+                const int qb = ui & 1;
+                if (!mbar_wait(bar(B_QE + qb), ((ui >> 1) & 1) ^ 1, abort_flag)) break;
+                mbar_expect_tx(bar(B_QF + qb), TILE_BYTES);
+                tma_load_2d(sbase + OFF_Q + qb * TILE_BYTES, &tm, head * HD, it.x, bar(B_QF + qb));
+                q_armed[qb] = true;
+                q_par[qb] = (ui >> 1) & 1;
+                const int xk = p.hidden + head * HD, xv = 2 * p.hidden + head * HD;
+                for (int kt = 0; kt < nk; ++kt, ++g) {
+                    const int s = g % KV_STAGES;
+                    const uint32_t r = g / KV_STAGES;
+                    if (!mbar_wait(bar(B_KVE + s), (r & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int y = it.z + kt * BKV;
+                    mbar_expect_tx(bar(B_KVF + s), 2 * TILE_BYTES);
+                    tma_load_2d(sbase + OFF_K + s * TILE_BYTES, &tm, xk, y, bar(B_KVF + s));
+                    tma_load_2d(sbase + OFF_V + s * TILE_BYTES, &tm, xv, y, bar(B_KVF + s));
+                    kv_armed[s] = true;
+                    kv_par[s] = r & 1;
+                }
             }
-            mbar_wait_drain(bar(B_Q), 0);
+            for (int b = 0; b < 2; ++b)
+                if (q_armed[b]) mbar_wait_drain(bar(B_QF + b), q_par[b]);
             for (int s = 0; s < KV_STAGES; ++s)
-                if (armed[s]) mbar_wait_drain(bar(B_KVF + s), armed_parity[s]);
+                if (kv_armed[s]) mbar_wait_drain(bar(B_KVF + s), kv_par[s]);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -138,37 +158,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_s = make_idesc(BQ, BKV);
             constexpr uint32_t idesc_pv = make_idesc(BQ, HD) | IDESC_B_MN_MAJOR;
-            bool ok = mbar_wait(bar(B_Q), 0, abort_flag);
-            const uint64_t qdesc = sw128_desc(sbase + OFF_Q);
-            for (int kt = 0; ok && kt <= nk; ++kt) {
-                if (kt < nk) {
-                    const int st = kt % KV_STAGES, sb = kt & 1;
-                    if (!mbar_wait(bar(B_KVF + st), (kt / KV_STAGES) & 1, abort_flag)) break;
-                    if (!mbar_wait(bar(B_SE + sb), ((kt >> 1) & 1) ^ 1, abort_flag)) break;
+            uint32_t t = 0;          // tiles whose S has been issued (global)
+            bool ok = true;
+            bool pend = false;       // a tile whose P V is still to be issued
+            uint32_t pend_t = 0;
+            // P_t V_t for the pending tile t
+            auto issue_pv = [&](uint32_t tt) -> bool {
+                const int pb = tt & 1, st = tt % KV_STAGES;
+                if (!mbar_wait(bar(B_PF + pb), (tt >> 1) & 1, abort_flag)) return false;
+                if (!mbar_wait(bar(B_OE + pb), ((tt >> 1) & 1) ^ 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t pbase = sbase + OFF_P + pb * P_BYTES;
+                const uint32_t vbase = sbase + OFF_V + st * TILE_BYTES;
+#pragma unroll
+                for (int s = 0; s < BKV / 16; ++s) {
+                    const uint64_t adesc = sw128_desc(pbase + (s >> 2) * (P_BYTES / 2)) + 2 * (s & 3);
+                    const uint64_t vdesc = sw128_desc_mn(vbase + s * 2048);
+                    mma_bf16(tmem_base + TM_O + pb * HD, adesc, vdesc, idesc_pv, s != 0);
+                }
+                mma_commit(bar(B_OF + pb));
+                mma_commit(bar(B_KVE + st));
+                return true;
+            };
+            int ui = 0;
+            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
+                const int nk = n_kv_tiles(p.items[u / p.n_heads]);
+                const int qb = ui & 1;
+                if (!mbar_wait(bar(B_QF + qb), (ui >> 1) & 1, abort_flag)) break;
+                const uint64_t qdesc = sw128_desc(sbase + OFF_Q + qb * TILE_BYTES);
+                for (int kt = 0; kt < nk; ++kt, ++t) {
+                    const int st = t % KV_STAGES, sb = t & 1;
+                    if (!mbar_wait(bar(B_KVF + st), (t / KV_STAGES) & 1, abort_flag) ||
+                        !mbar_wait(bar(B_SE + sb), ((t >> 1) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const uint64_t kdesc = sw128_desc(sbase + OFF_K + st * TILE_BYTES);
 #pragma unroll
                     for (int k = 0; k < HD / 16; ++k)
                         mma_bf16(tmem_base + TM_S + sb * BKV, qdesc + 2 * k, kdesc + 2 * k, idesc_s, k != 0);
                     mma_commit(bar(B_SF + sb));
-                }
-                if (kt >= 1) {
-                    const int j = kt - 1, pb = j & 1, st = j % KV_STAGES;
-                    if (!mbar_wait(bar(B_PF + pb), (j >> 1) & 1, abort_flag)) break;
-                    if (!mbar_wait(bar(B_OE + pb), ((j >> 1) & 1) ^ 1, abort_flag)) break;
-                    tc_fence_after();
-                    const uint32_t pbase = sbase + OFF_P + pb * P_BYTES;
-                    const uint32_t vbase = sbase + OFF_V + st * TILE_BYTES;
-#pragma unroll
-                    for (int s = 0; s < BKV / 16; ++s) {
-                        const uint64_t adesc = sw128_desc(pbase + (s >> 2) * (P_BYTES / 2)) + 2 * (s & 3);
-                        const uint64_t vdesc = sw128_desc_mn(vbase + s * 2048);
-                        mma_bf16(tmem_base + TM_O + pb * HD, adesc, vdesc, idesc_pv, s != 0);
+                    if (kt == nk - 1) mma_commit(bar(B_QE + qb));   // Q buffer free once these S MMAs finish
+                    if (pend && !issue_pv(pend_t)) {
+                        ok = false;
+                        break;
                     }
-                    mma_commit(bar(B_OF + pb));
-                    mma_commit(bar(B_KVE + st));
+                    pend = true;
+                    pend_t = t;
                 }
             }
+            if (ok && pend) issue_pv(pend_t);
             mma_commit(bar(B_DONE));
             mbar_wait_drain(bar(B_DONE), 0);
         }
@@ -177,104 +217,104 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------- softmax / output (warps 2..5) ----------------
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
-        const int qg = q_start + r;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint8_t* prow0 = smem + OFF_P + r * 128;
-        float m = -INFINITY, l = 0.f, corr_pending = 1.f;
-        float O[HD];
-#pragma unroll
-        for (int d = 0; d < HD; ++d) O[d] = 0.f;
+        const float sl2 = p.scale_log2;
+        uint32_t t = 0;
         bool ok = true;
+        float O[HD];
 
-        auto o_phase = [&](int j, float corr) -> bool {
-            const int ob = j & 1;
-            if (!mbar_wait(bar(B_OF + ob), (j >> 1) & 1, abort_flag)) return false;
+        auto o_phase = [&](uint32_t tt, float corr) -> bool {
+            const int ob = tt & 1;
+            if (!mbar_wait(bar(B_OF + ob), (tt >> 1) & 1, abort_flag)) return false;
             tc_fence_after();
-            float pv[32];
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                tmem_ld32(tmem_base + lane_off + TM_O + ob * HD + c * 32, pv);
-#pragma unroll
-                for (int d = 0; d < 32; ++d) O[c * 32 + d] = O[c * 32 + d] * corr + pv[d];
-            }
+            float pv[HD];
+            tmem_ld64(tmem_base + lane_off + TM_O + ob * HD, pv);
             tc_fence_before();
             mbar_arrive(bar(B_OE + ob));
+#pragma unroll
+            for (int d = 0; d < HD; ++d) O[d] = fmaf(O[d], corr, pv[d]);
             return true;
         };
 
-        for (int kt = 0; kt < nk && ok; ++kt) {
-            const int sb = kt & 1;
-            if (!mbar_wait(bar(B_SF + sb), (kt >> 1) & 1, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t saddr = tmem_base + lane_off + TM_S + sb * BKV;
-            const int key0 = k_lo + kt * BKV;
-            // pass 1: row maximum of the masked, scaled scores
-            float mx = -INFINITY;
-            float v[32];
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(saddr + c * 32, v);
+        for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+            const int4 it = p.items[u / p.n_heads];
+            const int head = u % p.n_heads;
+            const int q_start = it.x, q_len = it.y, k_lo = it.z, k_hi = it.w;
+            const int nk = n_kv_tiles(it);
+            const int qg = q_start + r;
+            float m = -INFINITY, l = 0.f, corr_pending = 1.f;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int kg = key0 + c * 32 + i;
-                    const bool valid = kg < k_hi && (p.is_global || abs(qg - kg) <= p.window);
-                    if (valid) mx = fmaxf(mx, v[i] * p.scale_log2);
+            for (int d = 0; d < HD; ++d) O[d] = 0.f;
+            for (int kt = 0; kt < nk; ++kt, ++t) {
+                const int sb = t & 1;
+                if (!mbar_wait(bar(B_SF + sb), (t >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-            }
-            const float m_new = fmaxf(m, mx);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float corr = exp2f(m - m_use);
-            // pass 2: probabilities, row sum, bf16 P into shared memory (128B swizzle)
-            float sum = 0.f;
-            uint8_t* prow = prow0 + sb * P_BYTES;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(saddr + c * 32, v);
+                tc_fence_after();
+                float v[BKV];
+                tmem_ld128(tmem_base + lane_off + TM_S + sb * BKV, v);
+                tc_fence_before();
+                mbar_arrive(bar(B_SE + sb));
+                const int key0 = k_lo + kt * BKV;
+                const bool full = key0 + BKV <= k_hi &&
+                                  (p.is_global || (qg - key0 <= p.window && key0 + BKV - 1 - qg <= p.window));
+                if (!full) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int kg = key0 + c * 32 + i;
-                    const bool valid = kg < k_hi && (p.is_global || abs(qg - kg) <= p.window);
-                    const float pr = valid ? exp2f(v[i] * p.scale_log2 - m_use) : 0.f;
-                    sum += pr;
-                    v[i] = pr;
+                    for (int i = 0; i < BKV; ++i) {
+                        const int kg = key0 + i;
+                        const bool valid = kg < k_hi && (p.is_global || abs(qg - kg) <= p.window);
+                        if (!valid) v[i] = -INFINITY;
+                    }
                 }
-                uint8_t* region = prow + (c >> 1) * (P_BYTES / 2);
+                float mx = v[0];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int chunk = ((c & 1) * 4 + i) ^ (r & 7);
+                for (int i = 1; i < BKV; ++i) mx = fmaxf(mx, v[i]);
+                const float m_new = fmaxf(m, mx * sl2);
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                const float corr = ex2_approx(m - m_use);
+                float sum = 0.f;
+#pragma unroll
+                for (int i = 0; i < BKV; ++i) {
+                    v[i] = ex2_approx(fmaf(v[i], sl2, -m_use));
+                    sum += v[i];
+                }
+                uint8_t* prow = prow0 + sb * P_BYTES;
+#pragma unroll
+                for (int c = 0; c < BKV / 8; ++c) {
                     uint4 q;
-                    q.x = pack_bf16(v[8 * i + 0], v[8 * i + 1]);
-                    q.y = pack_bf16(v[8 * i + 2], v[8 * i + 3]);
-                    q.z = pack_bf16(v[8 * i + 4], v[8 * i + 5]);
-                    q.w = pack_bf16(v[8 * i + 6], v[8 * i + 7]);
-                    *reinterpret_cast<uint4*>(region + chunk * 16) = q;
+                    q.x = pack_bf16(v[8 * c + 0], v[8 * c + 1]);
+                    q.y = pack_bf16(v[8 * c + 2], v[8 * c + 3]);
+                    q.z = pack_bf16(v[8 * c + 4], v[8 * c + 5]);
+                    q.w = pack_bf16(v[8 * c + 6], v[8 * c + 7]);
+                    // 16-byte chunk c of the row: region c / 8 (64 keys each), swizzled by row
+                    *reinterpret_cast<uint4*>(prow + (c >> 3) * (P_BYTES / 2) + (((c & 7) ^ (r & 7)) << 4)) = q;
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(B_PF + sb));
+                l = l * corr + sum;
+                m = m_new;
+                if (kt >= 1 && !o_phase(t - 1, corr_pending)) {
+                    ok = false;
+                    break;
+                }
+                corr_pending = corr;
             }
-            tc_fence_before();
-            mbar_arrive(bar(B_SE + sb));
-            fence_proxy_async_smem();
-            mbar_arrive(bar(B_PF + sb));
-            l = l * corr + sum;
-            m = m_new;
-            if (kt >= 1 && !o_phase(kt - 1, corr_pending)) {
+            if (!ok || !o_phase(t - 1, corr_pending)) {
                 ok = false;
                 break;
             }
-            corr_pending = corr;
-        }
-        if (ok && nk > 0) ok = o_phase(nk - 1, corr_pending);
-        if (ok && r < q_len) {
-            const float inv = 1.0f / l;
-            float out[32];
-            bf16* dst = p.o + (size_t)qg * p.hidden + head * HD;
+            if (r < q_len) {
+                const float inv = 1.0f / l;
+                float out[32];
+                bf16* dst = p.o + (size_t)qg * p.hidden + head * HD;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 2; ++c) {
 #pragma unroll
-                for (int d = 0; d < 32; ++d) out[d] = O[c * 32 + d] * inv;
-                store_bf16x32(dst + c * 32, out);
+                    for (int d = 0; d < 32; ++d) out[d] = O[c * 32 + d] * inv;
+                    store_bf16x32(dst + c * 32, out);
+                }
             }
         }
     }
@@ -293,6 +333,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 cudaError_t g_init_err = cudaSuccess;
 bool g_attr_set = false;
+int g_num_sms = 0;
 
 void init_once() {
     cudaDriverEntryPointQueryResult q;
@@ -303,6 +344,10 @@ void init_once() {
         return;
     }
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) g_init_err = e;
 }
 
 }  // namespace
@@ -329,7 +374,10 @@ cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, cons
         if (e != cudaSuccess) return e;
         g_attr_set = true;
     }
-    AttnParams p{d_items, n_heads, H, is_global ? 1 : 0, window, 1.4426950408889634f / 8.0f, (bf16*)o, status};
-    attn_tc_kernel<<<n_items * n_heads, NUM_THREADS, SMEM_TOTAL, s>>>(tm, p);
+    const int n_units = n_items * n_heads;
+    AttnParams p{d_items, n_units, n_heads, H, is_global ? 1 : 0, window, 1.4426950408889634f / 8.0f, (bf16*)o,
+                 status};
+    const int grid = n_units < g_num_sms ? n_units : g_num_sms;
+    attn_tc_kernel<<<grid, NUM_THREADS, SMEM_TOTAL, s>>>(tm, p);
     return cudaGetLastError();
 }
