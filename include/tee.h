@@ -146,7 +146,8 @@ int tee_encode_device(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, c
                       int n_texts, float* d_out, void* stream);
 
 /* Message of the last failure on this context ("" if none).  NULL ctx: the
- * message of the last failed tee_create in this process. */
+ * message of the last failed context-free call in this process (tee_create,
+ * tee_pool_l2_noalloc). */
 const char* tee_last_error(const tee_ctx* ctx);
 
 /* Release the context and all its device memory.  NULL-safe. */

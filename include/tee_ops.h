@@ -77,6 +77,36 @@ int tee_op_ffn_out(tee_ctx* ctx, int layer, const void* d_z, float* d_x, int T, 
 int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts,
                    float* d_out, void* stream);
 
+/*
+ * Allocation-free mean-pool + L2 normalisation.  The page has no counterpart:
+ * this entry point exists for callers that cannot allocate device memory --
+ * code running inside a host framework that owns all device memory through
+ * its own pool and forbids raw cudaMalloc, or a latency-critical path that
+ * cannot afford the implicit synchronisation of an allocation.  It needs no
+ * context and calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Computes the same result as tee_op_pool_l2 with the same kernels:
+ *   d_x    device float[T * hidden], T = h_cu[n_texts];
+ *   d_cu   device int32[n_texts + 1];  h_cu: host copy of the same array
+ *          (validated, and used to size the launch);
+ *   d_out  device float[n_texts * hidden];  async on `stream`.
+ * Its scratch (chunk offsets and the partial sums of 64-row chunks) lives in
+ * file-scope device arrays of fixed size that every GPU loading the library
+ * holds until the process exits (about 4 MiB).  Limits: n_texts <=
+ * TEE_POOL_NOALLOC_MAX_TEXTS, sum_j ceil(len_j / 64) * hidden <=
+ * TEE_POOL_NOALLOC_MAX_PARTIAL, hidden a multiple of 4 in [4, 1024]; larger
+ * inputs return TEE_ETOOLONG / TEE_EINVAL with a message in
+ * tee_last_error(NULL).  Every call on a device shares the same scratch and
+ * overwrites all of it that it reads, so calls that overlap on the GPU (for
+ * instance on two streams) race.  The first call on a device looks up the
+ * arrays' device addresses (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.
+ */
+#define TEE_POOL_NOALLOC_MAX_TEXTS   8192
+#define TEE_POOL_NOALLOC_MAX_PARTIAL 1048576   /* floats */
+int tee_pool_l2_noalloc(const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int hidden,
+                        float* d_out, void* stream);
+
 /* ---- W8A8 pieces (TEE_W8A8 contexts) ----------------------------------- */
 
 /* Per-row 7-bit quantiser: s[m] = max|x[m,:]| / 63 (IEEE fp32 division),

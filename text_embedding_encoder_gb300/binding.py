@@ -83,6 +83,7 @@ SIGNATURES = {
     "tee_op_w8a8_partials": (_i, [_ctx, _i, _i, _vp, _i, _vp, _vp]),
     "tee_weight_codes": (_i, [_ctx, _i, _i, _vp, _vp]),
     "tee_device_status": (_i, [_ctx]),
+    "tee_pool_l2_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp]),
 }
 
 _LIB = None

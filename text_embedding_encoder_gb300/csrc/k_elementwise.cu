@@ -7,6 +7,8 @@
 // text, reductions by warp shuffles.
 #include "tee_internal.cuh"
 
+#include <mutex>
+
 namespace {
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -225,6 +227,45 @@ __global__ void pool_finish_kernel(const float* __restrict__ partial, const int3
     }
 }
 
+// Chunk offsets of the two-pass pool computed on the device from cu: text j
+// owns ceil(len_j / POOL_CHUNK) chunks; chunk_off[j] is the exclusive prefix
+// sum and chunk_off[n] the total.  One block; each thread scans a contiguous
+// run of texts, then a block-wide exclusive scan of the per-thread totals.
+__global__ void pool_chunk_offsets_kernel(const int32_t* __restrict__ cu, int n_texts,
+                                          int32_t* __restrict__ chunk_off) {
+    __shared__ int warp_excl[32];
+    const int per = (n_texts + blockDim.x - 1) / blockDim.x;
+    const int j0 = min(n_texts, (int)threadIdx.x * per), j1 = min(n_texts, j0 + per);
+    int local = 0;
+    for (int j = j0; j < j1; ++j) local += (cu[j + 1] - cu[j] + POOL_CHUNK - 1) / POOL_CHUNK;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_excl[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        const int tot = lane < (int)(blockDim.x >> 5) ? warp_excl[lane] : 0;
+        int inc = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        warp_excl[lane] = inc - tot;
+    }
+    __syncthreads();
+    int base = warp_excl[w] + incl - local;
+    for (int j = j0; j < j1; ++j) {
+        chunk_off[j] = base;
+        base += (cu[j + 1] - cu[j] + POOL_CHUNK - 1) / POOL_CHUNK;
+    }
+    if (threadIdx.x == blockDim.x - 1) chunk_off[n_texts] = base;
+}
+
 }  // namespace
 
 cudaError_t launch_convert_f32_bf16(const float* src, bf16* dst, size_t n, cudaStream_t s) {
@@ -295,4 +336,70 @@ cudaError_t launch_pool_l2(const float* x, const int32_t* cu, const int32_t* chu
     if (e != cudaSuccess) return e;
     pool_finish_kernel<<<n_texts, 256, 0, s>>>(partial, cu, chunk_off, H, out);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free mean-pool + L2 (tee_pool_l2_noalloc).  Its scratch -- the
+// chunk offsets and the partial column sums of the two-pass pool -- lives in
+// these fixed-size device arrays, which every GPU that loads the library
+// holds until the process exits.  Host code may not use the arrays' names as
+// device addresses: the addresses come from cudaGetSymbolAddress, once per
+// device, on the first call made on that device.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) int32_t g_noalloc_chunk_off[TEE_POOL_NOALLOC_MAX_TEXTS + 1];
+static __device__ __align__(256) float g_noalloc_partial[TEE_POOL_NOALLOC_MAX_PARTIAL];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_off_ptr[kMaxDevices] = {};
+float* g_noalloc_partial_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" int tee_pool_l2_noalloc(const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts,
+                                   int hidden, float* d_out, void* stream) {
+    if (!d_x || !d_cu || !h_cu || !d_out) return tee_set_global_error(TEE_EINVAL, "pool_l2_noalloc: NULL pointer");
+    if (n_texts < 1) return tee_set_global_error(TEE_EINVAL, "pool_l2_noalloc: n_texts must be >= 1");
+    if (n_texts > TEE_POOL_NOALLOC_MAX_TEXTS)
+        return tee_set_global_error(TEE_ETOOLONG, "pool_l2_noalloc: n_texts exceeds TEE_POOL_NOALLOC_MAX_TEXTS");
+    if (hidden < 4 || hidden > 1024 || hidden % 4)
+        return tee_set_global_error(TEE_EINVAL, "pool_l2_noalloc: hidden must be a multiple of 4 in [4, 1024]");
+    if (h_cu[0] != 0) return tee_set_global_error(TEE_EINVAL, "pool_l2_noalloc: cu_seqlens[0] must be 0");
+    long long n_chunks = 0;
+    for (int j = 0; j < n_texts; ++j) {
+        const int len = h_cu[j + 1] - h_cu[j];
+        if (len <= 0)
+            return tee_set_global_error(TEE_EINVAL, "pool_l2_noalloc: cu_seqlens must be strictly increasing");
+        n_chunks += (len + POOL_CHUNK - 1) / POOL_CHUNK;
+    }
+    if (n_chunks * hidden > TEE_POOL_NOALLOC_MAX_PARTIAL)
+        return tee_set_global_error(TEE_ETOOLONG,
+                                    "pool_l2_noalloc: sum_j ceil(len_j / 64) * hidden exceeds TEE_POOL_NOALLOC_MAX_PARTIAL");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return tee_set_global_error(TEE_ECUDA, cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return tee_set_global_error(TEE_EINVAL, "pool_l2_noalloc: device index too large");
+    int32_t* off_ptr;
+    float* partial_ptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_off_ptr[dev]) {
+            void* a = nullptr;
+            void* b = nullptr;
+            e = cudaGetSymbolAddress(&a, g_noalloc_chunk_off);
+            if (e != cudaSuccess) return tee_set_global_error(TEE_ECUDA, cudaGetErrorString(e));
+            e = cudaGetSymbolAddress(&b, g_noalloc_partial);
+            if (e != cudaSuccess) return tee_set_global_error(TEE_ECUDA, cudaGetErrorString(e));
+            g_noalloc_partial_ptr[dev] = (float*)b;
+            g_noalloc_off_ptr[dev] = (int32_t*)a;
+        }
+        off_ptr = g_noalloc_off_ptr[dev];
+        partial_ptr = g_noalloc_partial_ptr[dev];
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    pool_chunk_offsets_kernel<<<1, 1024, 0, s>>>(d_cu, n_texts, off_ptr);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = launch_pool_l2(d_x, d_cu, off_ptr, n_texts, (int)n_chunks, hidden, partial_ptr, d_out, s);
+    if (e != cudaSuccess) return tee_set_global_error(TEE_ECUDA, cudaGetErrorString(e));
+    return TEE_OK;
 }

@@ -224,6 +224,8 @@ int prepare_attention_items(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cuda
 
 }  // namespace
 
+int tee_set_global_error(int code, const char* msg) { return fail(nullptr, code, "%s", msg); }
+
 // ---------------------------------------------------------------------------
 // profiling
 // ---------------------------------------------------------------------------

@@ -84,6 +84,9 @@ inline bool act_is_bf16(const tee_ctx* c) { return c->cfg.dtype == TEE_BF16; }
 inline size_t act_size(const tee_ctx* c) { return act_is_bf16(c) ? 2 : 4; }
 inline int layer_is_global(const tee_ctx* c, int l) { return (l % c->cfg.global_every) == 0; }
 
+// Record the message returned by tee_last_error(NULL) for context-free calls; returns `code`.
+int tee_set_global_error(int code, const char* msg);
+
 // Profiling brackets: record events around one launch when profiling is on.
 int prof_begin(tee_ctx* c, cudaStream_t s, int kclass, double flops, double bytes);
 void prof_end(tee_ctx* c, cudaStream_t s, int slot);
