@@ -18,12 +18,16 @@
 //                   transpose) into one of two TMEM O buffers.  S of tile t+1
 //                   is issued before P_t V_t, across unit boundaries too, so
 //                   the softmax of one tile overlaps the QK^T of the next;
-//   warps 2-5       one query row per thread: one 128-column TMEM load of S,
-//                   the mask (skipped when the whole tile is visible to the
-//                   row), the online softmax in fp32 with exp2 (scale folded
-//                   into one FMA), P as bf16 into shared memory in the 128-byte
-//                   swizzle layout, O = O * corr + P_t V_t in registers, and
-//                   O / l stored as bf16.
+//   warps 2-9       two threads per query row (a warp may read only its
+//                   32-lane TMEM quadrant, so warps w and w+4 share one and
+//                   split the 128 key columns, and the 64 output dimensions,
+//                   in halves): one 64-column TMEM load of S, the mask as a
+//                   per-row interval of visible keys, the tile's row maximum
+//                   exchanged through shared memory with a pair barrier, the
+//                   online softmax in fp32 with exp2 (scale folded into one
+//                   FMA), P as bf16 into shared memory in the 128-byte swizzle
+//                   layout, O = O * corr + P_t V_t in registers, O / l stored
+//                   as bf16.
 // Pipeline counters run across units; every wait is bounded.
 #include "tee_internal.cuh"
 
@@ -42,7 +46,8 @@ constexpr int BQ = 128;
 constexpr int BKV = 128;
 constexpr int HD = 64;
 constexpr int KV_STAGES = 3;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;
+constexpr int SM_THREADS = 256;   // softmax warps 2..9
 constexpr uint32_t TILE_BYTES = BQ * HD * 2;        // Q, K or V tile: 16 KB
 constexpr uint32_t P_BYTES = BQ * BKV * 2;          // 32 KB
 constexpr uint32_t OFF_Q = 0;                       // 2 Q buffers
@@ -53,7 +58,8 @@ constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
 // barrier indices
 constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = B_KVF + KV_STAGES, B_SF = B_KVE + KV_STAGES, B_SE = B_SF + 2,
               B_PF = B_SE + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_DONE = B_OE + 2, N_BARS = B_DONE + 1;
-constexpr uint32_t SMEM_TOTAL = OFF_BAR + N_BARS * 8 + 16 + 1024;
+constexpr uint32_t OFF_RED = OFF_BAR + N_BARS * 8 + 16;       // row-maximum exchange: [2 tiles][2 halves][128 rows]
+constexpr uint32_t SMEM_TOTAL = OFF_RED + 2 * 2 * 128 * 4 + 1024;
 constexpr uint32_t TMEM_COLS = 512;                 // S: 2 x 128 columns, O: 2 x 64 columns
 constexpr uint32_t TM_S = 0, TM_O = 256;
 
@@ -88,10 +94,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(B_QF + b), 1);
             mbar_init(bar(B_QE + b), 1);
             mbar_init(bar(B_SF + b), 1);
-            mbar_init(bar(B_SE + b), 128);
-            mbar_init(bar(B_PF + b), 128);
+            mbar_init(bar(B_SE + b), SM_THREADS);
+            mbar_init(bar(B_PF + b), SM_THREADS);
             mbar_init(bar(B_OF + b), 1);
-            mbar_init(bar(B_OE + b), 128);
+            mbar_init(bar(B_OE + b), SM_THREADS);
         }
         for (int s = 0; s < KV_STAGES; ++s) {
             mbar_init(bar(B_KVF + s), 1);
@@ -214,26 +220,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ---------------- softmax / output (warps 2..5) ----------------
+        // ---------------- softmax / output (warps 2..9) ----------------
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;
+        const int half = (warp - 2) >> 2;               // key columns [64*half, 64*half + 64)
+        const int r = quad * 32 + lane;                 // query row of the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        uint8_t* prow0 = smem + OFF_P + r * 128;
+        uint8_t* prow0 = smem + OFF_P + half * (P_BYTES / 2) + r * 128;
+        float* red = reinterpret_cast<float*>(smem + OFF_RED);   // [2][2][128]
+        const uint32_t pair_bar = 1 + quad;             // named barrier of warps (w, w + 4)
         const float sl2 = p.scale_log2;
         uint32_t t = 0;
         bool ok = true;
-        float O[HD];
+        float O[HD / 2];
 
+        auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
         auto o_phase = [&](uint32_t tt, float corr) -> bool {
             const int ob = tt & 1;
             if (!mbar_wait(bar(B_OF + ob), (tt >> 1) & 1, abort_flag)) return false;
             tc_fence_after();
-            float pv[HD];
-            tmem_ld64(tmem_base + lane_off + TM_O + ob * HD, pv);
+            float pv[32];
+            tmem_ld32(tmem_base + lane_off + TM_O + ob * HD + half * 32, pv);
             tc_fence_before();
             mbar_arrive(bar(B_OE + ob));
 #pragma unroll
-            for (int d = 0; d < HD; ++d) O[d] = fmaf(O[d], corr, pv[d]);
+            for (int d = 0; d < HD / 2; ++d) O[d] = fmaf(O[d], corr, pv[d]);
             return true;
         };
 
@@ -243,9 +253,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int q_start = it.x, q_len = it.y, k_lo = it.z, k_hi = it.w;
             const int nk = n_kv_tiles(it);
             const int qg = q_start + r;
+            // keys visible to this row: [vis_lo, vis_hi)
+            const int vis_lo = p.is_global ? k_lo : max(k_lo, qg - p.window);
+            const int vis_hi = p.is_global ? k_hi : min(k_hi, qg + p.window + 1);
             float m = -INFINITY, l = 0.f, corr_pending = 1.f;
 #pragma unroll
-            for (int d = 0; d < HD; ++d) O[d] = 0.f;
+            for (int d = 0; d < HD / 2; ++d) O[d] = 0.f;
             for (int kt = 0; kt < nk; ++kt, ++t) {
                 const int sb = t & 1;
                 if (!mbar_wait(bar(B_SF + sb), (t >> 1) & 1, abort_flag)) {
@@ -253,43 +266,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                float v[BKV];
-                tmem_ld128(tmem_base + lane_off + TM_S + sb * BKV, v);
+                float v[64];
+                tmem_ld64(tmem_base + lane_off + TM_S + sb * BKV + half * 64, v);
                 tc_fence_before();
                 mbar_arrive(bar(B_SE + sb));
-                const int key0 = k_lo + kt * BKV;
-                const bool full = key0 + BKV <= k_hi &&
-                                  (p.is_global || (qg - key0 <= p.window && key0 + BKV - 1 - qg <= p.window));
-                if (!full) {
+                const int key0 = k_lo + kt * BKV + half * 64;
+                const int lo = vis_lo - key0, hi = vis_hi - key0;   // visible columns [lo, hi)
+                if (lo > 0 || hi < 64) {
 #pragma unroll
-                    for (int i = 0; i < BKV; ++i) {
-                        const int kg = key0 + i;
-                        const bool valid = kg < k_hi && (p.is_global || abs(qg - kg) <= p.window);
-                        if (!valid) v[i] = -INFINITY;
-                    }
+                    for (int i = 0; i < 64; ++i)
+                        if (i < lo || i >= hi) v[i] = -INFINITY;
                 }
                 float mx = v[0];
 #pragma unroll
-                for (int i = 1; i < BKV; ++i) mx = fmaxf(mx, v[i]);
+                for (int i = 1; i < 64; ++i) mx = fmaxf(mx, v[i]);
+                float* red_t = red + (t & 1) * 256;
+                red_t[half * 128 + r] = mx;
+                pair_sync();
+                mx = fmaxf(mx, red_t[(half ^ 1) * 128 + r]);
                 const float m_new = fmaxf(m, mx * sl2);
                 const float m_use = m_new == -INFINITY ? 0.f : m_new;
                 const float corr = ex2_approx(m - m_use);
                 float sum = 0.f;
 #pragma unroll
-                for (int i = 0; i < BKV; ++i) {
+                for (int i = 0; i < 64; ++i) {
                     v[i] = ex2_approx(fmaf(v[i], sl2, -m_use));
                     sum += v[i];
                 }
                 uint8_t* prow = prow0 + sb * P_BYTES;
 #pragma unroll
-                for (int c = 0; c < BKV / 8; ++c) {
+                for (int c = 0; c < 8; ++c) {
                     uint4 q;
                     q.x = pack_bf16(v[8 * c + 0], v[8 * c + 1]);
                     q.y = pack_bf16(v[8 * c + 2], v[8 * c + 3]);
                     q.z = pack_bf16(v[8 * c + 4], v[8 * c + 5]);
                     q.w = pack_bf16(v[8 * c + 6], v[8 * c + 7]);
-                    // 16-byte chunk c of the row: region c / 8 (64 keys each), swizzled by row
-                    *reinterpret_cast<uint4*>(prow + (c >> 3) * (P_BYTES / 2) + (((c & 7) ^ (r & 7)) << 4)) = q;
+                    *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = q;
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(bar(B_PF + sb));
@@ -305,16 +317,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ok = false;
                 break;
             }
+            // the row sum is split between the two halves
+            float* red_l = red + (t & 1) * 256;
+            red_l[half * 128 + r] = l;
+            pair_sync();
+            l += red_l[(half ^ 1) * 128 + r];
+            pair_sync();
             if (r < q_len) {
                 const float inv = 1.0f / l;
                 float out[32];
-                bf16* dst = p.o + (size_t)qg * p.hidden + head * HD;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-#pragma unroll
-                    for (int d = 0; d < 32; ++d) out[d] = O[c * 32 + d] * inv;
-                    store_bf16x32(dst + c * 32, out);
-                }
+                for (int d = 0; d < 32; ++d) out[d] = O[d] * inv;
+                store_bf16x32(p.o + (size_t)qg * p.hidden + head * HD + half * 32, out);
             }
         }
     }
