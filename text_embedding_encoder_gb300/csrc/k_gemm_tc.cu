@@ -50,11 +50,17 @@ struct Params {
     unsigned int* status;
 };
 
-template <int BN>
+// bf16-output epilogues stage each warp's 32 rows x 64 columns in a 4 KB
+// swizzled box (two per warp) and store it with a TMA bulk tensor store.
+template <int EPI>
+constexpr uint32_t staging_bytes() { return EPI == GEMM_EPI_ADD_F32 ? 0u : 4u * 2u * 4096u; }
+
+template <int BN, int EPI>
 struct Smem {
     static constexpr uint32_t B_BYTES = BN * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr uint32_t OUT_OFF = STAGES * STAGE_BYTES;
+    static constexpr uint32_t BAR_OFF = OUT_OFF + staging_bytes<EPI>();
     static constexpr uint32_t N_BARS = 2 * STAGES + 5;
     static constexpr uint32_t TOTAL = BAR_OFF + N_BARS * 8 + 16 + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -62,8 +68,9 @@ struct Smem {
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
-    using S = Smem<BN>;
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, Params p) {
+    using S = Smem<BN, EPI>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -92,6 +99,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+        if (EPI != GEMM_EPI_ADD_F32)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -178,22 +187,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------- epilogue (warps 2..5) ----------------
         const int quad = warp & 3;
         const int row_local = quad * 32 + lane;
+        uint8_t* stage = smem + S::OUT_OFF + (warp - 2) * 8192;   // this warp's two staging boxes
+        uint32_t n_stores = 0;                                     // store groups this warp committed
+        // Stage 64 bf16 columns of this warp's 32 rows and store them at (x, y).
+        auto store64 = [&](const float* v, int x, int y) {
+            uint8_t* box = stage + (n_stores & 1) * 4096;
+            if (lane == 0 && n_stores >= 2) bulk_wait_read<1>();   // the box's previous store has read it
+            __syncwarp();
+            stage_row_bf16x64(box, lane, v);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(&tmC, smem_u32(box), x, y);
+                bulk_commit();
+            }
+            ++n_stores;
+        };
         int it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
             const int acc = it & 1, use = it >> 1;
             const int n_t = tile % num_n, m_t = tile / num_n;
             const int gr = m_t * BM + row_local;
             const bool valid = gr < p.M;
+            const int y_box = m_t * BM + quad * 32;
             const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
             if constexpr (EPI == GEMM_EPI_STORE_BF16) {
                 if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
                 tc_fence_after();
-                bf16* C = reinterpret_cast<bf16*>(p.C) + (size_t)gr * p.N + n_t * BN;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(taddr + c * 32, v);
-                    if (valid) store_bf16x32(C + c * 32, v);
+                for (int g = 0; g < BN / 64; ++g) {
+                    float v[64];
+                    tmem_ld64(taddr + g * 64, v);
+                    store64(v, n_t * BN + g * 64, y_box);
                 }
             } else if constexpr (EPI == GEMM_EPI_ADD_F32) {
                 // the residual chunk is fetched one chunk ahead (the first one
@@ -234,7 +259,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // q and k tiles (columns < 2*hidden; 2*hidden is a multiple of
                 // the tile width) rotate every head with the row's cos/sin,
                 // fetched once per tile before the accumulator is ready
-                bf16* C = reinterpret_cast<bf16*>(p.C) + (size_t)gr * p.N + n_t * BN;
                 const bool rope = n_t * BN < 2 * p.hidden;
                 float cs[32], sn[32];
                 if (rope) {
@@ -252,42 +276,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
 #pragma unroll 1
                 for (int hh = 0; hh < BN / 64; ++hh) {
-                    float lo[32], hi[32];
-                    tmem_ld32(taddr + hh * 64, lo);
-                    tmem_ld32(taddr + hh * 64 + 32, hi);
+                    float v[64];   // one head: v[j] pairs with v[j + 32]
+                    tmem_ld64(taddr + hh * 64, v);
                     if (rope) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const float a = lo[j] * cs[j] - hi[j] * sn[j];
-                            const float b = hi[j] * cs[j] + lo[j] * sn[j];
-                            lo[j] = a;
-                            hi[j] = b;
+                            const float a = v[j] * cs[j] - v[j + 32] * sn[j];
+                            const float b = v[j + 32] * cs[j] + v[j] * sn[j];
+                            v[j] = a;
+                            v[j + 32] = b;
                         }
                     }
-                    if (valid) {
-                        store_bf16x32(C + hh * 64, lo);
-                        store_bf16x32(C + hh * 64 + 32, hi);
-                    }
+                    store64(v, n_t * BN + hh * 64, y_box);
                 }
-            } else {   // GEMM_EPI_GEGLU (BN == 256)
+            } else {   // GEMM_EPI_GEGLU (BN == 256): columns [0, 128) GELU inputs, [128, 256) gates
                 if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
                 tc_fence_after();
-                bf16* C = reinterpret_cast<bf16*>(p.C) + (size_t)gr * (p.N / 2) + n_t * (BN / 2);
 #pragma unroll 1
-                for (int c = 0; c < BN / 64; ++c) {
-                    float a[32], g[32];
-                    tmem_ld32(taddr + c * 32, a);
-                    tmem_ld32(taddr + BN / 2 + c * 32, g);
-                    if (valid) {
+                for (int g = 0; g < BN / 128; ++g) {
+                    float a[64], gt[64];
+                    tmem_ld64(taddr + g * 64, a);
+                    tmem_ld64(taddr + BN / 2 + g * 64, gt);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) a[j] = gelu_erf(a[j]) * g[j];
-                        store_bf16x32(C + c * 32, a);
-                    }
+                    for (int j = 0; j < 64; ++j) a[j] = gelu_erf(a[j]) * gt[j];
+                    store64(a, n_t * (BN / 2) + g * 64, y_box);
                 }
             }
             tc_fence_before();
             mbar_arrive(bar(TEMPTY + acc));
         }
+        if (lane == 0) bulk_wait_all();   // stores complete before the CTA exits
     }
 
     tc_fence_before();
@@ -323,6 +341,18 @@ void init_once() {
     if (e != cudaSuccess) g_init_err = e;
 }
 
+// Output map: bf16 [rows, cols], boxes of 32 rows x 64 columns, 128B swizzle.
+bool make_out_map(CUtensorMap* map, const void* ptr, int rows, int cols) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* map, const void* ptr, int rows, int K, int box_rows) {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
@@ -335,16 +365,17 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, int K, int box_rows) 
 }
 
 template <int BN, int EPI>
-cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid, cudaStream_t s) {
+cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const Params& p, int grid,
+                     cudaStream_t s) {
     static bool attr_set = false;
-    constexpr uint32_t smem = Smem<BN>::TOTAL;
+    constexpr uint32_t smem = Smem<BN, EPI>::TOTAL;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    gemm_tc_kernel<BN, EPI><<<grid, NUM_THREADS, smem, s>>>(ma, mb, p);
+    gemm_tc_kernel<BN, EPI><<<grid, NUM_THREADS, smem, s>>>(ma, mb, mc, p);
     return cudaGetLastError();
 }
 
@@ -360,22 +391,24 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
         return cudaErrorMisalignedAddress;
     if (a.M == 0) return cudaSuccess;
     const int BN = (a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128;
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc;
     if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, BN)) return cudaErrorInvalidValue;
+    if (a.epi == GEMM_EPI_ADD_F32) mc = ma;   // unused
+    else if (!make_out_map(&mc, a.C, a.M, a.epi == GEMM_EPI_GEGLU ? a.N / 2 : a.N)) return cudaErrorInvalidValue;
     Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status};
     const int tiles = ((a.M + BM - 1) / BM) * (a.N / BN);
     const int grid = tiles < g_num_sms ? tiles : g_num_sms;
     if (BN == 256) {
         switch (a.epi) {
-            case GEMM_EPI_STORE_BF16: return launch_t<256, GEMM_EPI_STORE_BF16>(ma, mb, p, grid, s);
-            case GEMM_EPI_ADD_F32: return launch_t<256, GEMM_EPI_ADD_F32>(ma, mb, p, grid, s);
-            case GEMM_EPI_ROPE_BF16: return launch_t<256, GEMM_EPI_ROPE_BF16>(ma, mb, p, grid, s);
-            default: return launch_t<256, GEMM_EPI_GEGLU>(ma, mb, p, grid, s);
+            case GEMM_EPI_STORE_BF16: return launch_t<256, GEMM_EPI_STORE_BF16>(ma, mb, mc, p, grid, s);
+            case GEMM_EPI_ADD_F32: return launch_t<256, GEMM_EPI_ADD_F32>(ma, mb, mc, p, grid, s);
+            case GEMM_EPI_ROPE_BF16: return launch_t<256, GEMM_EPI_ROPE_BF16>(ma, mb, mc, p, grid, s);
+            default: return launch_t<256, GEMM_EPI_GEGLU>(ma, mb, mc, p, grid, s);
         }
     }
     switch (a.epi) {
-        case GEMM_EPI_STORE_BF16: return launch_t<128, GEMM_EPI_STORE_BF16>(ma, mb, p, grid, s);
-        case GEMM_EPI_ADD_F32: return launch_t<128, GEMM_EPI_ADD_F32>(ma, mb, p, grid, s);
-        default: return launch_t<128, GEMM_EPI_ROPE_BF16>(ma, mb, p, grid, s);
+        case GEMM_EPI_STORE_BF16: return launch_t<128, GEMM_EPI_STORE_BF16>(ma, mb, mc, p, grid, s);
+        case GEMM_EPI_ADD_F32: return launch_t<128, GEMM_EPI_ADD_F32>(ma, mb, mc, p, grid, s);
+        default: return launch_t<128, GEMM_EPI_ROPE_BF16>(ma, mb, mc, p, grid, s);
     }
 }

@@ -225,3 +225,37 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 }  // namespace tc
+
+namespace tc {
+
+// TMA tile store from shared memory (bulk-group completion).  Rows or columns
+// outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+// Wait until all committed bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Write 64 fp32 values as bf16 into row `row` (0..31) of a 32 x 128-byte
+// staging box in the 128-byte swizzle layout (16-byte chunk c of a row lands
+// at chunk c ^ (row & 7)); `box` is 1024-byte aligned.
+__device__ __forceinline__ void stage_row_bf16x64(uint8_t* box, int row, const float* v) {
+    uint8_t* rp = box + row * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 q;
+        q.x = pack_bf16(v[8 * c + 0], v[8 * c + 1]);
+        q.y = pack_bf16(v[8 * c + 2], v[8 * c + 3]);
+        q.z = pack_bf16(v[8 * c + 4], v[8 * c + 5]);
+        q.w = pack_bf16(v[8 * c + 6], v[8 * c + 7]);
+        *reinterpret_cast<uint4*>(rp + ((c ^ (row & 7)) << 4)) = q;
+    }
+}
+
+}  // namespace tc
