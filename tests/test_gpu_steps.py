@@ -1,7 +1,9 @@
 """Each step of the pass, run through the C ABI on the GPU, against the oracle.
 
-Shapes: the tiny encoder (hidden 256) and an odd one (hidden 384, 6 heads,
-GeGLU width 640) whose projections exercise the 128-column GEMM tiles; token
+Shapes: the tiny encoder (hidden 256), an odd one (hidden 384, 6 heads,
+GeGLU width 640) whose projections exercise the 128-column GEMM tiles, and a
+wide one (GeGLU width 1280) whose long-K output projection runs on 192-column
+tiles; token
 counts are ragged (not multiples of the 128-row tiles) and texts straddle
 tile edges.
 """
@@ -17,14 +19,17 @@ from gpu_util import act_dtype, assert_step_close, dev, make_encoder, to_np  # n
 pytestmark = pytest.mark.gpu
 
 ODD = synth.Shape(n_layers=2, hidden=384, n_heads=6, head_dim=64, intermediate=640, vocab=1000)
+# a long GeGLU width: the feed-forward output projection (K = 1280) runs on 192-column tiles
+WIDE = synth.Shape(n_layers=2, hidden=384, n_heads=6, head_dim=64, intermediate=1280, vocab=1000)
 LENGTHS = [1, 2, 63, 64, 65, 66, 129, 127, 3, 300]   # 820 tokens
 
 
-@pytest.fixture(scope="module", params=[("tiny", "fp32"), ("tiny", "bf16"), ("odd", "bf16"), ("odd", "fp32")],
+@pytest.fixture(scope="module", params=[("tiny", "fp32"), ("tiny", "bf16"), ("odd", "bf16"), ("odd", "fp32"),
+                                        ("wide", "bf16")],
                 ids=lambda p: f"{p[0]}-{p[1]}")
 def setup(request, lib):
     name, dt = request.param
-    shape = synth.TINY if name == "tiny" else ODD
+    shape = {"tiny": synth.TINY, "odd": ODD, "wide": WIDE}[name]
     w = synth.make_weights(shape, seed=11, std=0.05)
     enc = make_encoder(shape, dt, w, max_tokens=1024, max_texts=64)
     model = oracle.OracleModel(w, shape, dt)

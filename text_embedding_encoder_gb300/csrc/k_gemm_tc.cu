@@ -36,7 +36,9 @@ using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+// Internal epilogue: the residual add with per-thread loads and stores (no
+// staging), used with 192-column tiles for long-K projections.
+constexpr int EPI_ADD_REG = 4;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 
@@ -51,19 +53,24 @@ struct Params {
 };
 
 // bf16-output epilogues stage each warp's 32 rows x 64 columns in a 4 KB
-// swizzled box (two per warp) and store it with a TMA bulk tensor store.
-template <int EPI>
-constexpr uint32_t staging_bytes() { return EPI == GEMM_EPI_ADD_F32 ? 0u : 4u * 2u * 4096u; }
+// swizzled box (two per warp) and store it with a TMA bulk tensor store.  The
+// residual epilogue stages each warp's whole 32 x BN fp32 slice of the
+// residual (BN/32 boxes of 32 x 32): TMA-loaded, updated in place, TMA-stored.
+template <int BN, int EPI>
+constexpr uint32_t staging_bytes() {
+    return EPI == EPI_ADD_REG ? 0u : (EPI == GEMM_EPI_ADD_F32 ? 4u * (BN / 32) * 4096u : 4u * 2u * 4096u);
+}
 
 template <int BN, int EPI>
 struct Smem {
     static constexpr uint32_t B_BYTES = BN * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = BN == 192 ? 5 : 4;
     static constexpr uint32_t OUT_OFF = STAGES * STAGE_BYTES;
-    static constexpr uint32_t BAR_OFF = OUT_OFF + staging_bytes<EPI>();
-    static constexpr uint32_t N_BARS = 2 * STAGES + 5;
+    static constexpr uint32_t BAR_OFF = OUT_OFF + staging_bytes<BN, EPI>();
+    static constexpr uint32_t N_BARS = 2 * STAGES + 9;   // + one residual-load barrier per epilogue warp
     static constexpr uint32_t TOTAL = BAR_OFF + N_BARS * 8 + 16 + 1024;   // + alignment slack
-    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;   // a power of two >= 2 * BN
 };
 
 template <int BN, int EPI>
@@ -79,14 +86,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     auto bar = [&](int i) { return smem_u32(bars + i); };
     // barrier indices
-    const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, TEMPTY = 2 * STAGES + 2, MMA_DONE = 2 * STAGES + 4;
+    const int FULL = 0, EMPTY = S::STAGES, TFULL = 2 * S::STAGES, TEMPTY = 2 * S::STAGES + 2, MMA_DONE = 2 * S::STAGES + 4,
+              RES = 2 * S::STAGES + 5;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_m = (p.M + BM - 1) / BM, num_n = p.N / BN, num_k = p.K / BK;
     const int num_tiles = num_m * num_n;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S::STAGES; ++s) {
             mbar_init(bar(FULL + s), 1);
             mbar_init(bar(EMPTY + s), 1);
         }
@@ -95,11 +103,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(TEMPTY + a), 128);
         }
         mbar_init(bar(MMA_DONE), 1);
+        for (int w = 0; w < 4; ++w) mbar_init(bar(RES + w), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
-        if (EPI != GEMM_EPI_ADD_F32)
+        if (EPI != EPI_ADD_REG)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC)) : "memory");
     }
     if (warp == 1) {
@@ -117,15 +126,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             uint32_t g = 0;
-            uint32_t armed_parity[STAGES];
-            bool armed[STAGES];
-            for (int s = 0; s < STAGES; ++s) armed[s] = false, armed_parity[s] = 0;
+            uint32_t armed_parity[S::STAGES];
+            bool armed[S::STAGES];
+            for (int s = 0; s < S::STAGES; ++s) armed[s] = false, armed_parity[s] = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 const int n_t = tile % num_n, m_t = tile / num_n;
                 for (int kb = 0; kb < num_k; ++kb, ++g) {
-                    const int s = g % STAGES;
-                    const uint32_t r = g / STAGES;
+                    const int s = g % S::STAGES;
+                    const uint32_t r = g / S::STAGES;
                     if (!mbar_wait(bar(EMPTY + s), (r & 1) ^ 1, abort_flag)) {
                         ok = false;
                         break;
@@ -140,7 +149,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             // no copy may still be landing in shared memory when the CTA exits
-            for (int s = 0; s < STAGES; ++s)
+            for (int s = 0; s < S::STAGES; ++s)
                 if (armed[s]) mbar_wait_drain(bar(FULL + s), armed_parity[s]);
         }
         __syncwarp();
@@ -160,8 +169,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < num_k; ++kb, ++g) {
-                    const int s = g % STAGES;
-                    const uint32_t r = g / STAGES;
+                    const int s = g % S::STAGES;
+                    const uint32_t r = g / S::STAGES;
                     if (!mbar_wait(bar(FULL + s), r & 1, abort_flag)) {
                         ok = false;
                         break;
@@ -189,6 +198,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row_local = quad * 32 + lane;
         uint8_t* stage = smem + S::OUT_OFF + (warp - 2) * 8192;   // this warp's two staging boxes
         uint32_t n_stores = 0;                                     // store groups this warp committed
+        bool res_armed = false;                                    // residual epilogue: a load is in flight
+        uint32_t res_parity = 0;
         // Stage 64 bf16 columns of this warp's 32 rows and store them at (x, y).
         auto store64 = [&](const float* v, int x, int y) {
             uint8_t* box = stage + (n_stores & 1) * 4096;
@@ -221,8 +232,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     store64(v, n_t * BN + g * 64, y_box);
                 }
             } else if constexpr (EPI == GEMM_EPI_ADD_F32) {
-                // the residual chunk is fetched one chunk ahead (the first one
-                // while the tile's MMAs still run) to keep loads in flight
+                // this warp's 32 x BN slice of the residual: TMA-load it (issued
+                // before the accumulator is ready, once the previous tile's
+                // stores have read the boxes), add in place, TMA-store it
+                uint8_t* slice = smem + S::OUT_OFF + (warp - 2) * (BN / 32) * 4096;
+                const uint32_t rbar = bar(RES + (warp - 2));
+                if (lane == 0) {
+                    bulk_wait_read<0>();
+                    mbar_expect_tx(rbar, (BN / 32) * 4096);
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+                        tma_load_2d(smem_u32(slice + c * 4096), &tmC, n_t * BN + c * 32, y_box, rbar);
+                }
+                res_armed = true;
+                res_parity = it & 1;
+                if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
+                tc_fence_after();
+                if (!mbar_wait(rbar, it & 1, abort_flag)) break;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    uint8_t* rp = slice + c * 4096 + lane * 128;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        float4* q = reinterpret_cast<float4*>(rp + ((k ^ (lane & 7)) << 4));
+                        float4 o = *q;
+                        o.x += v[4 * k + 0];
+                        o.y += v[4 * k + 1];
+                        o.z += v[4 * k + 2];
+                        o.w += v[4 * k + 3];
+                        *q = o;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, smem_u32(slice + c * 4096), n_t * BN + c * 32, y_box);
+                        bulk_commit();
+                    }
+                }
+            } else if constexpr (EPI == EPI_ADD_REG) {
+                // residual chunk fetched one chunk ahead (the first one while
+                // the tile's MMAs still run) to keep loads in flight
                 float* C = reinterpret_cast<float*>(p.C) + (size_t)gr * p.N + n_t * BN;
                 float4 cur[8], nxt[8];
 #pragma unroll
@@ -305,6 +356,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             mbar_arrive(bar(TEMPTY + acc));
         }
+        if (EPI == GEMM_EPI_ADD_F32 && res_armed) mbar_wait_drain(bar(RES + (warp - 2)), res_parity);
         if (lane == 0) bulk_wait_all();   // stores complete before the CTA exits
     }
 
@@ -341,13 +393,14 @@ void init_once() {
     if (e != cudaSuccess) g_init_err = e;
 }
 
-// Output map: bf16 [rows, cols], boxes of 32 rows x 64 columns, 128B swizzle.
-bool make_out_map(CUtensorMap* map, const void* ptr, int rows, int cols) {
+// Output map [rows, cols] of 2- or 4-byte elements, boxes of 32 rows x 128 bytes, 128B swizzle.
+bool make_out_map(CUtensorMap* map, const void* ptr, int rows, int cols, CUtensorMapDataType dt, int box_cols) {
+    const int esz = dt == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, 32};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, 32};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+    CUresult r = g_encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -390,18 +443,30 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.W) | reinterpret_cast<uintptr_t>(a.C)) & 15)
         return cudaErrorMisalignedAddress;
     if (a.M == 0) return cudaSuccess;
-    const int BN = (a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128;
+    // Residual add: short-K projections stage a whole 32 x 128 fp32 slice per
+    // warp through TMA (128-column tiles); long-K ones keep deep pipelines on
+    // 192-column tiles with per-thread residual loads.  Other epilogues use
+    // 256-column tiles where N allows.
+    const bool add_reg = a.epi == GEMM_EPI_ADD_F32 && a.K > 1024 && a.N % 192 == 0;
+    const int BN = add_reg ? 192
+                 : (a.epi == GEMM_EPI_ADD_F32 ? 128 : ((a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128));
     CUtensorMap ma, mb, mc;
     if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, BN)) return cudaErrorInvalidValue;
-    if (a.epi == GEMM_EPI_ADD_F32) mc = ma;   // unused
-    else if (!make_out_map(&mc, a.C, a.M, a.epi == GEMM_EPI_GEGLU ? a.N / 2 : a.N)) return cudaErrorInvalidValue;
+    if (add_reg) {
+        mc = ma;   // unused
+    } else if (a.epi == GEMM_EPI_ADD_F32) {
+        if (!make_out_map(&mc, a.C, a.M, a.N, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32)) return cudaErrorInvalidValue;
+    } else if (!make_out_map(&mc, a.C, a.M, a.epi == GEMM_EPI_GEGLU ? a.N / 2 : a.N, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                             64)) {
+        return cudaErrorInvalidValue;
+    }
     Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status};
     const int tiles = ((a.M + BM - 1) / BM) * (a.N / BN);
     const int grid = tiles < g_num_sms ? tiles : g_num_sms;
+    if (add_reg) return launch_t<192, EPI_ADD_REG>(ma, mb, mc, p, grid, s);
     if (BN == 256) {
         switch (a.epi) {
             case GEMM_EPI_STORE_BF16: return launch_t<256, GEMM_EPI_STORE_BF16>(ma, mb, mc, p, grid, s);
-            case GEMM_EPI_ADD_F32: return launch_t<256, GEMM_EPI_ADD_F32>(ma, mb, mc, p, grid, s);
             case GEMM_EPI_ROPE_BF16: return launch_t<256, GEMM_EPI_ROPE_BF16>(ma, mb, mc, p, grid, s);
             default: return launch_t<256, GEMM_EPI_GEGLU>(ma, mb, mc, p, grid, s);
         }
