@@ -27,18 +27,26 @@ sys.path.insert(0, ROOT)
 
 METRIC = "encoded tokens/sec (packed varlen, bf16) at 310m shape; % of tensor peak"
 UNIT = "tokens/s"
+SHAPE_NAME = "310m-shape encoder (25 layers, hidden 768, 12 heads, GeGLU 3072)"
+# workload name -> (tokens per batch, description); sweep32k is the headline
+WORKLOADS = {
+    "sweep32k": (32768, "packed sweep batches of 32768 tokens (log-uniform text lengths 8-1024)"),
+    "sweep8k": (8192, "packed sweep batches of 8192 tokens (log-uniform text lengths 8-1024)"),
+    "sweep2k": (2048, "packed sweep batches of 2048 tokens (log-uniform text lengths 8-1024)"),
+    "long": (65536, "long documents: 8 texts of 8192 tokens"),
+}
 BUDGET = 32768
-WORKLOAD = "310m-shape encoder (25 layers, hidden 768, 12 heads, GeGLU 3072), packed sweep batches of 32768 tokens"
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-leg", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="sweep32k", choices=sorted(WORKLOADS))
     return ap.parse_args()
 
 
@@ -50,6 +58,23 @@ def peaks():
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# DRAM bytes (read + write) per GEMM launch, the mean over the four projections,
+# from one ncu capture of each projection at 32768 tokens.  Valid only for the
+# kernel sources with this digest; otherwise reported as null.
+GEMM_TRAFFIC_BYTES = 230.4e6
+GEMM_TRAFFIC_SOURCES = ['text_embedding_encoder_gb300/csrc/k_gemm_tc.cu', 'text_embedding_encoder_gb300/csrc/tc_ptx.cuh', 'text_embedding_encoder_gb300/csrc/gemm_tc.cuh']
+GEMM_TRAFFIC_DIGEST = "e6e715db38e35f68"
+
+
+def gemm_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return GEMM_TRAFFIC_BYTES if h.hexdigest()[:16] == GEMM_TRAFFIC_DIGEST else None
 
 
 def gemm_flops_per_token(shape):
@@ -117,7 +142,7 @@ class ClockSampler:
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -167,15 +192,19 @@ def run_ours(args):
     torch.cuda.set_device(local)
     shape = synth.RURI_310M
 
-    # workload: the 20 sweep batches at 32768 tokens; rank r takes batches r, r+N, ...
+    # workload: the 20 seeded batches of the chosen size; rank r takes batches r, r+N, ...
+    budget, desc = WORKLOADS[args.workload]
     batches = []
     for b in range(rank, synth.SWEEP_BATCHES * world, world):
-        ids, cu = synth.sweep_batch(BUDGET, b % synth.SWEEP_BATCHES + (b // synth.SWEEP_BATCHES) * 100,
-                                    shape.vocab)
+        if args.workload == "long":
+            ids, cu = synth.make_batch(synth.LONG_DOC_LENGTHS, shape.vocab, seed=b)
+        else:
+            ids, cu = synth.sweep_batch(budget, b % synth.SWEEP_BATCHES + (b // synth.SWEEP_BATCHES) * 100,
+                                        shape.vocab)
         batches.append((ids, cu))
     max_texts = max(len(cu) - 1 for _, cu in batches)
     weights = synth.make_weights(shape, seed=0)
-    enc = binding.Encoder(shape, "bf16", max_tokens=BUDGET, max_texts=max_texts, device=local)
+    enc = binding.Encoder(shape, "bf16", max_tokens=budget, max_texts=max_texts, device=local)
     enc.load_weights(weights)
     del weights
 
@@ -217,7 +246,7 @@ def run_ours(args):
         t = torch.tensor([ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    tokens_per_rank = BUDGET * args.steps
+    tokens_per_rank = budget * args.steps
     value = tokens_per_rank * world / (ms / 1e3)
 
     # end to end through the public host API: pinned host inputs, H2D inside,
@@ -255,7 +284,7 @@ def run_ours(args):
     achieved_tflops = gemm_flops_avg / (gemm_ms_avg / 1e3) / 1e12 if g["launches"] else None
     peak = pk["bf16_tflops_sustained"]
     launches = sum(v["launches"] for v in prof.values())
-    flops_per_token = gemm_flops_per_token(shape) + prof["attention"]["flops"] / (BUDGET * args.steps)
+    flops_per_token = gemm_flops_per_token(shape) + prof["attention"]["flops"] / (budget * args.steps)
     kernel_share = {k: round(v["total_ms"] / max(1e-9, sum(x["total_ms"] for x in prof.values())), 4)
                     for k, v in prof.items() if v["launches"]}
 
@@ -272,7 +301,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights, uniform ids, log-uniform text lengths)",
-        "config": {"workload": WORKLOAD, "global_batch": BUDGET * world, "tokens_per_gpu_step": BUDGET,
+        "config": {"workload": f"{SHAPE_NAME}, {desc}", "workload_id": args.workload,
+                   "global_batch": budget * world, "tokens_per_gpu_step": budget,
                    "texts_per_batch_mean": round(float(np.mean([len(cu) - 1 for _, cu in batches])), 1),
                    "batches": len(batches), "parallelism": f"dp{world} (texts sharded, no collective)",
                    "l2": "inputs larger than L2 (weights 472 MB + activations per pass)"},
@@ -285,7 +315,8 @@ def run_ours(args):
                      "achieved": round(achieved_tflops, 1) if achieved_tflops else None,
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved_tflops / peak, 4) if achieved_tflops else None,
-                     "peak_source": f"{pk['source']} sustained bf16", "traffic": None},
+                     "peak_source": f"{pk['source']} sustained bf16", "traffic": gemm_traffic(),
+                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)"},
         "kernel_share": kernel_share,
         "kernel_ms_per_step": {k: round(v["total_ms"] / args.steps, 4) for k, v in prof.items() if v["launches"]},
     }
@@ -344,8 +375,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "sample_per_step": "one text (<= 160 tokens) "
-                                        "of sweep batch 0"},
+        "data": "synthetic", "config": {"workload": f"{SHAPE_NAME}, {WORKLOADS['sweep32k'][1]}",
+                                        "workload_id": "sweep32k",
+                                        "sample_per_step": "one text (<= 160 tokens) of sweep batch 0"},
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{args.steps} texts, {tokens} tokens of sweep batch 0"},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -3,8 +3,9 @@
 //
 // Method: tensai page "テキスト埋め込み", §何が動くか (エンコーダ, プーリング,
 // packing paragraph).  All of these are bandwidth-bound: rows are read with
-// 16-byte vector loads, one warp (LayerNorm) or one block (pool) per row /
-// text, reductions by warp shuffles.
+// 16-byte vector loads, one warp per row (LayerNorm) or one block per token
+// (gather); the pool reduces 64-row chunks of each text in parallel, then
+// combines each text's chunks in order; reductions by warp shuffles.
 #include "tee_internal.cuh"
 
 #include <mutex>
