@@ -124,6 +124,16 @@ int tee_op_w8a8_partials(tee_ctx* ctx, int layer, int which, const int8_t* d_q, 
  * of projection `which` of `layer` to host buffers.  Synchronous. */
 int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d);
 
+/* Failure-detection self-test.  Launches one thread that waits, with the same
+ * bounded mbarrier wait the tensor-core GEMM and attention pipelines use, on a
+ * barrier that nothing completes, and gives up after `wait_cycles` SM clock
+ * cycles (clamped to [1e3, 1e10]).  The expiry sets the timeout bit of the
+ * context's status word, as a stalled pipeline would, so the next
+ * tee_device_status() returns TEE_ETIMEOUT (and clears it).  The kernel
+ * returns once the limit expires; the context stays usable.  Asynchronous on
+ * `stream`. */
+int tee_selftest_wait_timeout(tee_ctx* ctx, long long wait_cycles, void* stream);
+
 /* Synchronise the context's device status word: TEE_OK, or TEE_EINVAL if a
  * kernel met an out-of-range token id since the last call (the word is then
  * cleared), or TEE_ETIMEOUT if a bounded device wait gave up. */

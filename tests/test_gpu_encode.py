@@ -191,3 +191,19 @@ def test_host_validation_and_recovery(lib, tiny_weights):
     assert enc.device_status() == binding.TEE_EINVAL
     assert enc.device_status() == 0
     enc.close()
+
+
+def test_bounded_wait_expiry_is_reported(lib, tiny_weights):
+    """A device wait that runs out (on a barrier nothing completes, ~1 ms limit)
+    is reported as TEE_ETIMEOUT through the status word, once, and the context
+    keeps working afterwards."""
+    enc = make_encoder(synth.TINY, "bf16", tiny_weights, max_tokens=512, max_texts=16)
+    assert enc.device_status() == binding.TEE_OK
+    enc.check(lib.tee_selftest_wait_timeout(enc.ctx, 2_000_000, None))
+    assert enc.device_status() == binding.TEE_ETIMEOUT
+    assert enc.device_status() == binding.TEE_OK
+    ids, cu = synth.make_batch(synth.TINY_LENGTHS, synth.TINY.vocab, seed=0)
+    got = enc.encode(ids, cu)
+    ref = oracle.encode_packed(ids, cu, oracle.OracleModel(tiny_weights, synth.TINY, "bf16"))
+    assert_embeddings_close(got, ref, "bf16")
+    enc.close()

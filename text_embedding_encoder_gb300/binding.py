@@ -84,6 +84,7 @@ SIGNATURES = {
     "tee_weight_codes": (_i, [_ctx, _i, _i, _vp, _vp]),
     "tee_device_status": (_i, [_ctx]),
     "tee_pool_l2_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp]),
+    "tee_selftest_wait_timeout": (_i, [_ctx, ctypes.c_longlong, _vp]),
 }
 
 _LIB = None

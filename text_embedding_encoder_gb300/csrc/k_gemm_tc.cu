@@ -6,9 +6,10 @@
 // token activations and W [N, K] the weights, both bf16 and K-contiguous.
 //
 // Design (one CTA per SM, persistent over output tiles):
-//   * tile 128 x BN (BN = 256, or 128 when N is not a multiple of 256), K step 64
-//     (one 128-byte swizzle atom); 4-stage shared-memory ring filled by TMA
-//     (cp.async.bulk.tensor, 128B swizzle, out-of-range rows zero-filled).
+//   * tile 128 x BN, K step 64 (one 128-byte swizzle atom); 4-stage
+//     shared-memory ring filled by TMA (cp.async.bulk.tensor, 128B swizzle,
+//     out-of-range rows zero-filled).  BN = 256 for the bf16-output
+//     projections, 128 (short K) or 192 (long K) for the residual ones.
 //   * warp 0 lane 0: TMA producer.  warp 1: TMEM allocator, lane 0 issues
 //     tcgen05.mma (M=128, N=BN, K=16) and commits to mbarriers.  warps 2-5:
 //     epilogue, each reading its 32-lane TMEM quadrant with tcgen05.ld.
@@ -17,7 +18,9 @@
 //   * tiles are ordered with the N index fastest, so CTAs running at the same
 //     time share their A rows in L2.
 //   * epilogues fused into the store: bf16 store, fp32 residual add, RoPE on
-//     the q/k columns (positions restart per text), GeGLU gate.
+//     the q/k columns (positions restart per text), GeGLU gate.  Outputs go
+//     out through per-warp swizzled shared-memory boxes and TMA bulk tensor
+//     stores; the residual is TMA-loaded into those boxes, updated in place.
 //   * every mbarrier wait is bounded: after ~2 s the CTA raises an abort flag,
 //     drains its in-flight copies and MMAs, frees TMEM, sets the timeout bit
 //     of the status word and returns.
@@ -36,9 +39,6 @@ using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-// Internal epilogue: the residual add with per-thread loads and stores (no
-// staging), used with 192-column tiles for long-K projections.
-constexpr int EPI_ADD_REG = 4;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 
@@ -56,16 +56,21 @@ struct Params {
 // swizzled box (two per warp) and store it with a TMA bulk tensor store.  The
 // residual epilogue stages each warp's whole 32 x BN fp32 slice of the
 // residual (BN/32 boxes of 32 x 32): TMA-loaded, updated in place, TMA-stored.
+// Residual epilogue: 32-column boxes staged per round (the whole 32 x BN slice
+// for BN <= 128, half of it for BN = 192).
+template <int BN>
+__host__ __device__ constexpr int res_round_boxes() { return BN / 32 <= 4 ? BN / 32 : BN / 64; }
+
 template <int BN, int EPI>
 constexpr uint32_t staging_bytes() {
-    return EPI == EPI_ADD_REG ? 0u : (EPI == GEMM_EPI_ADD_F32 ? 4u * (BN / 32) * 4096u : 4u * 2u * 4096u);
+    return EPI == GEMM_EPI_ADD_F32 ? 4u * res_round_boxes<BN>() * 4096u : 4u * 2u * 4096u;
 }
 
 template <int BN, int EPI>
 struct Smem {
     static constexpr uint32_t B_BYTES = BN * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 192 ? 5 : 4;
+    static constexpr int STAGES = 4;
     static constexpr uint32_t OUT_OFF = STAGES * STAGE_BYTES;
     static constexpr uint32_t BAR_OFF = OUT_OFF + staging_bytes<BN, EPI>();
     static constexpr uint32_t N_BARS = 2 * STAGES + 9;   // + one residual-load barrier per epilogue warp
@@ -108,8 +113,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
-        if (EPI != EPI_ADD_REG)
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -198,8 +202,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row_local = quad * 32 + lane;
         uint8_t* stage = smem + S::OUT_OFF + (warp - 2) * 8192;   // this warp's two staging boxes
         uint32_t n_stores = 0;                                     // store groups this warp committed
-        bool res_armed = false;                                    // residual epilogue: a load is in flight
-        uint32_t res_parity = 0;
+        bool res_armed = false;                                    // residual epilogue: a load was issued
+        uint32_t res_parity = 0;                                   // ... with this phase parity
+        uint32_t res_phase = 0;                                    // residual rounds completed by this warp
         // Stage 64 bf16 columns of this warp's 32 rows and store them at (x, y).
         auto store64 = [&](const float* v, int x, int y) {
             uint8_t* box = stage + (n_stores & 1) * 4096;
@@ -232,80 +237,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     store64(v, n_t * BN + g * 64, y_box);
                 }
             } else if constexpr (EPI == GEMM_EPI_ADD_F32) {
-                // this warp's 32 x BN slice of the residual: TMA-load it (issued
-                // before the accumulator is ready, once the previous tile's
-                // stores have read the boxes), add in place, TMA-store it
-                uint8_t* slice = smem + S::OUT_OFF + (warp - 2) * (BN / 32) * 4096;
+                // this warp's 32 x BN slice of the residual, in rounds of RB
+                // 32-column boxes: TMA-load a round (the first one before the
+                // accumulator is ready, each once the previous stores have read
+                // the boxes), add in place, TMA-store it
+                constexpr int RB = res_round_boxes<BN>();
+                constexpr int ROUNDS = (BN / 32) / RB;
+                uint8_t* slice = smem + S::OUT_OFF + (warp - 2) * RB * 4096;
                 const uint32_t rbar = bar(RES + (warp - 2));
-                if (lane == 0) {
-                    bulk_wait_read<0>();
-                    mbar_expect_tx(rbar, (BN / 32) * 4096);
-#pragma unroll
-                    for (int c = 0; c < BN / 32; ++c)
-                        tma_load_2d(smem_u32(slice + c * 4096), &tmC, n_t * BN + c * 32, y_box, rbar);
-                }
-                res_armed = true;
-                res_parity = it & 1;
-                if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
-                tc_fence_after();
-                if (!mbar_wait(rbar, it & 1, abort_flag)) break;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(taddr + c * 32, v);
-                    uint8_t* rp = slice + c * 4096 + lane * 128;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float4* q = reinterpret_cast<float4*>(rp + ((k ^ (lane & 7)) << 4));
-                        float4 o = *q;
-                        o.x += v[4 * k + 0];
-                        o.y += v[4 * k + 1];
-                        o.z += v[4 * k + 2];
-                        o.w += v[4 * k + 3];
-                        *q = o;
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+                auto issue_round = [&](int rd) {
                     if (lane == 0) {
-                        tma_store_2d(&tmC, smem_u32(slice + c * 4096), n_t * BN + c * 32, y_box);
-                        bulk_commit();
-                    }
-                }
-            } else if constexpr (EPI == EPI_ADD_REG) {
-                // residual chunk fetched one chunk ahead (the first one while
-                // the tile's MMAs still run) to keep loads in flight
-                float* C = reinterpret_cast<float*>(p.C) + (size_t)gr * p.N + n_t * BN;
-                float4 cur[8], nxt[8];
+                        bulk_wait_read<0>();
+                        mbar_expect_tx(rbar, RB * 4096);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    cur[i] = valid ? reinterpret_cast<const float4*>(C)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int c = 0; c < RB; ++c)
+                            tma_load_2d(smem_u32(slice + c * 4096), &tmC, n_t * BN + (rd * RB + c) * 32, y_box, rbar);
+                    }
+                    res_armed = true;
+                    res_parity = res_phase & 1;
+                };
+                issue_round(0);
                 if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
                 tc_fence_after();
+                bool ok = true;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    if (c + 1 < BN / 32) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            nxt[i] = valid ? reinterpret_cast<const float4*>(C + (c + 1) * 32)[i]
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int rd = 0; rd < ROUNDS && ok; ++rd) {
+                    if (rd > 0) issue_round(rd);
+                    if (!mbar_wait(rbar, res_phase & 1, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                    float v[32];
-                    tmem_ld32(taddr + c * 32, v);
-                    if (valid) {
-                        float4* d = reinterpret_cast<float4*>(C + c * 32);
+                    ++res_phase;
+#pragma unroll 1
+                    for (int c = 0; c < RB; ++c) {
+                        float v[32];
+                        tmem_ld32(taddr + (rd * RB + c) * 32, v);
+                        uint8_t* rp = slice + c * 4096 + lane * 128;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            float4 o = cur[i];
-                            o.x += v[4 * i + 0];
-                            o.y += v[4 * i + 1];
-                            o.z += v[4 * i + 2];
-                            o.w += v[4 * i + 3];
-                            d[i] = o;
+                        for (int k = 0; k < 8; ++k) {
+                            float4* q = reinterpret_cast<float4*>(rp + ((k ^ (lane & 7)) << 4));
+                            float4 o = *q;
+                            o.x += v[4 * k + 0];
+                            o.y += v[4 * k + 1];
+                            o.z += v[4 * k + 2];
+                            o.w += v[4 * k + 3];
+                            *q = o;
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, smem_u32(slice + c * 4096), n_t * BN + (rd * RB + c) * 32, y_box);
+                            bulk_commit();
                         }
                     }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
                 }
+                if (!ok) break;
             } else if constexpr (EPI == GEMM_EPI_ROPE_BF16) {
                 // q and k tiles (columns < 2*hidden; 2*hidden is a multiple of
                 // the tile width) rotate every head with the row's cos/sin,
@@ -443,18 +429,16 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.W) | reinterpret_cast<uintptr_t>(a.C)) & 15)
         return cudaErrorMisalignedAddress;
     if (a.M == 0) return cudaSuccess;
-    // Residual add: short-K projections stage a whole 32 x 128 fp32 slice per
-    // warp through TMA (128-column tiles); long-K ones keep deep pipelines on
-    // 192-column tiles with per-thread residual loads.  Other epilogues use
-    // 256-column tiles where N allows.
-    const bool add_reg = a.epi == GEMM_EPI_ADD_F32 && a.K > 1024 && a.N % 192 == 0;
-    const int BN = add_reg ? 192
+    // Residual add: short-K projections stage each warp's whole 32 x 128 fp32
+    // slice through TMA (128-column tiles, many tiles for N = 768); long-K ones
+    // use 192-column tiles (less operand traffic per FLOP) and stage the slice
+    // in two rounds.  Other epilogues use 256-column tiles where N allows.
+    const bool add_wide = a.epi == GEMM_EPI_ADD_F32 && a.K > 1024 && a.N % 192 == 0;
+    const int BN = add_wide ? 192
                  : (a.epi == GEMM_EPI_ADD_F32 ? 128 : ((a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128));
     CUtensorMap ma, mb, mc;
     if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, BN)) return cudaErrorInvalidValue;
-    if (add_reg) {
-        mc = ma;   // unused
-    } else if (a.epi == GEMM_EPI_ADD_F32) {
+    if (a.epi == GEMM_EPI_ADD_F32) {
         if (!make_out_map(&mc, a.C, a.M, a.N, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32)) return cudaErrorInvalidValue;
     } else if (!make_out_map(&mc, a.C, a.M, a.epi == GEMM_EPI_GEGLU ? a.N / 2 : a.N, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                              64)) {
@@ -463,7 +447,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status};
     const int tiles = ((a.M + BM - 1) / BM) * (a.N / BN);
     const int grid = tiles < g_num_sms ? tiles : g_num_sms;
-    if (add_reg) return launch_t<192, EPI_ADD_REG>(ma, mb, mc, p, grid, s);
+    if (add_wide) return launch_t<192, GEMM_EPI_ADD_F32>(ma, mb, mc, p, grid, s);
     if (BN == 256) {
         switch (a.epi) {
             case GEMM_EPI_STORE_BF16: return launch_t<256, GEMM_EPI_STORE_BF16>(ma, mb, mc, p, grid, s);

@@ -722,6 +722,15 @@ int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d
     return TEE_OK;
 }
 
+int tee_selftest_wait_timeout(tee_ctx* ctx, long long wait_cycles, void* stream) {
+    if (!ctx) return TEE_EINVAL;
+    if (wait_cycles < 1000) wait_cycles = 1000;
+    if (wait_cycles > 10000000000LL) wait_cycles = 10000000000LL;
+    CK(cudaSetDevice(ctx->device));
+    CK(launch_selftest_wait(wait_cycles, ctx->d_status, (cudaStream_t)stream));
+    return TEE_OK;
+}
+
 int tee_device_status(tee_ctx* ctx) {
     if (!ctx) return TEE_EINVAL;
     CK(cudaSetDevice(ctx->device));

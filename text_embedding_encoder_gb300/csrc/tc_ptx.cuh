@@ -37,18 +37,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Wait for the phase of `parity` to complete.  Gives up (returning false) when
-// another role raised the abort flag or after WAIT_CYCLES, raising it.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// another role raised the abort flag or after `limit` SM clock cycles, raising it.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > WAIT_CYCLES) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return mbar_wait_limit(bar, parity, abort_flag, WAIT_CYCLES);
 }
 // Bounded wait that ignores the abort flag (used to drain in-flight work).
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {

@@ -115,6 +115,10 @@ cudaError_t launch_attention_simple(const void* qkv, bool bf16_act, const int32_
 cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, const int4* d_items, int n_items,
                                 bool is_global, int window, void* o, unsigned int* status, cudaStream_t s);
 
+// Self-test of the bounded waits: a wait on a barrier nothing completes, limited
+// to `limit_cycles`; its expiry sets TEE_STATUS_TIMEOUT in `status`.
+cudaError_t launch_selftest_wait(long long limit_cycles, unsigned int* status, cudaStream_t s);
+
 // SIMT GEMM, C = A W^T.  epi 0: store C in A's type; epi 1: add into float C.
 cudaError_t launch_gemm_simt(const void* A, const void* W, void* C, bool bf16_in, int M, int N, int K, int epi,
                              cudaStream_t s);
