@@ -59,7 +59,8 @@ constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
 constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = B_KVF + KV_STAGES, B_SF = B_KVE + KV_STAGES, B_SE = B_SF + 2,
               B_PF = B_SE + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_DONE = B_OE + 2, N_BARS = B_DONE + 1;
 constexpr uint32_t OFF_RED = OFF_BAR + N_BARS * 8 + 16;       // row-maximum exchange: [2 tiles][2 halves][128 rows]
-constexpr uint32_t SMEM_TOTAL = OFF_RED + 2 * 2 * 128 * 4 + 1024;
+constexpr uint32_t OFF_REDL = OFF_RED + 2 * 2 * 128 * 4;       // row-sum exchange: [2 halves][128 rows]
+constexpr uint32_t SMEM_TOTAL = OFF_REDL + 2 * 128 * 4 + 1024;
 constexpr uint32_t TMEM_COLS = 512;                 // S: 2 x 128 columns, O: 2 x 64 columns
 constexpr uint32_t TM_S = 0, TM_O = 256;
 
@@ -234,7 +235,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float O[HD / 2];
 
         auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
-        auto o_phase = [&](uint32_t tt, float corr) -> bool {
+        // O_dst = O_dst * corr + (P_tt V_tt)[this thread's 32 dimensions]
+        auto o_phase = [&](uint32_t tt, float corr, float (&O_dst)[HD / 2]) -> bool {
             const int ob = tt & 1;
             if (!mbar_wait(bar(B_OF + ob), (tt >> 1) & 1, abort_flag)) return false;
             tc_fence_after();
@@ -243,7 +245,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             mbar_arrive(bar(B_OE + ob));
 #pragma unroll
-            for (int d = 0; d < HD / 2; ++d) O[d] = fmaf(O[d], corr, pv[d]);
+            for (int d = 0; d < HD / 2; ++d) O_dst[d] = fmaf(O_dst[d], corr, pv[d]);
+            return true;
+        };
+
+        // A finished unit waits for the P V of its last tile; that wait is
+        // deferred past the next unit's first softmax so it overlaps it.
+        float* red_l = reinterpret_cast<float*>(smem + OFF_REDL);   // [2][128]
+        bool pend = false;
+        float O_p[HD / 2];
+        float l_p = 0.f, corr_p = 1.f;
+        uint32_t t_p = 0;
+        bf16* dst_p = nullptr;
+        auto finalize = [&]() -> bool {
+            if (!o_phase(t_p, corr_p, O_p)) return false;
+            red_l[half * 128 + r] = l_p;                  // the row sum is split between the two halves
+            pair_sync();
+            const float l_tot = l_p + red_l[(half ^ 1) * 128 + r];
+            pair_sync();
+            if (dst_p) {
+                const float inv = 1.0f / l_tot;
+                float out[32];
+#pragma unroll
+                for (int d = 0; d < 32; ++d) out[d] = O_p[d] * inv;
+                store_bf16x32(dst_p, out);
+            }
+            pend = false;
             return true;
         };
 
@@ -307,30 +334,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_arrive(bar(B_PF + sb));
                 l = l * corr + sum;
                 m = m_new;
-                if (kt >= 1 && !o_phase(t - 1, corr_pending)) {
+                if (kt >= 1) {
+                    if (!o_phase(t - 1, corr_pending, O)) {
+                        ok = false;
+                        break;
+                    }
+                } else if (pend && !finalize()) {
                     ok = false;
                     break;
                 }
                 corr_pending = corr;
             }
-            if (!ok || !o_phase(t - 1, corr_pending)) {
-                ok = false;
-                break;
-            }
-            // the row sum is split between the two halves
-            float* red_l = red + (t & 1) * 256;
-            red_l[half * 128 + r] = l;
-            pair_sync();
-            l += red_l[(half ^ 1) * 128 + r];
-            pair_sync();
-            if (r < q_len) {
-                const float inv = 1.0f / l;
-                float out[32];
+            if (!ok) break;
 #pragma unroll
-                for (int d = 0; d < 32; ++d) out[d] = O[d] * inv;
-                store_bf16x32(p.o + (size_t)qg * p.hidden + head * HD + half * 32, out);
-            }
+            for (int d = 0; d < HD / 2; ++d) O_p[d] = O[d];
+            l_p = l;
+            corr_p = corr_pending;
+            t_p = t - 1;
+            dst_p = r < q_len ? p.o + (size_t)qg * p.hidden + head * HD + half * 32 : nullptr;
+            pend = true;
         }
+        if (ok && pend) finalize();
     }
 
     tc_fence_before();
