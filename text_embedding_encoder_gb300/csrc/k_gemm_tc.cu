@@ -56,8 +56,8 @@ struct Params {
 // swizzled box (two per warp) and store it with a TMA bulk tensor store.  The
 // residual epilogue stages each warp's whole 32 x BN fp32 slice of the
 // residual (BN/32 boxes of 32 x 32): TMA-loaded, updated in place, TMA-stored.
-// Residual epilogue: 32-column boxes staged per round (the whole 32 x BN slice
-// for BN <= 128, half of it for BN = 192).
+// Residual epilogue: 32-column staging boxes per warp (a ring over the warp's
+// chunks: 4 for BN = 128, 3 for BN = 192).
 template <int BN>
 __host__ __device__ constexpr int res_round_boxes() { return BN / 32 <= 4 ? BN / 32 : BN / 64; }
 
@@ -73,7 +73,7 @@ struct Smem {
     static constexpr int STAGES = 4;
     static constexpr uint32_t OUT_OFF = STAGES * STAGE_BYTES;
     static constexpr uint32_t BAR_OFF = OUT_OFF + staging_bytes<BN, EPI>();
-    static constexpr uint32_t N_BARS = 2 * STAGES + 9;   // + one residual-load barrier per epilogue warp
+    static constexpr uint32_t N_BARS = 2 * STAGES + 5 + 16;   // + one residual barrier per staging box (4 x 4)
     static constexpr uint32_t TOTAL = BAR_OFF + N_BARS * 8 + 16 + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;   // a power of two >= 2 * BN
 };
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(TEMPTY + a), 128);
         }
         mbar_init(bar(MMA_DONE), 1);
-        for (int w = 0; w < 4; ++w) mbar_init(bar(RES + w), 1);
+        for (int w = 0; w < 16; ++w) mbar_init(bar(RES + w), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -202,9 +202,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row_local = quad * 32 + lane;
         uint8_t* stage = smem + S::OUT_OFF + (warp - 2) * 8192;   // this warp's two staging boxes
         uint32_t n_stores = 0;                                     // store groups this warp committed
-        bool res_armed = false;                                    // residual epilogue: a load was issued
-        uint32_t res_parity = 0;                                   // ... with this phase parity
-        uint32_t res_phase = 0;                                    // residual rounds completed by this warp
+        // residual epilogue: chunk g (32 columns; g counts this warp's chunks
+        // over its tiles) is staged in box g % RB; lane 0 issues its load RB - 1
+        // chunks ahead, as soon as the store that last used the box has read it
+        constexpr int RB = res_round_boxes<BN>();
+        constexpr int NC = BN / 32;
+        uint8_t* rslice = smem + S::OUT_OFF + (warp - 2) * RB * 4096;
+        int last_issued[4] = {-1, -1, -1, -1};                     // lane 0: last chunk loaded into each box
+        int res_done = 0;                                          // chunks consumed by this warp
+        auto res_bar = [&](int b) { return bar(RES + (warp - 2) * 4 + b); };
+        auto issue_res_load = [&](int g) {                         // lane 0; box g % RB is free
+            const int k = g / NC, c = g % NC;
+            const int tile = blockIdx.x + k * gridDim.x;
+            if (tile >= num_tiles) return;
+            const int b = g % RB;
+            mbar_expect_tx(res_bar(b), 4096);
+            tma_load_2d(smem_u32(rslice + b * 4096), &tmC, (tile % num_n) * BN + c * 32, (tile / num_n) * BM + quad * 32,
+                        res_bar(b));
+            last_issued[b] = g;
+        };
         // Stage 64 bf16 columns of this warp's 32 rows and store them at (x, y).
         auto store64 = [&](const float* v, int x, int y) {
             uint8_t* box = stage + (n_stores & 1) * 4096;
@@ -237,57 +253,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     store64(v, n_t * BN + g * 64, y_box);
                 }
             } else if constexpr (EPI == GEMM_EPI_ADD_F32) {
-                // this warp's 32 x BN slice of the residual, in rounds of RB
-                // 32-column boxes: TMA-load a round (the first one before the
-                // accumulator is ready, each once the previous stores have read
-                // the boxes), add in place, TMA-store it
-                constexpr int RB = res_round_boxes<BN>();
-                constexpr int ROUNDS = (BN / 32) / RB;
-                uint8_t* slice = smem + S::OUT_OFF + (warp - 2) * RB * 4096;
-                const uint32_t rbar = bar(RES + (warp - 2));
-                auto issue_round = [&](int rd) {
-                    if (lane == 0) {
-                        bulk_wait_read<0>();
-                        mbar_expect_tx(rbar, RB * 4096);
-#pragma unroll
-                        for (int c = 0; c < RB; ++c)
-                            tma_load_2d(smem_u32(slice + c * 4096), &tmC, n_t * BN + (rd * RB + c) * 32, y_box, rbar);
-                    }
-                    res_armed = true;
-                    res_parity = res_phase & 1;
-                };
-                issue_round(0);
+                // this warp's 32 x BN slice of the residual, one 32-column box
+                // per chunk: the box was TMA-loaded ahead of time, is updated in
+                // place, TMA-stored, and then refilled with the chunk RB ahead
+                if (it == 0 && lane == 0)
+                    for (int g = 0; g < RB; ++g) issue_res_load(g);
                 if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
                 tc_fence_after();
                 bool ok = true;
 #pragma unroll 1
-                for (int rd = 0; rd < ROUNDS && ok; ++rd) {
-                    if (rd > 0) issue_round(rd);
-                    if (!mbar_wait(rbar, res_phase & 1, abort_flag)) {
+                for (int c = 0; c < NC; ++c) {
+                    const int g = it * NC + c;
+                    const int b = g % RB;
+                    if (!mbar_wait(res_bar(b), (g / RB) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    ++res_phase;
-#pragma unroll 1
-                    for (int c = 0; c < RB; ++c) {
-                        float v[32];
-                        tmem_ld32(taddr + (rd * RB + c) * 32, v);
-                        uint8_t* rp = slice + c * 4096 + lane * 128;
+                    res_done = g + 1;
+                    float v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    uint8_t* rp = rslice + b * 4096 + lane * 128;
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            float4* q = reinterpret_cast<float4*>(rp + ((k ^ (lane & 7)) << 4));
-                            float4 o = *q;
-                            o.x += v[4 * k + 0];
-                            o.y += v[4 * k + 1];
-                            o.z += v[4 * k + 2];
-                            o.w += v[4 * k + 3];
-                            *q = o;
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmC, smem_u32(slice + c * 4096), n_t * BN + (rd * RB + c) * 32, y_box);
-                            bulk_commit();
+                    for (int k = 0; k < 8; ++k) {
+                        float4* q = reinterpret_cast<float4*>(rp + ((k ^ (lane & 7)) << 4));
+                        float4 o = *q;
+                        o.x += v[4 * k + 0];
+                        o.y += v[4 * k + 1];
+                        o.z += v[4 * k + 2];
+                        o.w += v[4 * k + 3];
+                        *q = o;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, smem_u32(rslice + b * 4096), n_t * BN + c * 32, y_box);
+                        bulk_commit();
+                        if (g >= 1) {
+                            bulk_wait_read<1>();           // the store of chunk g - 1 has read its box
+                            issue_res_load(g - 1 + RB);
                         }
                     }
                 }
@@ -342,7 +345,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             mbar_arrive(bar(TEMPTY + acc));
         }
-        if (EPI == GEMM_EPI_ADD_F32 && res_armed) mbar_wait_drain(bar(RES + (warp - 2)), res_parity);
+        if (EPI == GEMM_EPI_ADD_F32 && lane == 0)   // residual loads still in flight land before exit
+            for (int b = 0; b < RB; ++b)
+                if (last_issued[b] >= res_done) mbar_wait_drain(res_bar(b), (last_issued[b] / RB) & 1);
         if (lane == 0) bulk_wait_all();   // stores complete before the CTA exits
     }
 
