@@ -73,6 +73,15 @@ int tee_op_ffn_in(tee_ctx* ctx, int layer, const void* d_y, void* d_z, int T, vo
 /* x float[T*H] += z ACT[T*I] Wo_ffn^T */
 int tee_op_ffn_out(tee_ctx* ctx, int layer, const void* d_z, float* d_x, int T, void* stream);
 
+/* Generic bf16 projection on the tensor cores: C = A W^T with A bf16[M*K],
+ * W bf16[N*K] (both K-contiguous), fp32 accumulation; epilogue 0 stores C as
+ * bf16[M*N], epilogue 1 adds it into float C[M*N].  N a multiple of 128, K a
+ * multiple of 64, pointers 16-byte aligned.  TEE_BF16 contexts only (the
+ * context supplies the device and the status word).  It is the kernel the
+ * pass uses for its four projections, exposed for shape tests and timing. */
+int tee_op_gemm_bf16(tee_ctx* ctx, const void* d_a, const void* d_w, void* d_c, int M, int N, int K, int epilogue,
+                     void* stream);
+
 /* out float[n*H] = L2-normalised per-text mean of x float[T*H]. */
 int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts,
                    float* d_out, void* stream);

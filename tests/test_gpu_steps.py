@@ -199,3 +199,29 @@ def test_weight_codes_and_block_sums_bit_exact(w8a8, which, name):
     enc.op("tee_op_w8a8_partials", layer, which, dev(qa), M, parts, 0)
     ref = oracle.int_block_partials(qa, q_ref)
     np.testing.assert_array_equal(parts.cpu().numpy().astype(np.int64), ref)
+
+
+# ---------------------------------------------------------------------------
+# the projection GEMM on arbitrary shapes (tile tails, both epilogues, every
+# tile width and the 2-CTA weight multicast)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (259, 384, 192), (1000, 256, 768), (513, 768, 3072),
+                                   (700, 2304, 768)])
+@pytest.mark.parametrize("epi", [0, 1])
+def test_gemm_bf16_shapes(lib, M, N, K, epi):
+    enc = binding.Encoder(synth.TINY, "bf16", max_tokens=16, max_texts=4)
+    rng = np.random.default_rng(M + N + K)
+    a = dev(rng.standard_normal((M, K)).astype(np.float32), torch.bfloat16)
+    w = dev((rng.standard_normal((N, K)) * 0.05).astype(np.float32), torch.bfloat16)
+    ref = to_np(a) @ to_np(w).T
+    if epi == 0:
+        c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 0, 0)
+        assert_step_close(to_np(c), ref, "bf16")
+    else:
+        c0 = rng.standard_normal((M, N)).astype(np.float32)
+        c = dev(c0)
+        enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 1, 0)
+        np.testing.assert_allclose(to_np(c), c0.astype(np.float64) + ref, atol=2e-3 * max(1.0, np.abs(ref).max()))
+    enc.close()

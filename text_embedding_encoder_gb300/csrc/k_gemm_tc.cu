@@ -16,7 +16,9 @@
 //   * two TMEM accumulators (2 x BN fp32 columns) so the epilogue of one tile
 //     overlaps the MMAs of the next.
 //   * tiles are ordered with the N index fastest, so CTAs running at the same
-//     time share their A rows in L2.
+//     time share their A rows in L2; CTAs run in clusters of two on vertically
+//     adjacent tiles, each loading half of the shared weight tile and
+//     multicasting it to both (one third less operand traffic per CTA).
 //   * epilogues fused into the store: bf16 store, fp32 residual add, RoPE on
 //     the q/k columns (positions restart per text), GeGLU gate.  Outputs go
 //     out through per-warp swizzled shared-memory boxes and TMA bulk tensor
@@ -78,7 +80,11 @@ struct Smem {
     static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;   // a power of two >= 2 * BN
 };
 
-template <int BN, int EPI>
+// MC: CTAs run in clusters of two that take vertically adjacent tiles (rows
+// m and m + 1 of the same column tile n); each loads half of the shared weight
+// tile and multicasts it to both, and a shared-memory stage is released only
+// when both CTAs' MMAs are done with it.
+template <int BN, int EPI, bool MC>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, Params p) {
@@ -96,12 +102,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_m = (p.M + BM - 1) / BM, num_n = p.N / BN, num_k = p.K / BK;
-    const int num_tiles = num_m * num_n;
+    // work units: one tile, or (with MC) a pair of vertically adjacent tiles per cluster
+    const uint32_t crank = MC ? cluster_ctarank() : 0;
+    const int num_units = (MC ? (num_m + 1) / 2 : num_m) * num_n;
+    const int unit0 = MC ? blockIdx.x / 2 : blockIdx.x;
+    const int ustride = MC ? gridDim.x / 2 : gridDim.x;
+    auto unit_m = [&](int u) { return MC ? 2 * (u / num_n) + (int)crank : u / num_n; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::STAGES; ++s) {
             mbar_init(bar(FULL + s), 1);
-            mbar_init(bar(EMPTY + s), 1);
+            mbar_init(bar(EMPTY + s), MC ? 2 : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar(TFULL + a), 1);
@@ -123,6 +134,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (MC) cluster_sync();   // the peer's multicasts may target these barriers only after init
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -134,8 +146,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool armed[S::STAGES];
             for (int s = 0; s < S::STAGES; ++s) armed[s] = false, armed_parity[s] = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                const int n_t = tile % num_n, m_t = tile / num_n;
+            for (int u = unit0; u < num_units && ok; u += ustride) {
+                const int n_t = u % num_n, m_t = unit_m(u);
                 for (int kb = 0; kb < num_k; ++kb, ++g) {
                     const int s = g % S::STAGES;
                     const uint32_t r = g / S::STAGES;
@@ -147,7 +159,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t sb = sa + A_BYTES;
                     mbar_expect_tx(bar(FULL + s), S::STAGE_BYTES);
                     tma_load_2d(sa, &tmA, kb * BK, m_t * BM, bar(FULL + s));
-                    tma_load_2d(sb, &tmB, kb * BK, n_t * BN, bar(FULL + s));
+                    if constexpr (MC)   // this CTA's half of the weight tile, into both CTAs
+                        tma_load_2d_mc(sb + crank * (BN / 2) * 128, &tmB, kb * BK, n_t * BN + crank * (BN / 2),
+                                       bar(FULL + s), 0x3);
+                    else
+                        tma_load_2d(sb, &tmB, kb * BK, n_t * BN, bar(FULL + s));
                     armed[s] = true;
                     armed_parity[s] = r & 1;
                 }
@@ -164,7 +180,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t g = 0;
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+            for (int u = unit0; u < num_units && ok; u += ustride, ++it) {
                 const int acc = it & 1, use = it >> 1;
                 if (!mbar_wait(bar(TEMPTY + acc), (use & 1) ^ 1, abort_flag)) {
                     ok = false;
@@ -186,7 +202,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
-                    mma_commit(bar(EMPTY + s));
+                    if constexpr (MC) mma_commit_mc(bar(EMPTY + s), 0x3);   // both CTAs' stage s
+                    else mma_commit(bar(EMPTY + s));
                 }
                 if (!ok) break;
                 mma_commit(bar(TFULL + acc));
@@ -213,11 +230,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         auto res_bar = [&](int b) { return bar(RES + (warp - 2) * 4 + b); };
         auto issue_res_load = [&](int g) {                         // lane 0; box g % RB is free
             const int k = g / NC, c = g % NC;
-            const int tile = blockIdx.x + k * gridDim.x;
-            if (tile >= num_tiles) return;
+            const int u = unit0 + k * ustride;
+            if (u >= num_units) return;
             const int b = g % RB;
             mbar_expect_tx(res_bar(b), 4096);
-            tma_load_2d(smem_u32(rslice + b * 4096), &tmC, (tile % num_n) * BN + c * 32, (tile / num_n) * BM + quad * 32,
+            tma_load_2d(smem_u32(rslice + b * 4096), &tmC, (u % num_n) * BN + c * 32, unit_m(u) * BM + quad * 32,
                         res_bar(b));
             last_issued[b] = g;
         };
@@ -236,9 +253,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ++n_stores;
         };
         int it = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+        for (int u = unit0; u < num_units; u += ustride, ++it) {
             const int acc = it & 1, use = it >> 1;
-            const int n_t = tile % num_n, m_t = tile / num_n;
+            const int n_t = u % num_n, m_t = unit_m(u);
             const int gr = m_t * BM + row_local;
             const bool valid = gr < p.M;
             const int y_box = m_t * BM + quad * 32;
@@ -359,6 +376,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      : "memory");
     }
     if (threadIdx.x == 0 && *abort_flag && p.status) atomicOr(p.status, TEE_STATUS_TIMEOUT);
+    // the peer's last multicast commits target this CTA's barriers: leave together
+    if constexpr (MC) cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -408,18 +427,41 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, int K, int box_rows) 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI>
-cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const Params& p, int grid,
+template <int BN, int EPI, bool MC>
+cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const Params& p, int units,
                      cudaStream_t s) {
-    static bool attr_set = false;
+    static int max_grid = 0;   // CTAs that can be resident at once (a multiple of 2 with MC)
     constexpr uint32_t smem = Smem<BN, EPI>::TOTAL;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+    auto kernel = gemm_tc_kernel<BN, EPI, MC>;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = MC ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!max_grid) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        if (MC) {
+            int clusters = 0;
+            cfg.gridDim = dim3(2 * g_num_sms);
+            e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+            if (e != cudaSuccess) return e;
+            max_grid = 2 * (clusters > 0 ? clusters : 1);
+        } else {
+            max_grid = g_num_sms;
+        }
     }
-    gemm_tc_kernel<BN, EPI><<<grid, NUM_THREADS, smem, s>>>(ma, mb, mc, p);
+    const int per_unit = MC ? 2 : 1;
+    const int grid = units * per_unit < max_grid ? units * per_unit : max_grid;
+    cfg.gridDim = dim3(grid);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ma, mb, mc, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -441,28 +483,36 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     const bool add_wide = a.epi == GEMM_EPI_ADD_F32 && a.K > 1024 && a.N % 192 == 0;
     const int BN = add_wide ? 192
                  : (a.epi == GEMM_EPI_ADD_F32 ? 128 : ((a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128));
-    CUtensorMap ma, mb, mc;
-    if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, BN)) return cudaErrorInvalidValue;
+    const int num_m = (a.M + BM - 1) / BM;
+    // pairs of CTAs share the weight tile (256-column tiles, at least two row
+    // tiles); the residual projections measured no gain from it
+    const bool mc = num_m >= 2 && BN == 256;
+    CUtensorMap ma, mb, mc_map;
+    if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, mc ? BN / 2 : BN))
+        return cudaErrorInvalidValue;
     if (a.epi == GEMM_EPI_ADD_F32) {
-        if (!make_out_map(&mc, a.C, a.M, a.N, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32)) return cudaErrorInvalidValue;
-    } else if (!make_out_map(&mc, a.C, a.M, a.epi == GEMM_EPI_GEGLU ? a.N / 2 : a.N, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                             64)) {
+        if (!make_out_map(&mc_map, a.C, a.M, a.N, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32)) return cudaErrorInvalidValue;
+    } else if (!make_out_map(&mc_map, a.C, a.M, a.epi == GEMM_EPI_GEGLU ? a.N / 2 : a.N,
+                             CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64)) {
         return cudaErrorInvalidValue;
     }
     Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status};
-    const int tiles = ((a.M + BM - 1) / BM) * (a.N / BN);
-    const int grid = tiles < g_num_sms ? tiles : g_num_sms;
-    if (add_wide) return launch_t<192, GEMM_EPI_ADD_F32>(ma, mb, mc, p, grid, s);
+    const int units = (mc ? (num_m + 1) / 2 : num_m) * (a.N / BN);
+#define TEE_GEMM_DISPATCH(BN_, EPI_)                                                                  \
+    return mc ? launch_t<BN_, EPI_, true>(ma, mb, mc_map, p, units, s)                               \
+              : launch_t<BN_, EPI_, false>(ma, mb, mc_map, p, units, s)
+    if (add_wide) TEE_GEMM_DISPATCH(192, GEMM_EPI_ADD_F32);
     if (BN == 256) {
         switch (a.epi) {
-            case GEMM_EPI_STORE_BF16: return launch_t<256, GEMM_EPI_STORE_BF16>(ma, mb, mc, p, grid, s);
-            case GEMM_EPI_ROPE_BF16: return launch_t<256, GEMM_EPI_ROPE_BF16>(ma, mb, mc, p, grid, s);
-            default: return launch_t<256, GEMM_EPI_GEGLU>(ma, mb, mc, p, grid, s);
+            case GEMM_EPI_STORE_BF16: TEE_GEMM_DISPATCH(256, GEMM_EPI_STORE_BF16);
+            case GEMM_EPI_ROPE_BF16: TEE_GEMM_DISPATCH(256, GEMM_EPI_ROPE_BF16);
+            default: TEE_GEMM_DISPATCH(256, GEMM_EPI_GEGLU);
         }
     }
     switch (a.epi) {
-        case GEMM_EPI_STORE_BF16: return launch_t<128, GEMM_EPI_STORE_BF16>(ma, mb, mc, p, grid, s);
-        case GEMM_EPI_ADD_F32: return launch_t<128, GEMM_EPI_ADD_F32>(ma, mb, mc, p, grid, s);
-        default: return launch_t<128, GEMM_EPI_ROPE_BF16>(ma, mb, mc, p, grid, s);
+        case GEMM_EPI_STORE_BF16: TEE_GEMM_DISPATCH(128, GEMM_EPI_STORE_BF16);
+        case GEMM_EPI_ADD_F32: TEE_GEMM_DISPATCH(128, GEMM_EPI_ADD_F32);
+        default: TEE_GEMM_DISPATCH(128, GEMM_EPI_ROPE_BF16);
     }
+#undef TEE_GEMM_DISPATCH
 }

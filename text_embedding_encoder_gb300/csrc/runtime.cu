@@ -678,6 +678,27 @@ int tee_op_ffn_out(tee_ctx* ctx, int layer, const void* d_z, float* d_x, int T, 
     return step_linear(ctx, layer, TEE_W_FFN_OUT, d_z, d_x, T, 1, GEMM_EPI_ADD_F32, nullptr, (cudaStream_t)stream);
 }
 
+int tee_op_gemm_bf16(tee_ctx* ctx, const void* d_a, const void* d_w, void* d_c, int M, int N, int K, int epilogue,
+                     void* stream) {
+    if (!ctx) return TEE_EINVAL;
+    if (ctx->cfg.dtype != TEE_BF16) return fail(ctx, TEE_EINVAL, "tee_op_gemm_bf16 needs a TEE_BF16 context");
+    if (!d_a || !d_w || !d_c) return fail(ctx, TEE_EINVAL, "NULL pointer");
+    if (M < 0 || N <= 0 || K <= 0 || N % 128 || K % 64) return fail(ctx, TEE_EINVAL, "bad GEMM shape");
+    if (epilogue != 0 && epilogue != 1) return fail(ctx, TEE_EINVAL, "epilogue must be 0 (store) or 1 (add)");
+    GemmTcArgs a{};
+    a.A = d_a;
+    a.W = d_w;
+    a.C = d_c;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.epi = epilogue == 0 ? GEMM_EPI_STORE_BF16 : GEMM_EPI_ADD_F32;
+    a.status = ctx->d_status;
+    cudaStream_t s = (cudaStream_t)stream;
+    LAUNCH(TEE_K_GEMM, 2.0 * M * N * K, 0, launch_gemm_tc(a, s));
+    return TEE_OK;
+}
+
 int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts,
                    float* d_out, void* stream) {
     if (!ctx) return TEE_EINVAL;

@@ -27,6 +27,8 @@ def main():
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--only", choices=STEPS, default=None)
     ap.add_argument("--long-docs", action="store_true", help="8 texts of tokens/8 each instead of a sweep batch")
+    ap.add_argument("--cublas", action="store_true",
+                    help="also time torch.matmul (cuBLAS) on the four projection shapes, for comparison only")
     args = ap.parse_args()
 
     shape = synth.RURI_310M
@@ -88,6 +90,41 @@ def main():
         if nbytes:
             row["gbs"] = round(nbytes / ms / 1e6, 1)
         report[name] = row
+    if args.cublas:
+        # this library's GEMM with a plain bf16 store (no fused epilogue) on the same shapes
+        for name, (n_out, k_in) in {"qkv": (3 * H, H), "out_proj": (H, H), "ffn_in": (2 * I, H),
+                                    "ffn_out": (H, I)}.items():
+            a = torch.randn(T, k_in, device="cuda", dtype=torch.bfloat16)
+            wt = torch.randn(n_out, k_in, device="cuda", dtype=torch.bfloat16)
+            c = torch.empty(T, n_out, device="cuda", dtype=torch.bfloat16)
+            fn = lambda: enc.op("tee_op_gemm_bf16", a, wt, c, T, n_out, k_in, 0, 0)  # noqa: E731
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.reps
+            report["plain_" + name] = {"ms": round(ms, 4), "tflops": round(2.0 * T * n_out * k_in / ms / 1e9, 1)}
+        # library reference point: plain bf16 GEMMs of the same shapes (no epilogue fusion)
+        for name, (n_out, k_in) in {"qkv": (3 * H, H), "out_proj": (H, H), "ffn_in": (2 * I, H),
+                                    "ffn_out": (H, I)}.items():
+            a = torch.randn(T, k_in, device="cuda", dtype=torch.bfloat16)
+            wt = torch.randn(n_out, k_in, device="cuda", dtype=torch.bfloat16)
+            for _ in range(3):
+                torch.matmul(a, wt.t())
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.reps):
+                torch.matmul(a, wt.t())
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.reps
+            report["cublas_" + name] = {"ms": round(ms, 4), "tflops": round(2.0 * T * n_out * k_in / ms / 1e9, 1)}
     print(json.dumps(report))
     enc.close()
 
