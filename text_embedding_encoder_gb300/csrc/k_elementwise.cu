@@ -3,8 +3,8 @@
 //
 // Method: tensai page "テキスト埋め込み", §何が動くか (エンコーダ, プーリング,
 // packing paragraph).  All of these are bandwidth-bound: rows are read with
-// 16-byte vector loads, one warp per row (LayerNorm) or one block per token
-// (gather); the pool reduces 64-row chunks of each text in parallel, then
+// 16-byte vector loads, one warp per row (LayerNorm) or per token (gather);
+// the pool reduces 64-row chunks of each text in parallel, then
 // combines each text's chunks in order; reductions by warp shuffles.
 #include "tee_internal.cuh"
 
@@ -34,29 +34,38 @@ __global__ void convert_f32_bf16_kernel(const float* __restrict__ src, bf16* __r
     for (; i < n; i += stride) dst[i] = __float2bfloat16_rn(src[i]);
 }
 
-// x[t, :] = E[id[t], :]; one block of H/4 threads per token, 16-byte loads.
+// x[t, :] = E[id[t], :]; one warp per token (8 tokens per 256-thread block),
+// 16-byte loads of the table row and 16-byte stores of the fp32 row.
 template <typename TE>
 __global__ void embed_kernel(const TE* __restrict__ emb, const int32_t* __restrict__ ids, int T, int H, int V,
                              float* __restrict__ x, unsigned int* status) {
-    int t = blockIdx.x;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
     if (t >= T) return;
-    int id = ids[t];
-    bool ok = (id >= 0 && id < V);
-    if (!ok && threadIdx.x == 0 && status) atomicOr(status, TEE_STATUS_BAD_ID);
+    const int id = ids[t];
+    const bool ok = (id >= 0 && id < V);
+    if (!ok && lane == 0 && status) atomicOr(status, TEE_STATUS_BAD_ID);
     float4* dst = reinterpret_cast<float4*>(x + (size_t)t * H);
-    for (int c4 = threadIdx.x; c4 < H / 4; c4 += blockDim.x) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ok) {
-            if constexpr (sizeof(TE) == 4) {
-                v = reinterpret_cast<const float4*>(emb + (size_t)id * H)[c4];
-            } else {
-                const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(emb + (size_t)id * H) + 2 * c4;
-                float2 a = __bfloat1622float2(p[0]);
-                float2 b = __bfloat1622float2(p[1]);
-                v = make_float4(a.x, a.y, b.x, b.y);
+    if constexpr (sizeof(TE) == 4) {
+        const float4* src = reinterpret_cast<const float4*>(emb + (size_t)(ok ? id : 0) * H);
+        for (int c4 = lane; c4 < H / 4; c4 += 32) dst[c4] = ok ? src[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        // 8 bf16 (16 bytes) per load -> two float4 stores
+        const uint4* src = reinterpret_cast<const uint4*>(emb + (size_t)(ok ? id : 0) * H);
+        for (int c8 = lane; c8 < H / 8; c8 += 32) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (ok) {
+                const uint4 q = src[c8];
+                const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.x));
+                const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.y));
+                const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.z));
+                const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.w));
+                a = make_float4(f0.x, f0.y, f1.x, f1.y);
+                b = make_float4(f2.x, f2.y, f3.x, f3.y);
             }
+            dst[2 * c8] = a;
+            dst[2 * c8 + 1] = b;
         }
-        dst[c4] = v;
     }
 }
 
@@ -175,15 +184,37 @@ __global__ void pool_partial_kernel(const float* __restrict__ x, const int32_t* 
     const int r0 = cu[j] + (chunk - chunk_off[j]) * POOL_CHUNK;
     const int r1 = min(cu[j + 1], r0 + POOL_CHUNK);
     for (int c4 = threadIdx.x; c4 < H / 4; c4 += blockDim.x) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int r = r0; r < r1; ++r) {
-            const float4 v = reinterpret_cast<const float4*>(x + (size_t)r * H)[c4];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+        // eight independent accumulators keep eight row loads in flight
+        float4 acc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        int r = r0;
+        for (; r + 8 <= r1; r += 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float4 v = reinterpret_cast<const float4*>(x + (size_t)(r + u) * H)[c4];
+                acc[u].x += v.x;
+                acc[u].y += v.y;
+                acc[u].z += v.z;
+                acc[u].w += v.w;
+            }
         }
-        reinterpret_cast<float4*>(partial + (size_t)chunk * H)[c4] = acc;
+        for (int u = 0; r < r1; ++r, ++u) {
+            const float4 v = reinterpret_cast<const float4*>(x + (size_t)r * H)[c4];
+            acc[u].x += v.x;
+            acc[u].y += v.y;
+            acc[u].z += v.z;
+            acc[u].w += v.w;
+        }
+        float4 tot = acc[0];
+#pragma unroll
+        for (int u = 1; u < 8; ++u) {
+            tot.x += acc[u].x;
+            tot.y += acc[u].y;
+            tot.z += acc[u].z;
+            tot.w += acc[u].w;
+        }
+        reinterpret_cast<float4*>(partial + (size_t)chunk * H)[c4] = tot;
     }
 }
 
@@ -280,11 +311,11 @@ cudaError_t launch_convert_f32_bf16(const float* src, bf16* dst, size_t n, cudaS
 cudaError_t launch_embed(const void* emb, bool emb_bf16, const int32_t* ids, int T, int H, int V, float* x,
                          unsigned int* status, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    int threads = H / 4 < 256 ? H / 4 : 256;
+    const unsigned blocks = (unsigned)((T + 7) / 8);   // one warp per token
     if (emb_bf16)
-        embed_kernel<bf16><<<T, threads, 0, s>>>((const bf16*)emb, ids, T, H, V, x, status);
+        embed_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)emb, ids, T, H, V, x, status);
     else
-        embed_kernel<float><<<T, threads, 0, s>>>((const float*)emb, ids, T, H, V, x, status);
+        embed_kernel<float><<<blocks, 256, 0, s>>>((const float*)emb, ids, T, H, V, x, status);
     return cudaGetLastError();
 }
 

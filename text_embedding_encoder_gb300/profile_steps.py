@@ -18,14 +18,15 @@ import torch
 
 from . import binding, synth
 
-STEPS = ["layernorm", "qkv", "attn_global", "attn_window", "out_proj", "ffn_in", "ffn_out", "pool"]
+STEPS = ["embed", "layernorm", "qkv", "attn_global", "attn_window", "out_proj", "ffn_in", "ffn_out", "pool"]
+PLAIN = ["plain_qkv", "plain_out_proj", "plain_ffn_in", "plain_ffn_out"]
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--tokens", type=int, default=32768)
     ap.add_argument("--reps", type=int, default=10)
-    ap.add_argument("--only", choices=STEPS, default=None)
+    ap.add_argument("--only", choices=STEPS + PLAIN, default=None)
     ap.add_argument("--long-docs", action="store_true", help="8 texts of tokens/8 each instead of a sweep batch")
     ap.add_argument("--cublas", action="store_true",
                     help="also time torch.matmul (cuBLAS) on the four projection shapes, for comparison only")
@@ -59,7 +60,9 @@ def main():
     pairs_g = float((lens ** 2).sum())
     pairs_w = float(sum(sum(min(L - 1, i + 64) - max(0, i - 64) + 1 for i in range(int(L))) for L in lens))
 
+    d_ids = dev(ids)
     steps = {
+        "embed": (lambda: enc.op("tee_op_embed", d_ids, T, x, 0), None, T * H * 6.0 + T * 4.0),
         "layernorm": (lambda: enc.op("tee_op_layernorm", 0, 0, x, y, T, 0), None, T * H * 6.0),
         "qkv": (lambda: enc.op("tee_op_qkv", 0, y, pos, qkv_out, T, 0), 2.0 * T * 3 * H * H, None),
         "attn_global": (lambda: enc.op("tee_op_attention", 0, qkv, d_cu, cu, n, o, 0), 3072.0 * pairs_g, None),
@@ -90,10 +93,12 @@ def main():
         if nbytes:
             row["gbs"] = round(nbytes / ms / 1e6, 1)
         report[name] = row
-    if args.cublas:
+    if args.cublas or (args.only or "").startswith("plain_"):
         # this library's GEMM with a plain bf16 store (no fused epilogue) on the same shapes
         for name, (n_out, k_in) in {"qkv": (3 * H, H), "out_proj": (H, H), "ffn_in": (2 * I, H),
                                     "ffn_out": (H, I)}.items():
+            if args.only and args.only != "plain_" + name:
+                continue
             a = torch.randn(T, k_in, device="cuda", dtype=torch.bfloat16)
             wt = torch.randn(n_out, k_in, device="cuda", dtype=torch.bfloat16)
             c = torch.empty(T, n_out, device="cuda", dtype=torch.bfloat16)
@@ -109,6 +114,7 @@ def main():
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / args.reps
             report["plain_" + name] = {"ms": round(ms, 4), "tflops": round(2.0 * T * n_out * k_in / ms / 1e9, 1)}
+    if args.cublas:
         # library reference point: plain bf16 GEMMs of the same shapes (no epilogue fusion)
         for name, (n_out, k_in) in {"qkv": (3 * H, H), "out_proj": (H, H), "ffn_in": (2 * I, H),
                                     "ffn_out": (H, I)}.items():
