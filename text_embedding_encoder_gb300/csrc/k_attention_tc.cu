@@ -61,7 +61,7 @@ constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = B_KVF + KV_STAGES, B_SF = B
 constexpr uint32_t OFF_RED = OFF_BAR + N_BARS * 8 + 16;       // row-maximum exchange: [2 tiles][2 halves][128 rows]
 constexpr uint32_t OFF_REDL = OFF_RED + 2 * 2 * 128 * 4;       // row-sum exchange: [2 halves][128 rows]
 constexpr uint32_t SMEM_TOTAL = OFF_REDL + 2 * 128 * 4 + 1024;
-constexpr uint32_t TMEM_COLS = 512;                 // S: 2 x 128 columns, O: 2 x 64 columns
+constexpr uint32_t TMEM_COLS = 512;                 // S: 2 x 128 columns (by tile), O: 2 x 64 (by unit)
 constexpr uint32_t TM_S = 0, TM_O = 256;
 
 struct AttnParams {
@@ -165,15 +165,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_s = make_idesc(BQ, BKV);
             constexpr uint32_t idesc_pv = make_idesc(BQ, HD) | IDESC_B_MN_MAJOR;
-            uint32_t t = 0;          // tiles whose S has been issued (global)
-            bool ok = true;
-            bool pend = false;       // a tile whose P V is still to be issued
-            uint32_t pend_t = 0;
-            // P_t V_t for the pending tile t
-            auto issue_pv = [&](uint32_t tt) -> bool {
+            // P_tt V_tt accumulated into the unit's TMEM O buffer; the first
+            // tile of a unit overwrites it once the softmax warps have read the
+            // unit two back out of that buffer
+            auto issue_pv = [&](uint32_t tt, bool first, int ub, uint32_t uuse) -> bool {
                 const int pb = tt & 1, st = tt % KV_STAGES;
                 if (!mbar_wait(bar(B_PF + pb), (tt >> 1) & 1, abort_flag)) return false;
-                if (!mbar_wait(bar(B_OE + pb), ((tt >> 1) & 1) ^ 1, abort_flag)) return false;
+                if (first && !mbar_wait(bar(B_OE + ub), (uuse & 1) ^ 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t pbase = sbase + OFF_P + pb * P_BYTES;
                 const uint32_t vbase = sbase + OFF_V + st * TILE_BYTES;
@@ -181,12 +179,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int s = 0; s < BKV / 16; ++s) {
                     const uint64_t adesc = sw128_desc(pbase + (s >> 2) * (P_BYTES / 2)) + 2 * (s & 3);
                     const uint64_t vdesc = sw128_desc_mn(vbase + s * 2048);
-                    mma_bf16(tmem_base + TM_O + pb * HD, adesc, vdesc, idesc_pv, s != 0);
+                    mma_bf16(tmem_base + TM_O + ub * HD, adesc, vdesc, idesc_pv, !(first && s == 0));
                 }
                 mma_commit(bar(B_OF + pb));
                 mma_commit(bar(B_KVE + st));
                 return true;
             };
+            uint32_t t = 0;          // tiles whose S has been issued (global)
+            bool ok = true;
+            bool pend = false;       // a tile whose P V is still to be issued
+            uint32_t pend_t = 0, pend_use = 0;
+            bool pend_first = false;
+            int pend_ub = 0;
             int ui = 0;
             for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
                 const int nk = n_kv_tiles(p.items[u / p.n_heads]);
@@ -207,85 +211,86 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mma_bf16(tmem_base + TM_S + sb * BKV, qdesc + 2 * k, kdesc + 2 * k, idesc_s, k != 0);
                     mma_commit(bar(B_SF + sb));
                     if (kt == nk - 1) mma_commit(bar(B_QE + qb));   // Q buffer free once these S MMAs finish
-                    if (pend && !issue_pv(pend_t)) {
+                    if (pend && !issue_pv(pend_t, pend_first, pend_ub, pend_use)) {
                         ok = false;
                         break;
                     }
                     pend = true;
                     pend_t = t;
+                    pend_first = kt == 0;
+                    pend_ub = ui & 1;
+                    pend_use = (uint32_t)ui >> 1;
                 }
             }
-            if (ok && pend) issue_pv(pend_t);
+            if (ok && pend) issue_pv(pend_t, pend_first, pend_ub, pend_use);
             mma_commit(bar(B_DONE));
             mbar_wait_drain(bar(B_DONE), 0);
         }
         __syncwarp();
     } else {
         // ---------------- softmax / output (warps 2..9) ----------------
+        // Warps w and w + 4 share a TMEM lane quadrant (rows 32*quad ..) and
+        // split each tile's 128 key columns; the tile's row maximum is exchanged
+        // through shared memory.  P V accumulates in TMEM across the unit's key
+        // tiles against a reference maximum m_ref that moves only when a tile's
+        // maximum exceeds it by more than RESCALE_LOG2 (then the row of O is
+        // rescaled in TMEM), so most tiles touch no O at all.
+        constexpr float RESCALE_LOG2 = 8.0f;
         const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;               // key columns [64*half, 64*half + 64)
+        const int half = (warp - 2) >> 2;               // key columns [64*half, +64), O columns [32*half, +32)
         const int r = quad * 32 + lane;                 // query row of the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint8_t* prow0 = smem + OFF_P + half * (P_BYTES / 2) + r * 128;
         float* red = reinterpret_cast<float*>(smem + OFF_RED);   // [2][2][128]
+        float* red_l = reinterpret_cast<float*>(smem + OFF_REDL);   // [2][128]
         const uint32_t pair_bar = 1 + quad;             // named barrier of warps (w, w + 4)
         const float sl2 = p.scale_log2;
         uint32_t t = 0;
         bool ok = true;
-        float O[HD / 2];
 
         auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
-        // O_dst = O_dst * corr + (P_tt V_tt)[this thread's 32 dimensions]
-        auto o_phase = [&](uint32_t tt, float corr, float (&O_dst)[HD / 2]) -> bool {
-            const int ob = tt & 1;
-            if (!mbar_wait(bar(B_OF + ob), (tt >> 1) & 1, abort_flag)) return false;
-            tc_fence_after();
-            float pv[32];
-            tmem_ld32(tmem_base + lane_off + TM_O + ob * HD + half * 32, pv);
-            tc_fence_before();
-            mbar_arrive(bar(B_OE + ob));
-#pragma unroll
-            for (int d = 0; d < HD / 2; ++d) O_dst[d] = fmaf(O_dst[d], corr, pv[d]);
-            return true;
-        };
 
-        // A finished unit waits for the P V of its last tile; that wait is
-        // deferred past the next unit's first softmax so it overlaps it.
-        float* red_l = reinterpret_cast<float*>(smem + OFF_REDL);   // [2][128]
+        // The previous unit's output, deferred past the next unit's first
+        // softmax: wait for its last P V, read this warp's 32 columns of O,
+        // release the buffer, combine the row sum with the partner, store.
         bool pend = false;
-        float O_p[HD / 2];
-        float l_p = 0.f, corr_p = 1.f;
+        float l_p = 0.f;
         uint32_t t_p = 0;
+        int ub_p = 0;
         bf16* dst_p = nullptr;
         auto finalize = [&]() -> bool {
-            if (!o_phase(t_p, corr_p, O_p)) return false;
-            red_l[half * 128 + r] = l_p;                  // the row sum is split between the two halves
+            if (!mbar_wait(bar(B_OF + (t_p & 1)), (t_p >> 1) & 1, abort_flag)) return false;
+            tc_fence_after();
+            float o[32];
+            tmem_ld32(tmem_base + lane_off + TM_O + ub_p * HD + half * 32, o);
+            tc_fence_before();
+            mbar_arrive(bar(B_OE + ub_p));
+            red_l[half * 128 + r] = l_p;
             pair_sync();
             const float l_tot = l_p + red_l[(half ^ 1) * 128 + r];
             pair_sync();
             if (dst_p) {
                 const float inv = 1.0f / l_tot;
-                float out[32];
 #pragma unroll
-                for (int d = 0; d < 32; ++d) out[d] = O_p[d] * inv;
-                store_bf16x32(dst_p, out);
+                for (int d = 0; d < 32; ++d) o[d] *= inv;
+                store_bf16x32(dst_p, o);
             }
             pend = false;
             return true;
         };
 
-        for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        int ui = 0;
+        for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
             const int4 it = p.items[u / p.n_heads];
             const int head = u % p.n_heads;
             const int q_start = it.x, q_len = it.y, k_lo = it.z, k_hi = it.w;
             const int nk = n_kv_tiles(it);
             const int qg = q_start + r;
+            const int ub = ui & 1;
             // keys visible to this row: [vis_lo, vis_hi)
             const int vis_lo = p.is_global ? k_lo : max(k_lo, qg - p.window);
             const int vis_hi = p.is_global ? k_hi : min(k_hi, qg + p.window + 1);
-            float m = -INFINITY, l = 0.f, corr_pending = 1.f;
-#pragma unroll
-            for (int d = 0; d < HD / 2; ++d) O[d] = 0.f;
+            float m_ref = -INFINITY, l = 0.f;
             for (int kt = 0; kt < nk; ++kt, ++t) {
                 const int sb = t & 1;
                 if (!mbar_wait(bar(B_SF + sb), (t >> 1) & 1, abort_flag)) {
@@ -310,10 +315,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 float* red_t = red + (t & 1) * 256;
                 red_t[half * 128 + r] = mx;
                 pair_sync();
-                mx = fmaxf(mx, red_t[(half ^ 1) * 128 + r]);
-                const float m_new = fmaxf(m, mx * sl2);
-                const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                const float corr = ex2_approx(m - m_use);
+                mx = fmaxf(mx, red_t[(half ^ 1) * 128 + r]) * sl2;
+                if (kt == 0) {
+                    m_ref = mx;
+                } else {
+                    // both warps of the pair see the same row maxima, so they
+                    // agree on which rows (and so whether the warp) rescale
+                    const bool need = mx > m_ref + RESCALE_LOG2;
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float corr = need ? ex2_approx(m_ref - mx) : 1.0f;
+                        // P V of the previous tile must be in O before it is rescaled
+                        if (!mbar_wait(bar(B_OF + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        float o[32];
+                        const uint32_t oaddr = tmem_base + lane_off + TM_O + ub * HD + half * 32;
+                        tmem_ld32(oaddr, o);
+#pragma unroll
+                        for (int d = 0; d < 32; ++d) o[d] *= corr;
+                        tmem_st32(oaddr, o);
+                        tc_fence_before();
+                        if (need) {
+                            l *= corr;
+                            m_ref = mx;
+                        }
+                    }
+                }
+                if (kt == 0 && pend && !finalize()) {   // previous unit, overlapped with this first softmax
+                    ok = false;
+                    break;
+                }
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
                 float sum = 0.f;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
@@ -332,25 +366,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(bar(B_PF + sb));
-                l = l * corr + sum;
-                m = m_new;
-                if (kt >= 1) {
-                    if (!o_phase(t - 1, corr_pending, O)) {
-                        ok = false;
-                        break;
-                    }
-                } else if (pend && !finalize()) {
-                    ok = false;
-                    break;
-                }
-                corr_pending = corr;
+                l += sum;
             }
             if (!ok) break;
-#pragma unroll
-            for (int d = 0; d < HD / 2; ++d) O_p[d] = O[d];
             l_p = l;
-            corr_p = corr_pending;
             t_p = t - 1;
+            ub_p = ub;
             dst_p = r < q_len ? p.o + (size_t)qg * p.hidden + head * HD + half * 32 : nullptr;
             pend = true;
         }
