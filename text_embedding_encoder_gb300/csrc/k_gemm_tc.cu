@@ -6,19 +6,23 @@
 // token activations and W [N, K] the weights, both bf16 and K-contiguous.
 //
 // Design (one CTA per SM, persistent over output tiles):
-//   * tile 128 x BN, K step 64 (one 128-byte swizzle atom); 4-stage
-//     shared-memory ring filled by TMA (cp.async.bulk.tensor, 128B swizzle,
-//     out-of-range rows zero-filled).  BN = 256 for the bf16-output
-//     projections, 128 (short K) or 192 (long K) for the residual ones.
+//   * tile 128 x BN per CTA, K step 64 (one 128-byte swizzle atom); a
+//     shared-memory ring of as many stages as fit, filled by TMA
+//     (cp.async.bulk.tensor, 128B swizzle, out-of-range rows zero-filled).
+//     BN = 256 for the bf16-output projections, 128 (short K) or 192 (long K)
+//     for the residual ones.
+//   * CTA pairs (clusters of two) compute 256 x BN tiles with tcgen05
+//     cta_group::2 MMAs (M=256) issued by the even CTA: each CTA stages its
+//     128 rows of A and half of the weight tile, and holds its 128 accumulator
+//     rows in its own tensor memory.  Row counts below two tiles, and the
+//     short-K residual projection, run one CTA per tile (M=128 MMAs).
 //   * warp 0 lane 0: TMA producer.  warp 1: TMEM allocator, lane 0 issues
-//     tcgen05.mma (M=128, N=BN, K=16) and commits to mbarriers.  warps 2-5:
+//     tcgen05.mma (N=BN, K=16) and commits to mbarriers.  warps 2-5:
 //     epilogue, each reading its 32-lane TMEM quadrant with tcgen05.ld.
 //   * two TMEM accumulators (2 x BN fp32 columns) so the epilogue of one tile
 //     overlaps the MMAs of the next.
 //   * tiles are ordered with the N index fastest, so CTAs running at the same
-//     time share their A rows in L2; CTAs run in clusters of two on vertically
-//     adjacent tiles, each loading half of the shared weight tile and
-//     multicasting it to both (one third less operand traffic per CTA).
+//     time share their A rows in L2.
 //   * epilogues fused into the store: bf16 store, fp32 residual add, RoPE on
 //     the q/k columns (positions restart per text), GeGLU gate.  Outputs go
 //     out through per-warp swizzled shared-memory boxes and TMA bulk tensor
@@ -68,27 +72,39 @@ constexpr uint32_t staging_bytes() {
     return EPI == GEMM_EPI_ADD_F32 ? 4u * res_round_boxes<BN>() * 4096u : 4u * 2u * 4096u;
 }
 
-template <int BN, int EPI>
+// How CTAs share the work of a tile.
+//   MODE_SINGLE: one CTA per 128 x BN tile.
+//   MODE_PAIR: clusters of two compute one 256 x BN tile with tcgen05
+//     cta_group::2 MMAs issued by the even CTA: each CTA holds its 128 rows of
+//     A and half of the weight tile (BN/2 rows) in shared memory and its 128
+//     rows of the accumulator in tensor memory.  A stage carries a third less
+//     data per CTA than a single CTA's (so the ring gets more stages), and the
+//     weight tile is read from L2 once per 256 rows.
+constexpr int MODE_SINGLE = 0, MODE_PAIR = 2;
+constexpr uint32_t SMEM_LIMIT = 227 * 1024;
+
+template <int BN, int EPI, int MODE>
 struct Smem {
-    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t B_BYTES = (MODE == MODE_PAIR ? BN / 2 : BN) * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = 4;
+    static constexpr uint32_t FIXED = staging_bytes<BN, EPI>() + (2 * 8 + 5 + 16) * 8 + 16 + 1024;
+    static constexpr int STAGES_FIT = (int)((SMEM_LIMIT - FIXED) / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;   // as many as fit, at most 8
     static constexpr uint32_t OUT_OFF = STAGES * STAGE_BYTES;
     static constexpr uint32_t BAR_OFF = OUT_OFF + staging_bytes<BN, EPI>();
     static constexpr uint32_t N_BARS = 2 * STAGES + 5 + 16;   // + one residual barrier per staging box (4 x 4)
     static constexpr uint32_t TOTAL = BAR_OFF + N_BARS * 8 + 16 + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;   // a power of two >= 2 * BN
+    static_assert(TOTAL <= SMEM_LIMIT, "shared memory");
 };
 
-// MC: CTAs run in clusters of two that take vertically adjacent tiles (rows
-// m and m + 1 of the same column tile n); each loads half of the shared weight
-// tile and multicasts it to both, and a shared-memory stage is released only
-// when both CTAs' MMAs are done with it.
-template <int BN, int EPI, bool MC>
+template <int BN, int EPI, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, Params p) {
-    using S = Smem<BN, EPI>;
+    using S = Smem<BN, EPI, MODE>;
+    constexpr bool PAIR = MODE == MODE_PAIR, CL = MODE != MODE_SINGLE;
+    constexpr int CG = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -102,21 +118,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_m = (p.M + BM - 1) / BM, num_n = p.N / BN, num_k = p.K / BK;
-    // work units: one tile, or (with MC) a pair of vertically adjacent tiles per cluster
-    const uint32_t crank = MC ? cluster_ctarank() : 0;
-    const int num_units = (MC ? (num_m + 1) / 2 : num_m) * num_n;
-    const int unit0 = MC ? blockIdx.x / 2 : blockIdx.x;
-    const int ustride = MC ? gridDim.x / 2 : gridDim.x;
-    auto unit_m = [&](int u) { return MC ? 2 * (u / num_n) + (int)crank : u / num_n; };
+    // work units: one tile, or (clustered) a pair of vertically adjacent tiles per cluster
+    const uint32_t crank = CL ? cluster_ctarank() : 0;
+    const int num_units = (CL ? (num_m + 1) / 2 : num_m) * num_n;
+    const int unit0 = CL ? blockIdx.x / 2 : blockIdx.x;
+    const int ustride = CL ? gridDim.x / 2 : gridDim.x;
+    auto unit_m = [&](int u) { return CL ? 2 * (u / num_n) + (int)crank : u / num_n; };
+    // PAIR: the even CTA's barriers that both CTAs' copies and epilogues signal
+    auto lead_bar = [&](int i) { return mapa_shared(bar(i), 0); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::STAGES; ++s) {
             mbar_init(bar(FULL + s), 1);
-            mbar_init(bar(EMPTY + s), MC ? 2 : 1);
+            mbar_init(bar(EMPTY + s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar(TFULL + a), 1);
-            mbar_init(bar(TEMPTY + a), 128);
+            mbar_init(bar(TEMPTY + a), PAIR ? 256 : 128);   // every epilogue thread of the tile's CTAs
         }
         mbar_init(bar(MMA_DONE), 1);
         for (int w = 0; w < 16; ++w) mbar_init(bar(RES + w), 1);
@@ -126,15 +144,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC)) : "memory");
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(S::TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1) tmem_alloc<CG>(smem_u32(tmem_slot), S::TMEM_COLS);   // PAIR: both CTAs, collectively
     tc_fence_before();
     __syncthreads();
-    if constexpr (MC) cluster_sync();   // the peer's multicasts may target these barriers only after init
+    if constexpr (CL) cluster_sync();   // the peer's copies and commits may target these barriers only after init
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -157,13 +170,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const uint32_t sa = sbase + s * S::STAGE_BYTES;
                     const uint32_t sb = sa + A_BYTES;
+                    if constexpr (PAIR) {
+                        // both CTAs' halves land on the even CTA's full barrier, which expects both
+                        if (crank == 0) mbar_expect_tx(bar(FULL + s), 2 * S::STAGE_BYTES);
+                        tma_load_2d_pair(sa, &tmA, kb * BK, m_t * BM, lead_bar(FULL + s));
+                        tma_load_2d_pair(sb, &tmB, kb * BK, n_t * BN + (int)crank * (BN / 2), lead_bar(FULL + s));
+                        if (crank == 0) {
+                            armed[s] = true;
+                            armed_parity[s] = r & 1;
+                        }
+                        continue;
+                    }
                     mbar_expect_tx(bar(FULL + s), S::STAGE_BYTES);
                     tma_load_2d(sa, &tmA, kb * BK, m_t * BM, bar(FULL + s));
-                    if constexpr (MC)   // this CTA's half of the weight tile, into both CTAs
-                        tma_load_2d_mc(sb + crank * (BN / 2) * 128, &tmB, kb * BK, n_t * BN + crank * (BN / 2),
-                                       bar(FULL + s), 0x3);
-                    else
-                        tma_load_2d(sb, &tmB, kb * BK, n_t * BN, bar(FULL + s));
+                    tma_load_2d(sb, &tmB, kb * BK, n_t * BN, bar(FULL + s));
                     armed[s] = true;
                     armed_parity[s] = r & 1;
                 }
@@ -174,15 +194,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc(BM, BN);
+        // ---------------- MMA issuer (PAIR: the even CTA's, for both) ----------------
+        if (lane == 0 && (!PAIR || crank == 0)) {
+            constexpr uint32_t idesc = make_idesc(PAIR ? 2 * BM : BM, BN);
             uint32_t g = 0;
             int it = 0;
             bool ok = true;
             for (int u = unit0; u < num_units && ok; u += ustride, ++it) {
                 const int acc = it & 1, use = it >> 1;
-                if (!mbar_wait(bar(TEMPTY + acc), (use & 1) ^ 1, abort_flag)) {
+                if (!(PAIR ? mbar_wait_cluster(bar(TEMPTY + acc), (use & 1) ^ 1, abort_flag)
+                           : mbar_wait(bar(TEMPTY + acc), (use & 1) ^ 1, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -191,7 +212,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int kb = 0; kb < num_k; ++kb, ++g) {
                     const int s = g % S::STAGES;
                     const uint32_t r = g / S::STAGES;
-                    if (!mbar_wait(bar(FULL + s), r & 1, abort_flag)) {
+                    if (!(PAIR ? mbar_wait_cluster(bar(FULL + s), r & 1, abort_flag)
+                               : mbar_wait(bar(FULL + s), r & 1, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -200,21 +222,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t adesc = sw128_desc(sa);
                     const uint64_t bdesc = sw128_desc(sa + A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
-                    if constexpr (MC) mma_commit_mc(bar(EMPTY + s), 0x3);   // both CTAs' stage s
+                    for (int k = 0; k < BK / 16; ++k) {
+                        if constexpr (PAIR) mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                        else mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                    }
+                    if constexpr (PAIR) mma_commit_pair(bar(EMPTY + s), 0x3);   // both CTAs' stage s
                     else mma_commit(bar(EMPTY + s));
                 }
                 if (!ok) break;
-                mma_commit(bar(TFULL + acc));
+                if constexpr (PAIR) mma_commit_pair(bar(TFULL + acc), 0x3);   // both CTAs' accumulator halves
+                else mma_commit(bar(TFULL + acc));
             }
             // every MMA issued must be finished before TMEM is freed
-            mma_commit(bar(MMA_DONE));
+            if constexpr (PAIR) mma_commit_pair(bar(MMA_DONE), 0x1);
+            else mma_commit(bar(MMA_DONE));
             mbar_wait_drain(bar(MMA_DONE), 0);
         }
         __syncwarp();
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
+        // a warp reads TMEM lanes [32 * (warp % 4), +32): rows of its quadrant
         const int quad = warp & 3;
         const int row_local = quad * 32 + lane;
         uint8_t* stage = smem + S::OUT_OFF + (warp - 2) * 8192;   // this warp's two staging boxes
@@ -265,9 +292,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
 #pragma unroll 1
                 for (int g = 0; g < BN / 64; ++g) {
+                    const int col = g * 64;
                     float v[64];
-                    tmem_ld64(taddr + g * 64, v);
-                    store64(v, n_t * BN + g * 64, y_box);
+                    tmem_ld64(taddr + col, v);
+                    store64(v, n_t * BN + col, y_box);
                 }
             } else if constexpr (EPI == GEMM_EPI_ADD_F32) {
                 // this warp's 32 x BN slice of the residual, one 32-column box
@@ -333,8 +361,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
 #pragma unroll 1
                 for (int hh = 0; hh < BN / 64; ++hh) {
+                    const int col = hh * 64;
                     float v[64];   // one head: v[j] pairs with v[j + 32]
-                    tmem_ld64(taddr + hh * 64, v);
+                    tmem_ld64(taddr + col, v);
                     if (rope) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
@@ -344,23 +373,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             v[j + 32] = b;
                         }
                     }
-                    store64(v, n_t * BN + hh * 64, y_box);
+                    store64(v, n_t * BN + col, y_box);
                 }
             } else {   // GEMM_EPI_GEGLU (BN == 256): columns [0, 128) GELU inputs, [128, 256) gates
                 if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int g = 0; g < BN / 128; ++g) {
+                    const int col = g * 64;
                     float a[64], gt[64];
-                    tmem_ld64(taddr + g * 64, a);
-                    tmem_ld64(taddr + BN / 2 + g * 64, gt);
+                    tmem_ld64(taddr + col, a);
+                    tmem_ld64(taddr + BN / 2 + col, gt);
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) a[j] = gelu_erf(a[j]) * gt[j];
-                    store64(a, n_t * (BN / 2) + g * 64, y_box);
+                    for (int j = 0; j < 64; ++j) a[j] = gelu_as(a[j]) * gt[j];
+                    store64(a, n_t * (BN / 2) + col, y_box);
                 }
             }
             tc_fence_before();
-            mbar_arrive(bar(TEMPTY + acc));
+            if constexpr (PAIR) mbar_arrive_cluster(lead_bar(TEMPTY + acc));
+            else mbar_arrive(bar(TEMPTY + acc));
         }
         if (EPI == GEMM_EPI_ADD_F32 && lane == 0)   // residual loads still in flight land before exit
             for (int b = 0; b < RB; ++b)
@@ -370,14 +401,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    // PAIR: the even CTA's MMAs (which write both CTAs' tensor memory) have
+    // drained before either CTA frees it
+    if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(S::TMEM_COLS)
-                     : "memory");
+        tmem_dealloc<CG>(tmem_base, S::TMEM_COLS);
     }
     if (threadIdx.x == 0 && *abort_flag && p.status) atomicOr(p.status, TEE_STATUS_TIMEOUT);
-    // the peer's last multicast commits target this CTA's barriers: leave together
-    if constexpr (MC) cluster_sync();
+    // the peer's last copies, commits and arrivals target this CTA's barriers: leave together
+    if constexpr (CL) cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -427,16 +460,17 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, int K, int box_rows) 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI, bool MC>
+template <int BN, int EPI, int MODE>
 cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const Params& p, int units,
                      cudaStream_t s) {
-    static int max_grid = 0;   // CTAs that can be resident at once (a multiple of 2 with MC)
-    constexpr uint32_t smem = Smem<BN, EPI>::TOTAL;
-    auto kernel = gemm_tc_kernel<BN, EPI, MC>;
+    constexpr bool CL = MODE != MODE_SINGLE;
+    static int max_grid = 0;   // CTAs that can be resident at once (a multiple of 2 when clustered)
+    constexpr uint32_t smem = Smem<BN, EPI, MODE>::TOTAL;
+    auto kernel = gemm_tc_kernel<BN, EPI, MODE>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = MC ? 2 : 1;
+    attr[0].val.clusterDim.x = CL ? 2 : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(NUM_THREADS);
@@ -447,7 +481,7 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
     if (!max_grid) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        if (MC) {
+        if (CL) {
             int clusters = 0;
             cfg.gridDim = dim3(2 * g_num_sms);
             e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
@@ -457,7 +491,7 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
             max_grid = g_num_sms;
         }
     }
-    const int per_unit = MC ? 2 : 1;
+    const int per_unit = CL ? 2 : 1;
     const int grid = units * per_unit < max_grid ? units * per_unit : max_grid;
     cfg.gridDim = dim3(grid);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ma, mb, mc, p);
@@ -484,12 +518,15 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     const int BN = add_wide ? 192
                  : (a.epi == GEMM_EPI_ADD_F32 ? 128 : ((a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128));
     const int num_m = (a.M + BM - 1) / BM;
-    // pairs of CTAs share the weight tile (256-column tiles, at least two row
-    // tiles); the residual projections measured no gain from it
-    const bool mc = num_m >= 2 && BN == 256;
+    // CTA pairs compute 256-row tiles when there are at least two row tiles,
+    // except for the short-K residual projection, whose fp32 residual traffic
+    // per tile is large next to its MMA time: paired CTAs wait on each other's
+    // residual loads and measured slower than independent ones
+    const bool pair_ok = !(a.epi == GEMM_EPI_ADD_F32 && !add_wide);
+    const int mode = num_m >= 2 && pair_ok ? MODE_PAIR : MODE_SINGLE;
+    const int b_rows = mode == MODE_SINGLE ? BN : BN / 2;
     CUtensorMap ma, mb, mc_map;
-    if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, mc ? BN / 2 : BN))
-        return cudaErrorInvalidValue;
+    if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, b_rows)) return cudaErrorInvalidValue;
     if (a.epi == GEMM_EPI_ADD_F32) {
         if (!make_out_map(&mc_map, a.C, a.M, a.N, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32)) return cudaErrorInvalidValue;
     } else if (!make_out_map(&mc_map, a.C, a.M, a.epi == GEMM_EPI_GEGLU ? a.N / 2 : a.N,
@@ -497,10 +534,10 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     }
     Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status};
-    const int units = (mc ? (num_m + 1) / 2 : num_m) * (a.N / BN);
+    const int units = (mode != MODE_SINGLE ? (num_m + 1) / 2 : num_m) * (a.N / BN);
 #define TEE_GEMM_DISPATCH(BN_, EPI_)                                                                  \
-    return mc ? launch_t<BN_, EPI_, true>(ma, mb, mc_map, p, units, s)                               \
-              : launch_t<BN_, EPI_, false>(ma, mb, mc_map, p, units, s)
+    return mode == MODE_PAIR ? launch_t<BN_, EPI_, MODE_PAIR>(ma, mb, mc_map, p, units, s)           \
+                             : launch_t<BN_, EPI_, MODE_SINGLE>(ma, mb, mc_map, p, units, s)
     if (add_wide) TEE_GEMM_DISPATCH(192, GEMM_EPI_ADD_F32);
     if (BN == 256) {
         switch (a.epi) {
