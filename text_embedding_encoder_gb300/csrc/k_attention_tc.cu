@@ -309,9 +309,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int i = 0; i < 64; ++i)
                         if (i < lo || i >= hi) v[i] = -INFINITY;
                 }
-                float mx = v[0];
+                // row maximum and (below) row sum over eight independent
+                // partials: short dependency chains for the latency-bound warps
+                float m8[8];
 #pragma unroll
-                for (int i = 1; i < 64; ++i) mx = fmaxf(mx, v[i]);
+                for (int k = 0; k < 8; ++k) m8[k] = v[k];
+#pragma unroll
+                for (int i = 8; i < 64; ++i) m8[i & 7] = fmaxf(m8[i & 7], v[i]);
+                float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 float* red_t = red + (t & 1) * 256;
                 red_t[half * 128 + r] = mx;
                 pair_sync();
@@ -348,12 +354,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                float sum = 0.f;
+                float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
                     v[i] = ex2_approx(fmaf(v[i], sl2, -m_use));
-                    sum += v[i];
+                    s8[i & 7] += v[i];
                 }
+                const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
                 uint8_t* prow = prow0 + sb * P_BYTES;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
