@@ -128,8 +128,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t g = 0;   // KV tiles issued
             int ui = 0;
             bool ok = true;
+            int4 it_next = p.items[blockIdx.x / p.n_heads];   // work items are read a unit ahead
             for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
-                const int4 it = p.items[u / p.n_heads];
+                const int4 it = it_next;
+                if (u + gridDim.x < p.n_units) it_next = p.items[(u + gridDim.x) / p.n_heads];
                 const int head = u % p.n_heads;
                 const int nk = n_kv_tiles(it);
                 const int qb = ui & 1;
@@ -192,8 +194,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool pend_first = false;
             int pend_ub = 0;
             int ui = 0;
+            int4 it_next = p.items[blockIdx.x / p.n_heads];
             for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
-                const int nk = n_kv_tiles(p.items[u / p.n_heads]);
+                const int nk = n_kv_tiles(it_next);
+                if (u + gridDim.x < p.n_units) it_next = p.items[(u + gridDim.x) / p.n_heads];
                 const int qb = ui & 1;
                 if (!mbar_wait(bar(B_QF + qb), (ui >> 1) & 1, abort_flag)) break;
                 const uint64_t qdesc = sw128_desc(sbase + OFF_Q + qb * TILE_BYTES);
@@ -280,8 +284,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         };
 
         int ui = 0;
+        int4 it_next = p.items[blockIdx.x / p.n_heads];
         for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
-            const int4 it = p.items[u / p.n_heads];
+            const int4 it = it_next;
+            if (u + gridDim.x < p.n_units) it_next = p.items[(u + gridDim.x) / p.n_heads];
             const int head = u % p.n_heads;
             const int q_start = it.x, q_len = it.y, k_lo = it.z, k_hi = it.w;
             const int nk = n_kv_tiles(it);
