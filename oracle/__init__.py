@@ -22,6 +22,10 @@ embeddings).  Citations in this package name that page and its sections:
 * §精度と量子化 -- the -q8 integer path: stored weight blocks unchanged,
   activations rounded per row to 7 bits with one scale.
 
+The per-token (multi-vector) output follows the page "Les Embeddings
+multimodaux dans Llama.cpp et GGUF" (jina.ai), section "Problèmes restants":
+multi-vector embeddings are one linear layer over the token states.
+
 Floating point is fp64 throughout (inputs widened from their fp32 or bf16
 storage); the integer path accumulates exactly in int64.  Every function is
 pinned by a test in ``tests/test_oracle_*.py`` against something other than
@@ -40,6 +44,8 @@ from .encoder import (  # noqa: F401
     encode_text_states,
     encode_text,
     encode_packed,
+    encode_text_tokens,
+    encode_packed_tokens,
     cosine,
 )
 from .precision import round_to_bf16  # noqa: F401

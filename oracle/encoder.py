@@ -157,7 +157,10 @@ class OracleModel:
                     ``oracle.w8a8``; embedding and gains stay fp32.
 
     ``weights`` needs attributes tok_emb, ln_attn, wqkv, wo, ln_mlp, wi,
-    wo_ffn (lists per layer), in the layouts documented by the C header.
+    wo_ffn (lists per layer), in the layouts documented by the C header, and
+    ln_emb / ln_final / w_proj when the shape enables the optional embedding
+    norm, final norm or per-token projection (stored like the other gains and
+    projections of the variant).
     """
 
     def __init__(self, weights, shape, variant: str = "fp32"):
@@ -170,13 +173,18 @@ class OracleModel:
         self.tok_emb = conv(weights.tok_emb)  # kept fp32-sized; rows are widened on use
         self.ln_attn = [wide(g) for g in weights.ln_attn]
         self.ln_mlp = [wide(g) for g in weights.ln_mlp]
+        self.ln_emb = wide(weights.ln_emb) if getattr(shape, "emb_norm", False) else None
+        self.ln_final = wide(weights.ln_final) if getattr(shape, "final_norm", False) else None
+        names = ("wqkv", "wo", "wi", "wo_ffn")
+        proj = [weights.w_proj] if getattr(shape, "proj_dim", 0) else []
         if variant == "w8a8":
             from .w8a8 import quantize_weight_blocks
             self.q = {name: [quantize_weight_blocks(np.asarray(w, np.float32)) for w in getattr(weights, name)]
-                      for name in ("wqkv", "wo", "wi", "wo_ffn")}
+                      for name in names}
+            self.q["w_proj"] = [quantize_weight_blocks(np.asarray(w, np.float32)) for w in proj]
         else:
-            self.lin = {name: [wide(w) for w in getattr(weights, name)]
-                        for name in ("wqkv", "wo", "wi", "wo_ffn")}
+            self.lin = {name: [wide(w) for w in getattr(weights, name)] for name in names}
+            self.lin["w_proj"] = [wide(w) for w in proj]
 
     def linear(self, name: str, layer: int, x) -> np.ndarray:
         """y = x W^T (no bias: the page mentions none on any projection)."""
@@ -196,7 +204,9 @@ def encode_text_states(ids, model: OracleModel) -> np.ndarray:
         x += Wo_ffn . GeGLU(LN_mlp(x) Wi^T)
     with no embedding norm and no final norm (the page names neither; pooling
     is over the final layer's output).  Positions count from 0 at the text's
-    first token (BOS).
+    first token (BOS).  Optionally (``shape.emb_norm`` / ``shape.final_norm``,
+    the published ModernBERT layout) a bias-free LayerNorm is applied to the
+    token embeddings before layer 0 and to the last layer's output.
     """
     shape = model.shape
     H, nh, d, I = shape.hidden, shape.n_heads, shape.head_dim, shape.intermediate
@@ -204,6 +214,8 @@ def encode_text_states(ids, model: OracleModel) -> np.ndarray:
     L = ids.shape[0]
     pos = np.arange(L)
     x = model.tok_emb[ids].astype(np.float64)
+    if model.ln_emb is not None:
+        x = layernorm(x, model.ln_emb, shape.ln_eps)
     for l in range(shape.n_layers):
         is_global = layer_is_global(l, shape)
         base = shape.rope_base_global if is_global else shape.rope_base_local
@@ -219,7 +231,26 @@ def encode_text_states(ids, model: OracleModel) -> np.ndarray:
         n = layernorm(x, model.ln_mlp[l], shape.ln_eps)
         u = model.linear("wi", l, n)
         x = x + model.linear("wo_ffn", l, geglu(u, I))
+    if model.ln_final is not None:
+        x = layernorm(x, model.ln_final, shape.ln_eps)
     return x
+
+
+def encode_text_tokens(ids, model: OracleModel) -> np.ndarray:
+    """Per-token unit vectors [L, D] of one text (multi-vector output).
+
+    Page "Les Embeddings multimodaux dans Llama.cpp et GGUF", section
+    "Problèmes restants": multi-vector embeddings come from a single linear
+    layer applied to the token states.  Reading: the final per-token states
+    (after the optional final norm), times the projection W_proj^T when the
+    shape has one (D = proj_dim, else D = H), each scaled to unit length with
+    the norm floored at 1e-12, as the pooled vector is.
+    """
+    s = encode_text_states(ids, model)
+    if model.shape.proj_dim:
+        s = model.linear("w_proj", 0, s)
+    norms = np.maximum(np.linalg.norm(s, axis=1, keepdims=True), 1e-12)
+    return s / norms
 
 
 def encode_text(ids, model: OracleModel) -> np.ndarray:
@@ -241,4 +272,16 @@ def encode_packed(ids, cu_seqlens, model: OracleModel, texts=None) -> np.ndarray
     out = np.full((n, model.shape.hidden), np.nan)
     for j in (range(n) if texts is None else texts):
         out[j] = encode_text(np.asarray(ids)[cu[j]:cu[j + 1]], model)
+    return out
+
+
+def encode_packed_tokens(ids, cu_seqlens, model: OracleModel, texts=None) -> np.ndarray:
+    """Per-token unit vectors [T, D] of a packed batch, text by text (rows of
+    texts outside ``texts`` are left as NaN)."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    n = cu.shape[0] - 1
+    width = model.shape.proj_dim or model.shape.hidden
+    out = np.full((int(cu[-1]), width), np.nan)
+    for j in (range(n) if texts is None else texts):
+        out[cu[j]:cu[j + 1]] = encode_text_tokens(np.asarray(ids)[cu[j]:cu[j + 1]], model)
     return out

@@ -216,9 +216,11 @@ MICRO = synth.Shape(n_layers=4, hidden=8, n_heads=2, head_dim=4, intermediate=6,
                     global_every=3, window=2, rope_base_global=50.0, rope_base_local=7.0, ln_eps=1e-5)
 
 
-def _brute_encode(ids, lengths, w, shape):
+def _brute_encode(ids, lengths, w, shape, tokens=False):
     """Scalar loops over the packed sequence: every step written out from the
-    definition, with a dense same-text/window mask and complex RoPE."""
+    definition, with a dense same-text/window mask and complex RoPE.  With
+    ``tokens`` it returns the per-token unit vectors (projected when the shape
+    has a projection) instead of the pooled ones."""
     H, nh, d, I = shape.hidden, shape.n_heads, shape.head_dim, shape.intermediate
     T = len(ids)
     text, pos = [], []
@@ -238,6 +240,8 @@ def _brute_encode(ids, lengths, w, shape):
         return 0.5 * math.erfc(-a / math.sqrt(2.0))
 
     x = [[float(w.tok_emb[i][c]) for c in range(H)] for i in ids]
+    if shape.emb_norm:
+        x = [ln(row, w.ln_emb) for row in x]
     for l in range(shape.n_layers):
         glob = l % shape.global_every == 0
         base = shape.rope_base_global if glob else shape.rope_base_local
@@ -271,6 +275,11 @@ def _brute_encode(ids, lengths, w, shape):
             z = [u[c] * phi(u[c]) * u[I + c] for c in range(I)]
             y = matvec(w.wo_ffn[l], z)
             x[t] = [x[t][c] + y[c] for c in range(H)]
+    if shape.final_norm:
+        x = [ln(row, w.ln_final) for row in x]
+    if tokens:
+        rows = [matvec(w.w_proj, row) if shape.proj_dim else row for row in x]
+        return np.array([[a / math.sqrt(sum(b * b for b in row)) for a in row] for row in rows])
     out = []
     start = 0
     for n in lengths:
@@ -299,6 +308,63 @@ def test_encoder_matches_scalar_bruteforce(variant):
         w.tok_emb = oracle.round_to_bf16(w.tok_emb)
     want = _brute_encode(ids, lengths, w, MICRO)
     np.testing.assert_allclose(got, want, atol=1e-12)
+
+
+MICRO_EXT = synth.Shape(**{**MICRO.as_dict(), "emb_norm": True, "final_norm": True, "proj_dim": 5})
+
+
+def _rounded(w, variant):
+    """The weights as the bf16 variant stores them (for the brute force)."""
+    if variant == "bf16":
+        for name in ("wqkv", "wo", "wi", "wo_ffn", "ln_attn", "ln_mlp"):
+            setattr(w, name, [oracle.round_to_bf16(a) for a in getattr(w, name)])
+        for name in ("tok_emb", "ln_emb", "ln_final", "w_proj"):
+            if getattr(w, name) is not None:
+                setattr(w, name, oracle.round_to_bf16(getattr(w, name)))
+    return w
+
+
+@pytest.mark.parametrize("variant", ["fp32", "bf16"])
+def test_optional_norms_and_token_output_match_scalar_bruteforce(variant):
+    # embedding norm, final norm, and the per-token projected unit vectors
+    lengths = [1, 3, 7, 5]
+    w = synth.make_weights(MICRO_EXT, seed=7, std=0.5)
+    ids, cu = synth.make_batch(lengths, MICRO.vocab, seed=8)
+    model = oracle.OracleModel(w, MICRO_EXT, variant)
+    pooled = oracle.encode_packed(ids, cu, model)
+    toks = oracle.encode_packed_tokens(ids, cu, model)
+    assert toks.shape == (sum(lengths), MICRO_EXT.proj_dim)
+    w = _rounded(w, variant)
+    np.testing.assert_allclose(pooled, _brute_encode(ids, lengths, w, MICRO_EXT), atol=1e-12)
+    np.testing.assert_allclose(toks, _brute_encode(ids, lengths, w, MICRO_EXT, tokens=True), atol=1e-12)
+
+
+def test_optional_norms_change_the_result_and_draws_stay_put():
+    # the optional parts are drawn after the layers: the shared weights are identical
+    base = synth.make_weights(MICRO, seed=7, std=0.5)
+    ext = synth.make_weights(MICRO_EXT, seed=7, std=0.5)
+    np.testing.assert_array_equal(base.tok_emb, ext.tok_emb)
+    for l in range(MICRO.n_layers):
+        np.testing.assert_array_equal(base.wo_ffn[l], ext.wo_ffn[l])
+    ids, cu = synth.make_batch([6, 4], MICRO.vocab, seed=9)
+    a = oracle.encode_packed(ids, cu, oracle.OracleModel(base, MICRO))
+    b = oracle.encode_packed(ids, cu, oracle.OracleModel(ext, MICRO_EXT))
+    assert np.abs(a - b).max() > 1e-3
+
+
+def test_token_output_closed_forms():
+    # no projection: a one-token text's token vector is its pooled vector;
+    # identity projection = no projection; every token vector has unit norm
+    shape = synth.TINY
+    w = synth.make_weights(shape, seed=10)
+    ids, cu = synth.make_batch([1, 9, 30], shape.vocab, seed=11)
+    model = oracle.OracleModel(w, shape)
+    toks = oracle.encode_packed_tokens(ids, cu, model)
+    np.testing.assert_allclose(np.linalg.norm(toks, axis=1), 1.0, atol=1e-14)
+    np.testing.assert_allclose(toks[0], oracle.encode_packed(ids, cu, model)[0], atol=1e-14)
+    eye = synth.Shape(**{**shape.as_dict(), "proj_dim": shape.hidden})
+    w.w_proj = np.eye(shape.hidden, dtype=np.float32)
+    np.testing.assert_allclose(oracle.encode_packed_tokens(ids, cu, oracle.OracleModel(w, eye)), toks, atol=1e-14)
 
 
 def test_encoder_zero_projections_is_mean_embedding():

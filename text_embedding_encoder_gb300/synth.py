@@ -9,8 +9,9 @@ Recipe (stated once, used everywhere):
 
 * weights: one ``numpy.random.Generator(PCG64(seed))`` per model, drawn in a
   fixed order -- the token embedding E, then per layer gamma_attn, Wqkv, Wo,
-  gamma_mlp, Wi, Wo_ffn.  Linear and embedding entries are N(0, 0.02^2) in
-  fp32; LayerNorm gains are 1 + 0.02 * N(0, 1).
+  gamma_mlp, Wi, Wo_ffn, then (when the shape enables them) gamma_emb,
+  gamma_final and the per-token projection.  Linear and embedding entries are
+  N(0, 0.02^2) in fp32; LayerNorm gains are 1 + 0.02 * N(0, 1).
 * outlier variant: a fixed set of hidden channels (a seeded permutation) has
   both LayerNorm gains of every layer multiplied by 20, so the inputs of the
   QKV and Wi projections carry large per-channel outliers.
@@ -46,6 +47,12 @@ class Shape:
     rope_base_global: float = 160000.0
     rope_base_local: float = 10000.0
     ln_eps: float = 1e-5
+    # optional parts (off in the page's encoder): a LayerNorm on the token
+    # embeddings, one on the last layer's output, and the width of a per-token
+    # output projection (0 = none)
+    emb_norm: bool = False
+    final_norm: bool = False
+    proj_dim: int = 0
 
     def as_dict(self):
         return asdict(self)
@@ -82,6 +89,9 @@ class Weights:
     ln_mlp: list = field(default_factory=list)
     wi: list = field(default_factory=list)
     wo_ffn: list = field(default_factory=list)
+    ln_emb: np.ndarray | None = None      # [H], with Shape.emb_norm
+    ln_final: np.ndarray | None = None    # [H], with Shape.final_norm
+    w_proj: np.ndarray | None = None      # [proj_dim, H], with Shape.proj_dim > 0
 
 
 def _normal(rng, shape, std):
@@ -107,6 +117,14 @@ def make_weights(shape: Shape, seed: int = 0, std: float = 0.02, outliers: bool 
         w.ln_mlp.append(np.float32(1.0) + _normal(rng, (H,), 0.02))
         w.wi.append(_normal(rng, (2 * I, H), std))
         w.wo_ffn.append(_normal(rng, (H, I), std))
+    # the optional parts are drawn after every layer, so enabling them leaves
+    # the draws above unchanged
+    if shape.emb_norm:
+        w.ln_emb = np.float32(1.0) + _normal(rng, (H,), 0.02)
+    if shape.final_norm:
+        w.ln_final = np.float32(1.0) + _normal(rng, (H,), 0.02)
+    if shape.proj_dim:
+        w.w_proj = _normal(rng, (shape.proj_dim, H), std)
     if outliers:
         ch = outlier_channels(H)
         for l in range(L):
