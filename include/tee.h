@@ -54,7 +54,8 @@ extern "C" {
 
 /*
  * Encoder shape and run limits.  Readings where the page is silent:
- * pre-norm blocks, no embedding or final norm, no bias on any projection,
+ * pre-norm blocks, no embedding or final norm (both available as options for
+ * the published ModernBERT layout), no bias on any projection,
  * rotate-half RoPE pairing (j, j + head_dim/2), a window of |i - j| <= window
  * (inclusive), softmax scale 1/sqrt(head_dim), GeGLU = GELU_erf(first half)
  * * second half, LayerNorm with biased variance and eps inside the root.
@@ -74,6 +75,12 @@ typedef struct tee_config {
     int   dtype;             /* TEE_F32 | TEE_BF16 | TEE_W8A8                        */
     int   max_tokens;        /* capacity of one pass (sum of text lengths), >= 1     */
     int   max_texts;         /* capacity of one pass (number of texts), >= 1         */
+    /* optional parts, 0 = off (the page's encoder) */
+    int   emb_norm;          /* 1: bias-free LayerNorm (gain ln_emb) on the token embeddings  */
+    int   final_norm;        /* 1: bias-free LayerNorm (gain ln_final) on the last layer's output,
+                                before pooling or the per-token output                        */
+    int   proj_dim;          /* 0, or P (a multiple of 128, <= 1024): the per-token output of
+                                tee_encode_tokens is projected to P dimensions (w_proj)        */
 } tee_config;
 
 /*
@@ -95,6 +102,10 @@ typedef struct tee_weights {
     const float* const* ln_mlp;
     const float* const* wi;
     const float* const* wo_ffn;
+    const float*        ln_emb;     /* [H], read iff cfg.emb_norm (else may be NULL)       */
+    const float*        ln_final;   /* [H], read iff cfg.final_norm (else may be NULL)     */
+    const float*        w_proj;     /* [P * H], read iff cfg.proj_dim > 0 (else may be NULL);
+                                       stored like the four projections of the dtype     */
 } tee_weights;
 
 typedef struct tee_ctx tee_ctx;
@@ -144,6 +155,26 @@ int tee_encode(tee_ctx* ctx, const int32_t* token_ids, const int32_t* cu_seqlens
  */
 int tee_encode_device(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu,
                       int n_texts, float* d_out, void* stream);
+
+/*
+ * Per-token (multi-vector) output.  Page "Les Embeddings multimodaux dans
+ * Llama.cpp et GGUF" (jina.ai), section "Problèmes restants": multi-vector
+ * embeddings are one linear layer over the token states.  For every token t
+ * of the packed batch, in order: v_t = the final state (after the final norm
+ * when cfg.final_norm), times w_proj^T when cfg.proj_dim > 0; the output is
+ * v_t / max(|v_t|, 1e-12).  D = proj_dim if > 0, else hidden.
+ *   tee_encode_tokens         host ids / cu_seqlens as tee_encode; out host
+ *                             float[cu_seqlens[n_texts] * D]; synchronous.
+ *                             The first call allocates a device buffer of
+ *                             max_tokens * D floats, kept until tee_destroy.
+ *   tee_encode_tokens_device  device ids / cu_seqlens (+ host cu_seqlens) as
+ *                             tee_encode_device; d_out device float[T * D],
+ *                             16-byte aligned; asynchronous on `stream`.
+ * Errors as tee_encode / tee_encode_device; TEE_EINVAL for a misaligned d_out.
+ */
+int tee_encode_tokens(tee_ctx* ctx, const int32_t* token_ids, const int32_t* cu_seqlens, int n_texts, float* out);
+int tee_encode_tokens_device(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu,
+                             int n_texts, float* d_out, void* stream);
 
 /* Message of the last failure on this context ("" if none).  NULL ctx: the
  * message of the last failed context-free call in this process (tee_create,

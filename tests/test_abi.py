@@ -57,6 +57,7 @@ def _cfg(**over):
 @pytest.mark.parametrize("field,value", [
     ("head_dim", 32), ("hidden", 200), ("n_layers", 0), ("intermediate", 100), ("dtype", 7),
     ("max_tokens", 0), ("max_texts", 0), ("global_every", 0), ("window", -1), ("vocab", 0),
+    ("emb_norm", 2), ("final_norm", -1), ("proj_dim", 100), ("proj_dim", 2048), ("proj_dim", -128),
 ])
 def test_create_rejects_bad_config_without_a_device(built_lib, field, value):
     ctx = ctypes.c_void_p(123)
@@ -70,4 +71,6 @@ def test_create_rejects_bad_config_without_a_device(built_lib, field, value):
 def test_null_safety_without_a_device(built_lib):
     built_lib.tee_destroy(None)
     assert built_lib.tee_encode(None, None, None, 1, None) == binding.TEE_EINVAL
+    assert built_lib.tee_encode_tokens(None, None, None, 1, None) == binding.TEE_EINVAL
+    assert built_lib.tee_encode_tokens_device(None, None, None, None, 1, None, None) == binding.TEE_EINVAL
     assert built_lib.tee_create(None, 0, None) == binding.TEE_EINVAL

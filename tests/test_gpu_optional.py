@@ -1,0 +1,94 @@
+"""The optional parts of the encoder on the GPU against the oracle: the
+embedding and final LayerNorms (the published ModernBERT layout) and the
+per-token (multi-vector) output with and without a projection, in every
+arithmetic of the library, through the C ABI.
+
+Per-token vectors are held to the same bars as the pooled ones: fp32 max
+|GPU - oracle| <= 1e-4; bf16 cosine >= 0.9995 and max abs <= 3e-3 per vector;
+W8A8 (no outliers) cosine >= 0.9995 against the W8A8 oracle.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from text_embedding_encoder_gb300 import binding, synth
+
+torch = pytest.importorskip("torch")
+from gpu_util import BF16_COS, assert_embeddings_close, dev, make_encoder  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+EXT = synth.Shape(**{**synth.TINY.as_dict(), "emb_norm": True, "final_norm": True, "proj_dim": 128})
+NORMS_ONLY = synth.Shape(**{**synth.TINY.as_dict(), "emb_norm": True, "final_norm": True})
+LENGTHS = [1, 2, 8, 37, 64, 65, 150, 129]
+
+
+def _cos_rows(a, b):
+    return np.sum(a * b, axis=1) / (np.linalg.norm(a, axis=1) * np.linalg.norm(b, axis=1))
+
+
+@pytest.mark.parametrize("shape", [EXT, NORMS_ONLY], ids=["norms+proj128", "norms"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_pooled_and_token_outputs(lib, shape, dtype):
+    w = synth.make_weights(shape, seed=3, std=0.05)
+    ids, cu = synth.make_batch(LENGTHS, shape.vocab, seed=4)
+    enc = make_encoder(shape, dtype, w, max_tokens=1024, max_texts=16)
+    model = oracle.OracleModel(w, shape, dtype)
+    assert_embeddings_close(enc.encode(ids, cu), oracle.encode_packed(ids, cu, model), dtype)
+    toks = enc.encode_tokens(ids, cu)
+    assert toks.shape == (len(ids), shape.proj_dim or shape.hidden)
+    want = oracle.encode_packed_tokens(ids, cu, model)
+    assert_embeddings_close(toks, want, dtype)
+    np.testing.assert_allclose(np.linalg.norm(toks, axis=1), 1.0, atol=1e-5)
+    # the device path writes the same vectors
+    d_out = torch.empty(len(ids), enc.token_width, device="cuda")
+    enc.encode_tokens_device(dev(ids), dev(cu), cu, d_out)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(d_out.cpu().numpy(), toks)
+    enc.close()
+
+
+def test_token_output_w8a8(lib):
+    shape = EXT
+    w = synth.make_weights(shape, seed=5)
+    ids, cu = synth.make_batch([8, 37, 64, 150], shape.vocab, seed=6)
+    enc = make_encoder(shape, "w8a8", w, max_tokens=512, max_texts=8)
+    toks = enc.encode_tokens(ids, cu)
+    want = oracle.encode_packed_tokens(ids, cu, oracle.OracleModel(w, shape, "w8a8"))
+    cos = _cos_rows(toks.astype(np.float64), want)
+    assert cos.min() >= BF16_COS, cos.min()
+    enc.close()
+
+
+def test_ruri_token_output_bf16(lib):
+    shape = synth.Shape(**{**synth.RURI_310M.as_dict(), "emb_norm": True, "final_norm": True, "proj_dim": 128})
+    w = synth.make_weights(shape, seed=0)
+    ids, cu = synth.make_batch([8, 57, 190], shape.vocab, seed=0)
+    enc = make_encoder(shape, "bf16", w, max_tokens=512, max_texts=8)
+    model = oracle.OracleModel(w, shape, "bf16")
+    assert_embeddings_close(enc.encode_tokens(ids, cu), oracle.encode_packed_tokens(ids, cu, model), "bf16")
+    assert_embeddings_close(enc.encode(ids, cu), oracle.encode_packed(ids, cu, model), "bf16")
+    enc.close()
+
+
+def test_optional_weights_and_output_are_validated(lib):
+    shape = EXT
+    w = synth.make_weights(shape, seed=3)
+    enc = binding.Encoder(shape, "bf16", max_tokens=256, max_texts=8)
+    w_missing = synth.make_weights(shape, seed=3)
+    w_missing.w_proj = None
+    with pytest.raises(binding.TeeError) as e:
+        enc.load_weights(w_missing)
+    assert e.value.code == binding.TEE_EINVAL
+    enc.load_weights(w)
+    ids, cu = synth.make_batch([5, 9], shape.vocab, seed=1)
+    buf = torch.empty(len(ids) * 128 + 4, device="cuda")
+    rc = enc.lib.tee_encode_tokens_device(enc.ctx, dev(ids).data_ptr(), dev(cu).data_ptr(),
+                                          np.ascontiguousarray(cu).ctypes.data, 2, buf.data_ptr() + 4, None)
+    assert rc == binding.TEE_EINVAL
+    toks = enc.encode_tokens(ids, cu)   # the context is still usable
+    assert np.all(np.isfinite(toks))
+    assert enc.device_status() == 0
+    enc.close()

@@ -38,6 +38,7 @@ class TeeConfig(ctypes.Structure):
         ("global_every", ctypes.c_int), ("window", ctypes.c_int),
         ("rope_base_global", ctypes.c_float), ("rope_base_local", ctypes.c_float), ("ln_eps", ctypes.c_float),
         ("dtype", ctypes.c_int), ("max_tokens", ctypes.c_int), ("max_texts", ctypes.c_int),
+        ("emb_norm", ctypes.c_int), ("final_norm", ctypes.c_int), ("proj_dim", ctypes.c_int),
     ]
 
 
@@ -47,7 +48,8 @@ _FPP = ctypes.POINTER(_FP)
 
 class TeeWeights(ctypes.Structure):
     _fields_ = [("tok_emb", _FP), ("ln_attn", _FPP), ("wqkv", _FPP), ("wo", _FPP),
-                ("ln_mlp", _FPP), ("wi", _FPP), ("wo_ffn", _FPP)]
+                ("ln_mlp", _FPP), ("wi", _FPP), ("wo_ffn", _FPP),
+                ("ln_emb", _FP), ("ln_final", _FP), ("w_proj", _FP)]
 
 
 class TeeKernelStat(ctypes.Structure):
@@ -66,6 +68,8 @@ SIGNATURES = {
     "tee_load_weights": (_i, [_ctx, ctypes.POINTER(TeeWeights)]),
     "tee_encode": (_i, [_ctx, _vp, _vp, _i, _vp]),
     "tee_encode_device": (_i, [_ctx, _vp, _vp, _vp, _i, _vp, _vp]),
+    "tee_encode_tokens": (_i, [_ctx, _vp, _vp, _i, _vp]),
+    "tee_encode_tokens_device": (_i, [_ctx, _vp, _vp, _vp, _i, _vp, _vp]),
     "tee_last_error": (ctypes.c_char_p, [_ctx]),
     "tee_destroy": (None, [_ctx]),
     "tee_profile_enable": (_i, [_ctx, _i]),
@@ -137,7 +141,9 @@ def _ptr(a) -> int:
 def config_from_shape(shape, dtype: str, max_tokens: int, max_texts: int) -> TeeConfig:
     return TeeConfig(shape.n_layers, shape.hidden, shape.n_heads, shape.head_dim, shape.intermediate, shape.vocab,
                      shape.global_every, shape.window, shape.rope_base_global, shape.rope_base_local,
-                     shape.ln_eps, DTYPES[dtype], int(max_tokens), int(max_texts))
+                     shape.ln_eps, DTYPES[dtype], int(max_tokens), int(max_texts),
+                     int(getattr(shape, "emb_norm", False)), int(getattr(shape, "final_norm", False)),
+                     int(getattr(shape, "proj_dim", 0)))
 
 
 class Encoder:
@@ -186,8 +192,12 @@ class Encoder:
             keep.append(ptrs)
             return ctypes.cast(ptrs, _FPP)
 
+        def opt(a):
+            return f32(a) if a is not None else None
+
         tw = TeeWeights(f32(w.tok_emb), arr(w.ln_attn), arr(w.wqkv), arr(w.wo), arr(w.ln_mlp), arr(w.wi),
-                        arr(w.wo_ffn))
+                        arr(w.wo_ffn), opt(getattr(w, "ln_emb", None)), opt(getattr(w, "ln_final", None)),
+                        opt(getattr(w, "w_proj", None)))
         self.check(self.lib.tee_load_weights(self.ctx, ctypes.byref(tw)))
 
     def encode(self, ids, cu_seqlens) -> np.ndarray:
@@ -203,6 +213,25 @@ class Encoder:
         h_cu = np.ascontiguousarray(h_cu, dtype=np.int32)
         self.check(self.lib.tee_encode_device(self.ctx, _ptr(d_ids), _ptr(d_cu), h_cu.ctypes.data,
                                               h_cu.shape[0] - 1, _ptr(d_out), stream))
+
+    @property
+    def token_width(self) -> int:
+        """Width D of the per-token output: proj_dim, else hidden."""
+        return int(getattr(self.shape, "proj_dim", 0)) or self.shape.hidden
+
+    def encode_tokens(self, ids, cu_seqlens) -> np.ndarray:
+        """Host arrays in, host fp32 [T, D] per-token unit vectors out (synchronous)."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        out = np.empty((int(cu[-1]) if cu.shape[0] else 0, self.token_width), dtype=np.float32)
+        self.check(self.lib.tee_encode_tokens(self.ctx, ids.ctypes.data, cu.ctypes.data, cu.shape[0] - 1,
+                                              out.ctypes.data))
+        return out
+
+    def encode_tokens_device(self, d_ids, d_cu, h_cu, d_out, stream=0):
+        h_cu = np.ascontiguousarray(h_cu, dtype=np.int32)
+        self.check(self.lib.tee_encode_tokens_device(self.ctx, _ptr(d_ids), _ptr(d_cu), h_cu.ctypes.data,
+                                                     h_cu.shape[0] - 1, _ptr(d_out), stream))
 
     def profile_enable(self, on=True):
         self.check(self.lib.tee_profile_enable(self.ctx, 1 if on else 0))

@@ -77,9 +77,9 @@ __global__ void positions_kernel(const int32_t* __restrict__ cu, int n_texts, in
 }
 
 // One warp per row; H a multiple of 128 and <= 1024 (at most 8 float4 per lane).
+// y may be x itself (fp32 output): a warp reads its whole row before writing it.
 template <typename TY>
-__global__ void layernorm_kernel(const float* __restrict__ x, const float* __restrict__ gamma, TY* __restrict__ y,
-                                 int T, int H, float eps) {
+__global__ void layernorm_kernel(const float* x, const float* __restrict__ gamma, TY* y, int T, int H, float eps) {
     int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     int lane = threadIdx.x & 31;
     if (warp >= T) return;
@@ -259,6 +259,32 @@ __global__ void pool_finish_kernel(const float* __restrict__ partial, const int3
     }
 }
 
+// One warp per row: x[r] /= max(|x[r]|, 1e-12), D a multiple of 4 and <= 1024;
+// the sum of squares in a fixed order (per-lane partials, then the shuffle tree).
+__global__ void l2_rows_kernel(float* x, int M, int D) {
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= M) return;
+    float4* r = reinterpret_cast<float4*>(x + (size_t)row * D);
+    const int nv = D / 4;
+    float4 v[8];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int c = i * 32 + lane;
+        if (c < nv) {
+            v[i] = r[c];
+            ss += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
+        }
+    }
+    const float scale = 1.0f / fmaxf(sqrtf(warp_sum(ss)), 1e-12f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int c = i * 32 + lane;
+        if (c < nv) r[c] = make_float4(v[i].x * scale, v[i].y * scale, v[i].z * scale, v[i].w * scale);
+    }
+}
+
 // Chunk offsets of the two-pass pool computed on the device from cu: text j
 // owns ceil(len_j / POOL_CHUNK) chunks; chunk_off[j] is the exclusive prefix
 // sum and chunk_off[n] the total.  One block; each thread scans a contiguous
@@ -356,6 +382,13 @@ cudaError_t launch_geglu(const void* u, void* z, bool bf16_act, int T, int I, cu
         geglu_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)u, (bf16*)z, T, I);
     else
         geglu_kernel<float><<<blocks, 256, 0, s>>>((const float*)u, (float*)z, T, I);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_l2_rows(float* x, int M, int D, cudaStream_t s) {
+    if (M == 0) return cudaSuccess;
+    if (D % 4 || D > 1024) return cudaErrorInvalidValue;
+    l2_rows_kernel<<<(M + 7) / 8, 256, 0, s>>>(x, M, D);
     return cudaGetLastError();
 }
 

@@ -84,6 +84,10 @@ int validate_config(const tee_config* c) {
     if (c->dtype != TEE_F32 && c->dtype != TEE_BF16 && c->dtype != TEE_W8A8) return fail(nullptr, TEE_EINVAL, "unknown dtype");
     if (c->max_tokens < 1 || c->max_texts < 1) return fail(nullptr, TEE_EINVAL, "max_tokens and max_texts must be >= 1");
     if (c->max_tokens > (1 << 24)) return fail(nullptr, TEE_EINVAL, "max_tokens must be <= 2^24");
+    if ((c->emb_norm != 0 && c->emb_norm != 1) || (c->final_norm != 0 && c->final_norm != 1))
+        return fail(nullptr, TEE_EINVAL, "emb_norm and final_norm must be 0 or 1");
+    if (c->proj_dim < 0 || c->proj_dim % 128 || c->proj_dim > 1024)
+        return fail(nullptr, TEE_EINVAL, "proj_dim must be 0 or a multiple of 128, <= 1024");
     return TEE_OK;
 }
 
@@ -141,6 +145,10 @@ size_t carve_weights(tee_ctx* c, void* base) {
             L.wd[w] = g.dtype == TEE_W8A8 ? cv.take<float>((size_t)N * K / 32) : nullptr;
         }
     }
+    c->ln_emb = g.emb_norm ? cv.take<float>(H) : nullptr;
+    c->ln_final = g.final_norm ? cv.take<float>(H) : nullptr;
+    c->w_proj = g.proj_dim ? cv.take<char>((size_t)g.proj_dim * H, esz) : nullptr;
+    c->w_proj_d = g.proj_dim && g.dtype == TEE_W8A8 ? cv.take<float>((size_t)g.proj_dim * H / 32) : nullptr;
     return cv.off;
 }
 
@@ -381,14 +389,24 @@ int step_pool(tee_ctx* ctx, const float* x, const int32_t* d_cu, const int32_t* 
     return TEE_OK;
 }
 
-int run_pass(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int T,
-             float* d_out, cudaStream_t s) {
+// fp32 LayerNorm of the residual stream in place (optional embedding / final norm).
+int step_norm_in_place(tee_ctx* ctx, const float* gamma, int T, cudaStream_t s) {
+    const tee_config& g = ctx->cfg;
+    LAUNCH(TEE_K_LAYERNORM, 0, (double)T * g.hidden * 8 + g.hidden * 4.0,
+           launch_layernorm(ctx->x, gamma, ctx->x, false, T, g.hidden, g.ln_eps, s));
+    return TEE_OK;
+}
+
+// Embedding and every layer: the final token states in ctx->x.
+int run_layers(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int T,
+               cudaStream_t s) {
     const tee_config& g = ctx->cfg;
     int rc;
     if (g.dtype == TEE_BF16 && (rc = prepare_attention_items(ctx, h_cu, n_texts, s))) return rc;
     LAUNCH(TEE_K_EMBED, 0, (double)T * 4 * 2, launch_positions(d_cu, n_texts, T, ctx->d_pos, s));
     LAUNCH(TEE_K_EMBED, 0, (double)T * g.hidden * (4.0 + (act_is_bf16(ctx) ? 2 : 4)) + T * 4.0,
            launch_embed(ctx->emb, act_is_bf16(ctx), d_ids, T, g.hidden, g.vocab, ctx->x, ctx->d_status, s));
+    if (g.emb_norm && (rc = step_norm_in_place(ctx, ctx->ln_emb, T, s))) return rc;
     for (int l = 0; l < g.n_layers; ++l) {
         if ((rc = step_layernorm(ctx, l, TEE_LN_ATTN, ctx->x, ctx->y, T, s))) return rc;
         if ((rc = step_qkv(ctx, l, ctx->y, ctx->d_pos, ctx->qkv, T, s))) return rc;
@@ -398,7 +416,56 @@ int run_pass(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int3
         if ((rc = step_ffn_in(ctx, l, ctx->y, ctx->z, T, s))) return rc;
         if ((rc = step_linear(ctx, l, TEE_W_FFN_OUT, ctx->z, ctx->x, T, 1, GEMM_EPI_ADD_F32, nullptr, s))) return rc;
     }
+    if (g.final_norm && (rc = step_norm_in_place(ctx, ctx->ln_final, T, s))) return rc;
+    return TEE_OK;
+}
+
+// One pass with the pooled output: unit vectors [n_texts, H] in d_out.
+int run_pass(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int T,
+             float* d_out, cudaStream_t s) {
+    int rc = run_layers(ctx, d_ids, d_cu, h_cu, n_texts, T, s);
+    if (rc) return rc;
     return step_pool(ctx, ctx->x, d_cu, h_cu, n_texts, T, d_out, s);
+}
+
+// One pass with the per-token output: unit vectors [T, D] in d_out (16-byte
+// aligned), D = proj_dim or hidden.
+int run_tokens(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int T,
+               float* d_out, cudaStream_t s) {
+    const tee_config& g = ctx->cfg;
+    int rc = run_layers(ctx, d_ids, d_cu, h_cu, n_texts, T, s);
+    if (rc) return rc;
+    const int H = g.hidden, P = g.proj_dim, D = P ? P : H;
+    if (!P) {
+        CK(cudaMemcpyAsync(d_out, ctx->x, (size_t)T * H * 4, cudaMemcpyDeviceToDevice, s));
+    } else if (g.dtype == TEE_W8A8) {
+        LAUNCH(TEE_K_QUANT, 0, (double)T * H * 5 + T * 4.0, launch_quant_rows7(ctx->x, T, H, ctx->qa, ctx->qs, s));
+        LAUNCH(TEE_K_GEMM, 2.0 * T * P * H, (double)T * H + (double)P * H + (double)T * P * 4,
+               launch_gemm_w8a8(ctx->qa, ctx->qs, (const int8_t*)ctx->w_proj, ctx->w_proj_d, d_out, nullptr, T, P, H,
+                                0, s));
+    } else if (g.dtype == TEE_BF16) {
+        // the projection's A operand in bf16, accumulated into a zeroed fp32 output
+        LAUNCH(TEE_K_ELEMENTWISE, 0, (double)T * H * 6,
+               launch_convert_f32_bf16(ctx->x, (bf16*)ctx->y, (size_t)T * H, s));
+        CK(cudaMemsetAsync(d_out, 0, (size_t)T * P * 4, s));
+        GemmTcArgs a{};
+        a.A = ctx->y;
+        a.W = ctx->w_proj;
+        a.C = d_out;
+        a.M = T;
+        a.N = P;
+        a.K = H;
+        a.epi = GEMM_EPI_ADD_F32;
+        a.hidden = H;
+        a.status = ctx->d_status;
+        LAUNCH(TEE_K_GEMM, 2.0 * T * P * H, (double)T * H * 2 + (double)P * H * 2 + (double)T * P * 8,
+               launch_gemm_tc(a, s));
+    } else {
+        LAUNCH(TEE_K_GEMM, 2.0 * T * P * H, (double)T * H * 4 + (double)P * H * 4 + (double)T * P * 4,
+               launch_gemm_simt(ctx->x, ctx->w_proj, d_out, false, T, P, H, 0, s));
+    }
+    LAUNCH(TEE_K_POOL, 0, (double)T * D * 8, launch_l2_rows(d_out, T, D, s));
+    return TEE_OK;
 }
 
 int check_ready(tee_ctx* ctx) {
@@ -457,6 +524,8 @@ int tee_load_weights(tee_ctx* ctx, const tee_weights* w) {
     for (int l = 0; l < g.n_layers; ++l)
         if (!w->ln_attn[l] || !w->wqkv[l] || !w->wo[l] || !w->ln_mlp[l] || !w->wi[l] || !w->wo_ffn[l])
             return fail(ctx, TEE_EINVAL, "layer %d has a NULL weight pointer", l);
+    if ((g.emb_norm && !w->ln_emb) || (g.final_norm && !w->ln_final) || (g.proj_dim && !w->w_proj))
+        return fail(ctx, TEE_EINVAL, "an enabled optional weight (ln_emb, ln_final, w_proj) is NULL");
     CK(cudaSetDevice(ctx->device));
     ctx->loaded = false;
     if (ctx->weight_arena) {
@@ -468,7 +537,7 @@ int tee_load_weights(tee_ctx* ctx, const tee_weights* w) {
     carve_weights(ctx, ctx->weight_arena);
 
     const size_t H = g.hidden, V = g.vocab;
-    size_t stage_elems = std::max(V * H, (size_t)2 * g.intermediate * H);
+    size_t stage_elems = std::max({V * H, (size_t)2 * g.intermediate * H, (size_t)g.proj_dim * H});
     float* stage = nullptr;
     if (g.dtype != TEE_F32) CK(cudaMalloc(&stage, stage_elems * sizeof(float)));
     cudaStream_t s = ctx->stream;
@@ -487,29 +556,29 @@ int tee_load_weights(tee_ctx* ctx, const tee_weights* w) {
     };
     const int lin_kind = g.dtype == TEE_F32 ? 0 : (g.dtype == TEE_BF16 ? 1 : 2);
     const int emb_kind = g.dtype == TEE_BF16 ? 1 : 0;
+    // LayerNorm gains are stored as fp32 in every variant; the bf16 variant
+    // keeps their bf16-rounded values.
+    auto put_gain = [&](float* dst, const float* src) -> int {
+        if (g.dtype != TEE_BF16) return put(dst, src, H, 0, 0, 0, nullptr);
+        std::vector<float> tmp(H);
+        for (size_t i = 0; i < H; ++i) {
+            uint32_t u;
+            memcpy(&u, &src[i], 4);
+            u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+            memcpy(&tmp[i], &u, 4);
+        }
+        return put(dst, tmp.data(), H, 0, 0, 0, nullptr);
+    };
     if ((rc = put(ctx->emb, w->tok_emb, V * H, emb_kind, 0, 0, nullptr))) goto done;
+    if (g.emb_norm && (rc = put_gain(ctx->ln_emb, w->ln_emb))) goto done;
+    if (g.final_norm && (rc = put_gain(ctx->ln_final, w->ln_final))) goto done;
+    if (g.proj_dim && (rc = put(ctx->w_proj, w->w_proj, (size_t)g.proj_dim * H, lin_kind, g.proj_dim, (int)H,
+                                ctx->w_proj_d)))
+        goto done;
     for (int l = 0; l < g.n_layers && rc == TEE_OK; ++l) {
         LayerWeights& L = ctx->layers[l];
-        const float* ln_a = w->ln_attn[l];
-        const float* ln_m = w->ln_mlp[l];
-        // LayerNorm gains are stored as fp32 in every variant; the bf16 variant
-        // keeps their bf16-rounded values.
-        if (g.dtype == TEE_BF16) {
-            std::vector<float> tmp(H);
-            for (int which = 0; which < 2 && rc == TEE_OK; ++which) {
-                const float* src = which ? ln_m : ln_a;
-                for (size_t i = 0; i < H; ++i) {
-                    uint32_t u;
-                    memcpy(&u, &src[i], 4);
-                    u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
-                    memcpy(&tmp[i], &u, 4);
-                }
-                rc = put(which ? L.ln_mlp : L.ln_attn, tmp.data(), H, 0, 0, 0, nullptr);
-            }
-        } else {
-            if ((rc = put(L.ln_attn, ln_a, H, 0, 0, 0, nullptr))) break;
-            if ((rc = put(L.ln_mlp, ln_m, H, 0, 0, 0, nullptr))) break;
-        }
+        if ((rc = put_gain(L.ln_attn, w->ln_attn[l]))) break;
+        if ((rc = put_gain(L.ln_mlp, w->ln_mlp[l]))) break;
         const float* srcs[4] = {w->wqkv[l], w->wo[l], w->wi[l], w->wo_ffn[l]};
         for (int which = 0; which < 4 && rc == TEE_OK; ++which) {
             int N, K;
@@ -566,6 +635,40 @@ int tee_encode_device(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, c
     return run_pass(ctx, d_ids, d_cu, h_cu, n_texts, T, d_out, (cudaStream_t)stream);
 }
 
+int tee_encode_tokens(tee_ctx* ctx, const int32_t* token_ids, const int32_t* cu_seqlens, int n_texts, float* out) {
+    int rc = check_ready(ctx);
+    if (rc) return rc;
+    if (!token_ids || !out) return fail(ctx, TEE_EINVAL, "token_ids / out is NULL");
+    int T = 0;
+    if ((rc = check_cu(ctx, cu_seqlens, n_texts, &T))) return rc;
+    for (int t = 0; t < T; ++t)
+        if (token_ids[t] < 0 || token_ids[t] >= ctx->cfg.vocab)
+            return fail(ctx, TEE_EINVAL, "token id %d at position %d is outside [0, %d)", token_ids[t], t,
+                        ctx->cfg.vocab);
+    CK(cudaSetDevice(ctx->device));
+    const size_t D = ctx->cfg.proj_dim ? ctx->cfg.proj_dim : ctx->cfg.hidden;
+    if (!ctx->tok_out) CK(cudaMalloc(&ctx->tok_out, (size_t)ctx->cfg.max_tokens * D * sizeof(float)));
+    cudaStream_t s = ctx->stream;
+    CK(cudaMemcpyAsync(ctx->d_ids, token_ids, (size_t)T * 4, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(ctx->d_cu, cu_seqlens, (size_t)(n_texts + 1) * 4, cudaMemcpyHostToDevice, s));
+    if ((rc = run_tokens(ctx, ctx->d_ids, ctx->d_cu, cu_seqlens, n_texts, T, ctx->tok_out, s))) return rc;
+    CK(cudaMemcpyAsync(out, ctx->tok_out, (size_t)T * D * 4, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    return TEE_OK;
+}
+
+int tee_encode_tokens_device(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu,
+                             int n_texts, float* d_out, void* stream) {
+    int rc = check_ready(ctx);
+    if (rc) return rc;
+    if (!d_ids || !d_cu || !d_out) return fail(ctx, TEE_EINVAL, "device pointer is NULL");
+    if (reinterpret_cast<uintptr_t>(d_out) & 15) return fail(ctx, TEE_EINVAL, "d_out must be 16-byte aligned");
+    int T = 0;
+    if ((rc = check_cu(ctx, h_cu, n_texts, &T))) return rc;
+    CK(cudaSetDevice(ctx->device));
+    return run_tokens(ctx, d_ids, d_cu, h_cu, n_texts, T, d_out, (cudaStream_t)stream);
+}
+
 const char* tee_last_error(const tee_ctx* ctx) { return ctx ? ctx->err.c_str() : g_create_error.c_str(); }
 
 void tee_destroy(tee_ctx* ctx) {
@@ -578,6 +681,7 @@ void tee_destroy(tee_ctx* ctx) {
     }
     if (ctx->weight_arena) cudaFree(ctx->weight_arena);
     if (ctx->ws_arena) cudaFree(ctx->ws_arena);
+    if (ctx->tok_out) cudaFree(ctx->tok_out);
     if (ctx->stream) cudaStreamDestroy(ctx->stream);
     delete ctx;
 }

@@ -40,6 +40,11 @@ struct tee_ctx {
     size_t weight_bytes = 0;
     void* emb = nullptr;                // fp32 [V*H] (F32, W8A8) or bf16 (BF16)
     std::vector<LayerWeights> layers;
+    float* ln_emb = nullptr;            // optional embedding-norm gain, fp32 [H]
+    float* ln_final = nullptr;          // optional final-norm gain, fp32 [H]
+    void* w_proj = nullptr;             // optional per-token projection [P*H] (stored like the projections)
+    float* w_proj_d = nullptr;          // its W8A8 block scales [P*H/32]
+    float* tok_out = nullptr;           // per-token output of tee_encode_tokens, float [max_tokens*D] (lazy)
 
     // RoPE tables, index 0 = global base, 1 = window base: float [max_tokens][head_dim/2]
     float* rope_cos[2] = {nullptr, nullptr};
@@ -107,6 +112,9 @@ cudaError_t launch_geglu(const void* u, void* z, bool bf16_act, int T, int I, cu
 #define POOL_CHUNK 64
 cudaError_t launch_pool_l2(const float* x, const int32_t* cu, const int32_t* chunk_off, int n_texts, int n_chunks,
                            int H, float* partial, float* out, cudaStream_t s);
+// Scale each row of x [M, D] (D a multiple of 4, <= 1024) to unit length in place
+// (norm floored at 1e-12).
+cudaError_t launch_l2_rows(float* x, int M, int D, cudaStream_t s);
 cudaError_t launch_attention_simple(const void* qkv, bool bf16_act, const int32_t* cu, int n_texts, int T, int H,
                                     int n_heads, bool is_global, int window, void* o, cudaStream_t s);
 
