@@ -47,6 +47,11 @@ def parse():
     ap.add_argument("--cpu-leg", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="sweep32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--output", default="pooled", choices=["pooled", "tokens"],
+                    help="pooled: one unit vector per text (the headline); tokens: one per token")
+    ap.add_argument("--proj-dim", type=int, default=128,
+                    help="with --output tokens: width of the per-token projection (0 = none)")
+    ap.add_argument("--norms", action="store_true", help="enable the embedding and final LayerNorms")
     return ap.parse_args()
 
 
@@ -77,9 +82,10 @@ def gemm_traffic():
     return GEMM_TRAFFIC_BYTES if h.hexdigest()[:16] == GEMM_TRAFFIC_DIGEST else None
 
 
-def gemm_flops_per_token(shape):
+def gemm_flops_per_token(shape, tokens_out=False):
     H, I = shape.hidden, shape.intermediate
-    return 2.0 * (3 * H * H + H * H + 2 * I * H + I * H) * shape.n_layers
+    proj = 2.0 * H * shape.proj_dim if tokens_out else 0.0
+    return 2.0 * (3 * H * H + H * H + 2 * I * H + I * H) * shape.n_layers + proj
 
 
 # ---------------------------------------------------------------------------
@@ -190,7 +196,9 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
-    shape = synth.RURI_310M
+    tokens_out = args.output == "tokens"
+    shape = synth.Shape(**{**synth.RURI_310M.as_dict(), "emb_norm": args.norms, "final_norm": args.norms,
+                           "proj_dim": args.proj_dim if tokens_out else 0})
 
     # workload: the 20 seeded batches of the chosen size; rank r takes batches r, r+N, ...
     budget, desc = WORKLOADS[args.workload]
@@ -208,15 +216,18 @@ def run_ours(args):
     enc.load_weights(weights)
     del weights
 
+    width = enc.token_width if tokens_out else shape.hidden   # columns of one output row
     d_batches = []
     for ids, cu in batches:
+        rows = len(ids) if tokens_out else len(cu) - 1
         d_batches.append((torch.from_numpy(ids).cuda(), torch.from_numpy(cu).cuda(), cu,
-                          torch.empty(len(cu) - 1, shape.hidden, device="cuda")))
+                          torch.empty(rows, width, device="cuda")))
     stream = torch.cuda.current_stream().cuda_stream
+    encode_device = enc.encode_tokens_device if tokens_out else enc.encode_device
 
     def step(i):
         d_ids, d_cu, h_cu, d_out = d_batches[i % len(d_batches)]
-        enc.encode_device(d_ids, d_cu, h_cu, d_out, stream)
+        encode_device(d_ids, d_cu, h_cu, d_out, stream)
 
     for i in range(args.warmup):
         step(i)
@@ -265,19 +276,20 @@ def run_ours(args):
     for ids, cu in batches:
         pi = torch.from_numpy(ids).pin_memory()
         pc = torch.from_numpy(cu).pin_memory()
-        po = torch.empty(len(cu) - 1, shape.hidden).pin_memory()
+        po = torch.empty(len(ids) if tokens_out else len(cu) - 1, width).pin_memory()
         pinned.append((pi, pc, po, len(cu) - 1))
     lib = enc.lib
+    encode_host = lib.tee_encode_tokens if tokens_out else lib.tee_encode
     for i in range(2):
         pi, pc, po, n = pinned[i % len(pinned)]
-        enc.check(lib.tee_encode(enc.ctx, pi.data_ptr(), pc.data_ptr(), n, po.data_ptr()))
+        enc.check(encode_host(enc.ctx, pi.data_ptr(), pc.data_ptr(), n, po.data_ptr()))
     if dist:
         dist.barrier()
     t0 = time.perf_counter()
     h2d = d2h = 0
     for i in range(args.steps):
         pi, pc, po, n = pinned[i % len(pinned)]
-        enc.check(lib.tee_encode(enc.ctx, pi.data_ptr(), pc.data_ptr(), n, po.data_ptr()))
+        enc.check(encode_host(enc.ctx, pi.data_ptr(), pc.data_ptr(), n, po.data_ptr()))
         h2d += pi.numel() * 4 + pc.numel() * 4
         d2h += po.numel() * 4
     e2e_s = time.perf_counter() - t0
@@ -294,7 +306,7 @@ def run_ours(args):
     achieved_tflops = gemm_flops_avg / (gemm_ms_avg / 1e3) / 1e12 if g["launches"] else None
     peak = pk["bf16_tflops_sustained"]
     launches = sum(v["launches"] for v in prof.values())
-    flops_per_token = gemm_flops_per_token(shape) + prof["attention"]["flops"] / (budget * args.steps)
+    flops_per_token = gemm_flops_per_token(shape, tokens_out) + prof["attention"]["flops"] / (budget * args.steps)
     kernel_share = {k: round(v["total_ms"] / max(1e-9, sum(x["total_ms"] for x in prof.values())), 4)
                     for k, v in prof.items() if v["launches"]}
 
@@ -315,6 +327,9 @@ def run_ours(args):
                    "global_batch": budget * world, "tokens_per_gpu_step": budget,
                    "texts_per_batch_mean": round(float(np.mean([len(cu) - 1 for _, cu in batches])), 1),
                    "batches": len(batches), "parallelism": f"dp{world} (texts sharded, no collective)",
+                   "output": (f"per-token unit vectors, projection {shape.proj_dim or 'none'}" if tokens_out
+                              else "one unit vector per text (mean pool + L2)"),
+                   "norms": "embedding + final LayerNorm" if args.norms else "none (the page's encoder)",
                    "l2": "inputs larger than L2 (weights 472 MB + activations per pass)"},
         "pct_tensor_peak": round(100.0 * value / world * flops_per_token / (pk["bf16_tflops"] * 1e12), 2),
         "clocks": clk,

@@ -9,8 +9,8 @@
 //   * tile 128 x BN per CTA, K step 64 (one 128-byte swizzle atom); a
 //     shared-memory ring of as many stages as fit, filled by TMA
 //     (cp.async.bulk.tensor, 128B swizzle, out-of-range rows zero-filled).
-//     BN = 256 for the bf16-output projections, 128 (short K) or 192 (long K)
-//     for the residual ones.
+//     BN = 256 for the bf16-output projections, 128 (short K) or 256 / 192
+//     (long K) for the residual ones.
 //   * CTA pairs (clusters of two) compute 256 x BN tiles with tcgen05
 //     cta_group::2 MMAs (M=256) issued by the even CTA: each CTA stages its
 //     128 rows of A and half of the weight tile, and holds its 128 accumulator
@@ -510,13 +510,15 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.W) | reinterpret_cast<uintptr_t>(a.C)) & 15)
         return cudaErrorMisalignedAddress;
     if (a.M == 0) return cudaSuccess;
-    // Residual add: short-K projections stage each warp's whole 32 x 128 fp32
-    // slice through TMA (128-column tiles, many tiles for N = 768); long-K ones
-    // use 192-column tiles (less operand traffic per FLOP) and stage the slice
-    // in two rounds.  Other epilogues use 256-column tiles where N allows.
-    const bool add_wide = a.epi == GEMM_EPI_ADD_F32 && a.K > 1024 && a.N % 192 == 0;
-    const int BN = add_wide ? 192
-                 : (a.epi == GEMM_EPI_ADD_F32 ? 128 : ((a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128));
+    // Residual add: short-K projections use 128-column tiles (many tiles for
+    // N = 768) and stage each warp's whole 32 x 128 fp32 slice through TMA;
+    // long-K ones use the widest tile N allows (256, else 192: less operand
+    // traffic per FLOP) and stage the slice in a ring of 32-column boxes.
+    // Other epilogues use 256-column tiles where N allows.
+    const bool add_long = a.epi == GEMM_EPI_ADD_F32 && a.K > 1024;
+    const int add_bn = !add_long ? 128 : (a.N % 256 == 0 ? 256 : (a.N % 192 == 0 ? 192 : 128));
+    const bool add_wide = add_bn > 128;
+    const int BN = a.epi == GEMM_EPI_ADD_F32 ? add_bn : ((a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128);
     const int num_m = (a.M + BM - 1) / BM;
     // CTA pairs compute 256-row tiles when there are at least two row tiles,
     // except for the short-K residual projection, whose fp32 residual traffic
@@ -538,7 +540,8 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
 #define TEE_GEMM_DISPATCH(BN_, EPI_)                                                                  \
     return mode == MODE_PAIR ? launch_t<BN_, EPI_, MODE_PAIR>(ma, mb, mc_map, p, units, s)           \
                              : launch_t<BN_, EPI_, MODE_SINGLE>(ma, mb, mc_map, p, units, s)
-    if (add_wide) TEE_GEMM_DISPATCH(192, GEMM_EPI_ADD_F32);
+    if (add_bn == 256) TEE_GEMM_DISPATCH(256, GEMM_EPI_ADD_F32);
+    if (add_bn == 192) TEE_GEMM_DISPATCH(192, GEMM_EPI_ADD_F32);
     if (BN == 256) {
         switch (a.epi) {
             case GEMM_EPI_STORE_BF16: TEE_GEMM_DISPATCH(256, GEMM_EPI_STORE_BF16);
