@@ -45,16 +45,14 @@ using namespace tc;
 constexpr int BQ = 128;
 constexpr int BKV = 128;
 constexpr int HD = 64;
-constexpr int KV_STAGES = 3;
+constexpr int KV_STAGES = 5;
 constexpr int NUM_THREADS = 320;
 constexpr int SM_THREADS = 256;   // softmax warps 2..9
 constexpr uint32_t TILE_BYTES = BQ * HD * 2;        // Q, K or V tile: 16 KB
-constexpr uint32_t P_BYTES = BQ * BKV * 2;          // 32 KB
 constexpr uint32_t OFF_Q = 0;                       // 2 Q buffers
 constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + KV_STAGES * TILE_BYTES;
-constexpr uint32_t OFF_P = OFF_V + KV_STAGES * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + KV_STAGES * TILE_BYTES;
 // barrier indices
 constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = B_KVF + KV_STAGES, B_SF = B_KVE + KV_STAGES, B_SE = B_SF + 2,
               B_PF = B_SE + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_DONE = B_OE + 2, N_BARS = B_DONE + 1;
@@ -62,7 +60,7 @@ constexpr uint32_t OFF_RED = OFF_BAR + N_BARS * 8 + 16;       // row-maximum exc
 constexpr uint32_t OFF_REDL = OFF_RED + 2 * 2 * 128 * 4;       // row-sum exchange: [2 halves][128 rows]
 constexpr uint32_t SMEM_TOTAL = OFF_REDL + 2 * 128 * 4 + 1024;
 constexpr uint32_t TMEM_COLS = 512;                 // S: 2 x 128 columns (by tile), O: 2 x 64 (by unit)
-constexpr uint32_t TM_S = 0, TM_O = 256;
+constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;   // P: 2 x 64 columns (bf16 pairs), by tile
 
 struct AttnParams {
     const int4* items;      // {q_start, q_len, k_lo, k_hi} per (text, query tile)
@@ -175,13 +173,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait(bar(B_PF + pb), (tt >> 1) & 1, abort_flag)) return false;
                 if (first && !mbar_wait(bar(B_OE + ub), (uuse & 1) ^ 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t pbase = sbase + OFF_P + pb * P_BYTES;
+                const uint32_t pbase = tmem_base + TM_P + pb * (BKV / 2);
                 const uint32_t vbase = sbase + OFF_V + st * TILE_BYTES;
 #pragma unroll
                 for (int s = 0; s < BKV / 16; ++s) {
-                    const uint64_t adesc = sw128_desc(pbase + (s >> 2) * (P_BYTES / 2)) + 2 * (s & 3);
                     const uint64_t vdesc = sw128_desc_mn(vbase + s * 2048);
-                    mma_bf16(tmem_base + TM_O + ub * HD, adesc, vdesc, idesc_pv, !(first && s == 0));
+                    mma_bf16_ts(tmem_base + TM_O + ub * HD, pbase + 8 * s, vdesc, idesc_pv, !(first && s == 0));
                 }
                 mma_commit(bar(B_OF + pb));
                 mma_commit(bar(B_KVE + st));
@@ -244,7 +241,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int half = (warp - 2) >> 2;               // key columns [64*half, +64), O columns [32*half, +32)
         const int r = quad * 32 + lane;                 // query row of the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        uint8_t* prow0 = smem + OFF_P + half * (P_BYTES / 2) + r * 128;
         float* red = reinterpret_cast<float*>(smem + OFF_RED);   // [2][2][128]
         float* red_l = reinterpret_cast<float*>(smem + OFF_REDL);   // [2][128]
         const uint32_t pair_bar = 1 + quad;             // named barrier of warps (w, w + 4)
@@ -367,17 +363,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     s8[i & 7] += v[i];
                 }
                 const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
-                uint8_t* prow = prow0 + sb * P_BYTES;
+                // P as bf16 pairs into this tile's TMEM P buffer (the A operand
+                // of P V): this half's 64 keys are columns [32 * half, +32)
+                uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 q;
-                    q.x = pack_bf16(v[8 * c + 0], v[8 * c + 1]);
-                    q.y = pack_bf16(v[8 * c + 2], v[8 * c + 3]);
-                    q.z = pack_bf16(v[8 * c + 4], v[8 * c + 5]);
-                    q.w = pack_bf16(v[8 * c + 6], v[8 * c + 7]);
-                    *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = q;
-                }
-                fence_proxy_async_smem();
+                for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(v[2 * c], v[2 * c + 1]);
+                tmem_st32_u(tmem_base + lane_off + TM_P + sb * (BKV / 2) + half * 32, pk);
+                tc_fence_before();
                 mbar_arrive(bar(B_PF + sb));
                 l += sum;
             }
