@@ -218,22 +218,137 @@ __global__ void pool_partial_kernel(const float* __restrict__ x, const int32_t* 
     }
 }
 
-// Pass 2: one block per text sums its chunks' partials in chunk order (so the
-// result is deterministic), divides by the length and scales to unit norm
-// (norm floored at 1e-12).  H <= 4 * blockDim.x.
+// Single-launch mean-pool + L2: every block sums one chunk of up to
+// POOL_CHUNK_FUSED rows of one text (as pass 1 does for its chunks), then
+// bumps its text's arrival counter; the text's last block to arrive sums the
+// text's chunk partials in chunk order (eight at a time into eight fixed-order
+// accumulators, so the result is deterministic), scales by 1 / length and to
+// unit norm (floored at 1e-12), writes the vector and resets the counter to 0
+// for the next launch.  blockDim.x == H / 4 (H <= 1024).
+__global__ void pool_fused_kernel(const float* __restrict__ x, const int32_t* __restrict__ cu,
+                                  const int32_t* __restrict__ chunk_off, int n_texts, int H, float* partial,
+                                  unsigned int* counters, float* __restrict__ out) {
+    __shared__ float red[32];
+    __shared__ int is_last;
+    const int chunk = blockIdx.x;
+    const int j = text_of(chunk_off, n_texts, chunk);
+    const int c4 = threadIdx.x;
+    const int r0 = cu[j] + (chunk - chunk_off[j]) * POOL_CHUNK_FUSED;
+    const int r1 = min(cu[j + 1], r0 + POOL_CHUNK_FUSED);
+    {
+        float4 acc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        int r = r0;
+        for (; r + 8 <= r1; r += 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float4 v = reinterpret_cast<const float4*>(x + (size_t)(r + u) * H)[c4];
+                acc[u].x += v.x;
+                acc[u].y += v.y;
+                acc[u].z += v.z;
+                acc[u].w += v.w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {   // the last < 8 rows (static register indices)
+            if (r + u < r1) {
+                const float4 v = reinterpret_cast<const float4*>(x + (size_t)(r + u) * H)[c4];
+                acc[u].x += v.x;
+                acc[u].y += v.y;
+                acc[u].z += v.z;
+                acc[u].w += v.w;
+            }
+        }
+        float4 tot = acc[0];
+#pragma unroll
+        for (int u = 1; u < 8; ++u) {
+            tot.x += acc[u].x;
+            tot.y += acc[u].y;
+            tot.z += acc[u].z;
+            tot.w += acc[u].w;
+        }
+        reinterpret_cast<float4*>(partial + (size_t)chunk * H)[c4] = tot;
+    }
+    // publish the partial, then count this chunk in
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned int n = (unsigned int)(chunk_off[j + 1] - chunk_off[j]);
+        is_last = atomicAdd(&counters[j], 1u) == n - 1;
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    const int k0 = chunk_off[j], k1 = chunk_off[j + 1];
+    float4 a8[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) a8[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    int k = k0;
+    for (; k + 8 <= k1; k += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(partial + (size_t)(k + u) * H) + c4);
+            a8[u].x += v.x;
+            a8[u].y += v.y;
+            a8[u].z += v.z;
+            a8[u].w += v.w;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        if (k + u < k1) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(partial + (size_t)(k + u) * H) + c4);
+            a8[u].x += v.x;
+            a8[u].y += v.y;
+            a8[u].z += v.z;
+            a8[u].w += v.w;
+        }
+    }
+    const float inv_len = 1.0f / (float)(cu[j + 1] - cu[j]);
+    float4 m;
+    m.x = (((a8[0].x + a8[1].x) + (a8[2].x + a8[3].x)) + ((a8[4].x + a8[5].x) + (a8[6].x + a8[7].x))) * inv_len;
+    m.y = (((a8[0].y + a8[1].y) + (a8[2].y + a8[3].y)) + ((a8[4].y + a8[5].y) + (a8[6].y + a8[7].y))) * inv_len;
+    m.z = (((a8[0].z + a8[1].z) + (a8[2].z + a8[3].z)) + ((a8[4].z + a8[5].z) + (a8[6].z + a8[7].z))) * inv_len;
+    m.w = (((a8[0].w + a8[1].w) + (a8[2].w + a8[3].w)) + ((a8[4].w + a8[5].w) + (a8[6].w + a8[7].w))) * inv_len;
+    float ss = warp_sum((m.x * m.x + m.y * m.y) + (m.z * m.z + m.w * m.w));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < ((blockDim.x + 31) >> 5) ? red[threadIdx.x] : 0.f;
+        v = warp_sum(v);
+        if (threadIdx.x == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float scale = 1.0f / fmaxf(sqrtf(red[0]), 1e-12f);
+    reinterpret_cast<float4*>(out + (size_t)j * H)[c4] = make_float4(m.x * scale, m.y * scale, m.z * scale, m.w * scale);
+    if (threadIdx.x == 0) counters[j] = 0u;
+}
+
+// Pass 2: one block per text sums its chunks' partials (eight chunks at a time
+// into eight accumulators, combined in a fixed order, so the result is
+// deterministic and eight loads per column are in flight), divides by the
+// length and scales to unit norm (norm floored at 1e-12).  H <= 4 * blockDim.x.
 __global__ void pool_finish_kernel(const float* __restrict__ partial, const int32_t* __restrict__ cu,
                                    const int32_t* __restrict__ chunk_off, int H, float* __restrict__ out) {
     __shared__ float red[32];
     const int j = blockIdx.x;
     const int k0 = chunk_off[j], k1 = chunk_off[j + 1];
     const float inv_len = 1.0f / (float)(cu[j + 1] - cu[j]);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k = k0; k < k1; ++k) {
+    float acc[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int c = threadIdx.x + i * blockDim.x;
-            if (c < H) acc[i] += partial[(size_t)k * H + c];
+    for (int i = 0; i < 4; ++i) {
+        const int c = threadIdx.x + i * blockDim.x;
+        float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (c < H) {
+            int k = k0;
+            for (; k + 8 <= k1; k += 8) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) a8[u] += partial[(size_t)(k + u) * H + c];
+            }
+            for (int u = 0; k < k1; ++k, ++u) a8[u] += partial[(size_t)k * H + c];
         }
+        acc[i] = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
     }
     float ss = 0.f;
 #pragma unroll
@@ -389,6 +504,15 @@ cudaError_t launch_l2_rows(float* x, int M, int D, cudaStream_t s) {
     if (M == 0) return cudaSuccess;
     if (D % 4 || D > 1024) return cudaErrorInvalidValue;
     l2_rows_kernel<<<(M + 7) / 8, 256, 0, s>>>(x, M, D);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pool_l2_fused(const float* x, const int32_t* cu, const int32_t* chunk_off, int n_texts,
+                                 int n_chunks, int H, float* partial, unsigned int* counters, float* out,
+                                 cudaStream_t s) {
+    if (n_texts == 0) return cudaSuccess;
+    if (H % 4 || H > 1024) return cudaErrorInvalidValue;
+    pool_fused_kernel<<<n_chunks, H / 4, 0, s>>>(x, cu, chunk_off, n_texts, H, partial, counters, out);
     return cudaGetLastError();
 }
 

@@ -120,9 +120,10 @@ size_t carve_workspace(tee_ctx* c, void* base) {
     c->d_status = cv.take<unsigned int>(4);
     c->max_items = (int)(T / 128 + g.max_texts + 1);
     for (int b = 0; b < 2; ++b) c->d_items[b] = cv.take<int4>(c->max_items);
-    c->max_chunks = (int)(T / POOL_CHUNK + g.max_texts + 1);
+    c->max_chunks = (int)(T / POOL_CHUNK_FUSED + g.max_texts + 1);
     c->d_chunk_off = cv.take<int32_t>(g.max_texts + 1);
     c->pool_partial = cv.take<float>((size_t)c->max_chunks * H);
+    c->pool_counters = cv.take<unsigned int>(g.max_texts);
     return cv.off;
 }
 
@@ -363,13 +364,13 @@ int step_ffn_in(tee_ctx* ctx, int layer, const void* y, void* z, int T, cudaStre
     return TEE_OK;
 }
 
-// Chunk offsets of the two-pass pool: text j owns ceil(len_j / POOL_CHUNK) chunks.
+// Chunk offsets of the pool: text j owns ceil(len_j / POOL_CHUNK_FUSED) chunks.
 int prepare_pool_chunks(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cudaStream_t s) {
     ctx->h_chunk_off.resize(n_texts + 1);
     int total = 0;
     for (int j = 0; j < n_texts; ++j) {
         ctx->h_chunk_off[j] = total;
-        total += (h_cu[j + 1] - h_cu[j] + POOL_CHUNK - 1) / POOL_CHUNK;
+        total += (h_cu[j + 1] - h_cu[j] + POOL_CHUNK_FUSED - 1) / POOL_CHUNK_FUSED;
     }
     ctx->h_chunk_off[n_texts] = total;
     if (total > ctx->max_chunks) return fail(ctx, TEE_ETOOLONG, "too many pooling chunks");
@@ -385,7 +386,8 @@ int step_pool(tee_ctx* ctx, const float* x, const int32_t* d_cu, const int32_t* 
     if (rc) return rc;
     const int n_chunks = ctx->h_chunk_off[n_texts];
     LAUNCH(TEE_K_POOL, 0, (double)T * g.hidden * 4 + (double)n_texts * g.hidden * 4,
-           launch_pool_l2(x, d_cu, ctx->d_chunk_off, n_texts, n_chunks, g.hidden, ctx->pool_partial, out, s));
+           launch_pool_l2_fused(x, d_cu, ctx->d_chunk_off, n_texts, n_chunks, g.hidden, ctx->pool_partial,
+                                ctx->pool_counters, out, s));
     return TEE_OK;
 }
 
@@ -508,6 +510,8 @@ int tee_create(const tee_config* cfg, int device, tee_ctx** out) {
     carve_workspace(ctx, ctx->ws_arena);
     e = cudaMemset(ctx->d_status, 0, 4 * sizeof(unsigned int));
     if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaMemset(status)"));
+    e = cudaMemset(ctx->pool_counters, 0, (size_t)cfg->max_texts * sizeof(unsigned int));
+    if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaMemset(pool counters)"));
     if ((rc = build_rope_tables(ctx))) return bail(rc);
     e = cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking);
     if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaStreamCreate"));

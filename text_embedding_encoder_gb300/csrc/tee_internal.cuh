@@ -69,6 +69,7 @@ struct tee_ctx {
     int4* d_items[2] = {nullptr, nullptr};   // attention work items (global, window layers)
     int32_t* d_chunk_off = nullptr;     // pool: first chunk of each text [max_texts + 1]
     float* pool_partial = nullptr;      // pool: partial sums [max_chunks * H]
+    unsigned int* pool_counters = nullptr;   // pool: chunks finished per text [max_texts], zero between launches
     int max_chunks = 0;
     std::vector<int32_t> h_chunk_off;
     int max_items = 0;
@@ -110,8 +111,14 @@ cudaError_t launch_geglu(const void* u, void* z, bool bf16_act, int T, int I, cu
 // (chunk_off[j] = first chunk of text j, device int32[n+1]) into `partial`
 // (float [n_chunks * H]), then per text the ordered sum, mean and scaling.
 #define POOL_CHUNK 64
+#define POOL_CHUNK_FUSED 64   // rows per block of the single-launch pool (launch_pool_l2_fused)
 cudaError_t launch_pool_l2(const float* x, const int32_t* cu, const int32_t* chunk_off, int n_texts, int n_chunks,
                            int H, float* partial, float* out, cudaStream_t s);
+// The same in one launch: the last chunk of each text to finish combines that
+// text's partials; counters (unsigned [n_texts], all zero) are left zero.
+cudaError_t launch_pool_l2_fused(const float* x, const int32_t* cu, const int32_t* chunk_off, int n_texts,
+                                 int n_chunks, int H, float* partial, unsigned int* counters, float* out,
+                                 cudaStream_t s);
 // Scale each row of x [M, D] (D a multiple of 4, <= 1024) to unit length in place
 // (norm floored at 1e-12).
 cudaError_t launch_l2_rows(float* x, int M, int D, cudaStream_t s);
