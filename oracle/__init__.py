@@ -52,6 +52,7 @@ from .precision import round_to_bf16  # noqa: F401
 from .w8a8 import (  # noqa: F401
     quantize_rows7,
     quantize_weight_blocks,
+    quantize_weight_blocks4,
     int_block_partials,
     w8a8_linear,
 )

@@ -155,6 +155,7 @@ class OracleModel:
                     projections) rounded to bfloat16 first, then widened.
     variant "w8a8": projections go through the integer procedure of
                     ``oracle.w8a8``; embedding and gains stay fp32.
+    variant "w4a8": the same with 4-bit weight blocks (codes in [-7, 7]).
 
     ``weights`` needs attributes tok_emb, ln_attn, wqkv, wo, ln_mlp, wi,
     wo_ffn (lists per layer), in the layouts documented by the C header, and
@@ -164,7 +165,7 @@ class OracleModel:
     """
 
     def __init__(self, weights, shape, variant: str = "fp32"):
-        if variant not in ("fp32", "bf16", "w8a8"):
+        if variant not in ("fp32", "bf16", "w8a8", "w4a8"):
             raise ValueError(variant)
         self.shape = shape
         self.variant = variant
@@ -177,18 +178,18 @@ class OracleModel:
         self.ln_final = wide(weights.ln_final) if getattr(shape, "final_norm", False) else None
         names = ("wqkv", "wo", "wi", "wo_ffn")
         proj = [weights.w_proj] if getattr(shape, "proj_dim", 0) else []
-        if variant == "w8a8":
-            from .w8a8 import quantize_weight_blocks
-            self.q = {name: [quantize_weight_blocks(np.asarray(w, np.float32)) for w in getattr(weights, name)]
-                      for name in names}
-            self.q["w_proj"] = [quantize_weight_blocks(np.asarray(w, np.float32)) for w in proj]
+        if variant in ("w8a8", "w4a8"):
+            from .w8a8 import quantize_weight_blocks, quantize_weight_blocks4
+            quant = quantize_weight_blocks if variant == "w8a8" else quantize_weight_blocks4
+            self.q = {name: [quant(np.asarray(w, np.float32)) for w in getattr(weights, name)] for name in names}
+            self.q["w_proj"] = [quant(np.asarray(w, np.float32)) for w in proj]
         else:
             self.lin = {name: [wide(w) for w in getattr(weights, name)] for name in names}
             self.lin["w_proj"] = [wide(w) for w in proj]
 
     def linear(self, name: str, layer: int, x) -> np.ndarray:
         """y = x W^T (no bias: the page mentions none on any projection)."""
-        if self.variant == "w8a8":
+        if self.variant in ("w8a8", "w4a8"):
             from .w8a8 import w8a8_linear
             qw, d = self.q[name][layer]
             return w8a8_linear(x, qw, d)

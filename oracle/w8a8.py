@@ -12,6 +12,12 @@ Readings (the page fixes no formulas):
 * product: per block b the exact integer sum I[m, n, b] = sum_k qa * qw, then
   y[m, n] = s_m * sum_b d[n, b] * I[m, n, b].
 
+The -q4 path of the same section repacks the file's 4- and 6-bit block formats
+unchanged; the page names those formats but does not define them.  Reading: a
+4-bit analogue of the 8-bit blocks defined here -- blocks of 32 K elements,
+d = max|w| / 7, q = clamp(rint(w / d), -7, 7) -- with the same 7-bit
+activations and the same exact block sums (variant "w4a8").
+
 The quantisers decide integers from floating point, so they compute in fp32
 (IEEE division, round-half-even), the precision of the device kernels; the
 integer sums are exact (int64); the final combination is fp64.
@@ -20,6 +26,7 @@ import numpy as np
 
 ACT_LEVELS = 63
 WEIGHT_LEVELS = 127
+WEIGHT_LEVELS_4 = 7
 BLOCK = 32
 
 
@@ -38,8 +45,9 @@ def quantize_rows7(x):
     return q.astype(np.int8), s
 
 
-def quantize_weight_blocks(w):
-    """Blockwise int8 quantisation of a weight matrix [N, K], K a multiple of 32.
+def quantize_weight_blocks(w, levels: int = WEIGHT_LEVELS):
+    """Blockwise quantisation of a weight matrix [N, K], K a multiple of 32,
+    to integers in [-levels, levels] (127: int8 blocks; 7: 4-bit blocks).
 
     Returns (q int8[N, K], d float32[N, K/32]).
     """
@@ -48,12 +56,17 @@ def quantize_weight_blocks(w):
     if K % BLOCK:
         raise ValueError("K must be a multiple of 32")
     blocks = w.reshape(N, K // BLOCK, BLOCK)
-    d = (np.abs(blocks).max(axis=2) / np.float32(WEIGHT_LEVELS)).astype(np.float32)
+    d = (np.abs(blocks).max(axis=2) / np.float32(levels)).astype(np.float32)
     safe = np.where(d > 0, d, np.float32(1.0)).astype(np.float32)
     q = np.rint(blocks / safe[:, :, None]).astype(np.float32)
-    q = np.clip(q, -WEIGHT_LEVELS, WEIGHT_LEVELS)
+    q = np.clip(q, -levels, levels)
     q = np.where(d[:, :, None] > 0, q, np.float32(0.0))
     return q.reshape(N, K).astype(np.int8), d
+
+
+def quantize_weight_blocks4(w):
+    """4-bit blocks (the -q4 reading): codes in [-7, 7], d = max|w| / 7 per block of 32."""
+    return quantize_weight_blocks(w, WEIGHT_LEVELS_4)
 
 
 def _block_product(qa, qw, b) -> np.ndarray:

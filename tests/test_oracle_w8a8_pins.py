@@ -55,6 +55,35 @@ def test_quantize_weight_blocks_hand_cases():
     assert q[1, 40] == -127 and d[1, 1] == np.float32(3.0) / np.float32(127.0)
 
 
+def test_quantize_weight_blocks4_hand_cases():
+    # 4-bit blocks: d = max|w| / 7, codes rint(w / d) clamped to +-7, ties to even
+    w = np.zeros((2, 64), np.float32)
+    w[0, :32] = np.linspace(-7, 7, 32)
+    w[0, 32] = 0.5        # 0.5 / 1 -> 0 (tie to even)
+    w[0, 33] = 2.5        # -> 2
+    w[0, 34] = 3.5        # -> 4
+    w[0, 35] = 7.0        # the block maximum: d = 1
+    w[1, 40] = -3.0       # alone in its block: d = 3/7, code -7
+    q, d = oracle.quantize_weight_blocks4(w)
+    assert d[0, 0] == 1.0 and d[0, 1] == 1.0
+    np.testing.assert_array_equal(q[0, :32], np.rint(np.linspace(-7, 7, 32)).astype(np.int8))
+    assert q[0, 32] == 0 and q[0, 33] == 2 and q[0, 34] == 4 and q[0, 35] == 7
+    assert d[1, 0] == 0.0 and not q[1, :32].any()
+    assert q[1, 40] == -7 and d[1, 1] == np.float32(3.0) / np.float32(7.0)
+
+
+def test_quantize_weight_blocks4_range_and_error():
+    rng = np.random.default_rng(5)
+    w = (rng.standard_normal((16, 128)) * rng.uniform(0.01, 3, (16, 1))).astype(np.float32)
+    q, d = oracle.quantize_weight_blocks4(w)
+    assert q.min() >= -7 and q.max() <= 7
+    # every block reaches +-7 at its maximum, and the rounding error is at most d / 2
+    blocks = np.abs(q.reshape(16, 4, 32)).max(axis=2)
+    np.testing.assert_array_equal(blocks, 7)
+    err = np.abs(w.reshape(16, 4, 32) - q.reshape(16, 4, 32) * d[:, :, None])
+    assert np.all(err <= d[:, :, None] / 2 * (1 + 1e-6))
+
+
 def test_int_block_partials_against_integer_loops():
     rng = np.random.default_rng(1)
     M, N, K = 5, 4, 96
@@ -93,6 +122,24 @@ def test_w8a8_linear_within_rounding_bound():
     assert np.all(np.abs(y - exact) <= bound * (1 + 1e-9) + 1e-12)
     # and it is not trivially exact
     assert np.abs(y - exact).max() > 0
+
+
+def test_w4a8_model_uses_four_bit_codes():
+    from text_embedding_encoder_gb300 import synth
+    shape = synth.Shape(n_layers=2, hidden=64, n_heads=1, head_dim=64, intermediate=96, vocab=50)
+    w = synth.make_weights(shape, seed=3)
+    m = oracle.OracleModel(w, shape, "w4a8")
+    for name in ("wqkv", "wo", "wi", "wo_ffn"):
+        q, d = m.q[name][1]
+        assert np.abs(q).max() == 7
+        np.testing.assert_array_equal(q, w8a8.quantize_weight_blocks4(getattr(w, name)[1])[0])
+    ids, cu = synth.make_batch([9, 4], shape.vocab, seed=4)
+    e4 = oracle.encode_packed(ids, cu, m)
+    e8 = oracle.encode_packed(ids, cu, oracle.OracleModel(w, shape, "w8a8"))
+    ef = oracle.encode_packed(ids, cu, oracle.OracleModel(w, shape, "fp32"))
+    np.testing.assert_allclose(np.linalg.norm(e4, axis=1), 1.0, atol=1e-14)
+    # coarser weights: further from the float result than the 8-bit blocks
+    assert np.all((e4 * ef).sum(axis=1) < (e8 * ef).sum(axis=1))
 
 
 def test_w8a8_model_uses_integer_path():
