@@ -8,7 +8,7 @@
  * runs exactly these steps in this order.
  *
  * Activation buffers use the context's activation type ACT:
- *   TEE_F32 and TEE_W8A8 contexts: float;  TEE_BF16 contexts: bfloat16
+ *   TEE_F32, TEE_W8A8 and TEE_W4A8 contexts: float;  TEE_BF16 contexts: bfloat16
  *   (uint16 bit patterns).  The residual stream x is always float.
  * Shapes: T = rows (tokens), H = hidden, I = intermediate, row-major.
  * Return codes as in tee.h.  Buffers are borrowed for the duration of the
@@ -116,7 +116,7 @@ int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const in
 int tee_pool_l2_noalloc(const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int hidden,
                         float* d_out, void* stream);
 
-/* ---- W8A8 pieces (TEE_W8A8 contexts) ----------------------------------- */
+/* ---- integer-path pieces (TEE_W8A8 and TEE_W4A8 contexts) --------------- */
 
 /* Per-row 7-bit quantiser: s[m] = max|x[m,:]| / 63 (IEEE fp32 division),
  * q = clamp(rint(x / s), -63, 63) (ties to even); zero rows give s = 0, q = 0.
@@ -129,8 +129,9 @@ int tee_op_quant_rows7(tee_ctx* ctx, const float* d_x, int M, int K, int8_t* d_q
 int tee_op_w8a8_partials(tee_ctx* ctx, int layer, int which, const int8_t* d_q, int M, int32_t* d_partials,
                          void* stream);
 
-/* Copy the device-resident int8 codes int8[N*K] and block scales float[N*K/32]
- * of projection `which` of `layer` to host buffers.  Synchronous. */
+/* Copy the weight codes of projection `which` of `layer`, widened to int8[N*K]
+ * (the 4-bit codes of a TEE_W4A8 context unpacked), and the block scales
+ * float[N*K/32] to host buffers.  Synchronous. */
 int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d);
 
 /* Failure-detection self-test.  Launches one thread that waits, with the same

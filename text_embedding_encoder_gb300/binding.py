@@ -22,8 +22,8 @@ TEE_ECUDA = -4
 TEE_ETOOLONG = -5
 TEE_ETIMEOUT = -6
 
-TEE_F32, TEE_BF16, TEE_W8A8 = 0, 1, 2
-DTYPES = {"fp32": TEE_F32, "bf16": TEE_BF16, "w8a8": TEE_W8A8}
+TEE_F32, TEE_BF16, TEE_W8A8, TEE_W4A8 = 0, 1, 2, 3
+DTYPES = {"fp32": TEE_F32, "bf16": TEE_BF16, "w8a8": TEE_W8A8, "w4a8": TEE_W4A8}
 
 TEE_LN_ATTN, TEE_LN_MLP = 0, 1
 TEE_W_QKV, TEE_W_OUT, TEE_W_FFN_IN, TEE_W_FFN_OUT = 0, 1, 2, 3

@@ -158,9 +158,13 @@ __global__ void __launch_bounds__(256) attention_simple_kernel(const TA* __restr
 // W8A8
 // ---------------------------------------------------------------------------
 
-// One thread per (row n, 32-block b): d = max|w| / 127, q = clamp(rint(w / d), +-127).
+// One thread per (row n, 32-block b): d = max|w| / L, q = clamp(rint(w / d), +-L)
+// with L = 127 (int8 codes, one byte each) or, with W4, L = 7 (4-bit two's
+// complement codes, two per byte: element 2i in the low nibble of byte i).
+template <bool W4>
 __global__ void quant_weight_blocks_kernel(const float* __restrict__ w, int8_t* __restrict__ q,
                                            float* __restrict__ d, int N, int K) {
+    constexpr float L = W4 ? 7.0f : 127.0f;
     const int nb = K / 32;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (size_t)N * nb) return;
@@ -168,14 +172,37 @@ __global__ void quant_weight_blocks_kernel(const float* __restrict__ w, int8_t* 
     const float* src = w + n * K + b * 32;
     float amax = 0.f;
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(src[i]));
-    const float dd = __fdiv_rn(amax, 127.0f);
+    const float dd = __fdiv_rn(amax, L);
     d[idx] = dd;
-    int8_t* dst = q + n * K + b * 32;
+    int code[32];
+#pragma unroll
     for (int i = 0; i < 32; ++i) {
         float v = 0.f;
-        if (dd > 0.f) v = fminf(fmaxf(rintf(__fdiv_rn(src[i], dd)), -127.f), 127.f);
-        dst[i] = (int8_t)(int)v;
+        if (dd > 0.f) v = fminf(fmaxf(rintf(__fdiv_rn(src[i], dd)), -L), L);
+        code[i] = (int)v;
     }
+    if constexpr (W4) {
+        uint8_t* dst = reinterpret_cast<uint8_t*>(q) + (n * K + b * 32) / 2;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = (uint8_t)((code[2 * i] & 15) | ((code[2 * i + 1] & 15) << 4));
+    } else {
+        int8_t* dst = q + n * K + b * 32;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dst[i] = (int8_t)code[i];
+    }
+}
+
+// Four 4-bit codes (two bytes of packed nibbles, element k in bits 4k..4k+3)
+// widened to the four int8 lanes of one dp4a operand.
+__device__ __forceinline__ int unpack4x4(uint32_t two_bytes) {
+    uint32_t out = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int v = (int)((two_bytes >> (4 * i)) & 15u);
+        const int sv = (v ^ 8) - 8;   // sign-extend the 4-bit two's complement code
+        out |= ((uint32_t)sv & 255u) << (8 * i);
+    }
+    return (int)out;
 }
 
 // One warp per row: s = max|x| / 63, q = clamp(rint(x / s), +-63).
@@ -200,7 +227,7 @@ __global__ void quant_rows7_kernel(const float* __restrict__ x, int M, int K, in
 
 // C[M, N] (+)= s_m * sum_b d[n, b] * I[m, n, b], with I the exact int32 sum of
 // the 32 products of block b (dp4a).  64x64 tile, 4x4 outputs per thread.
-template <int EPI, bool PARTIALS>
+template <int EPI, bool PARTIALS, bool W4>
 __global__ void __launch_bounds__(256) gemm_w8a8_kernel(const int8_t* __restrict__ qa, const float* __restrict__ sa,
                                                         const int8_t* __restrict__ qw, const float* __restrict__ dw,
                                                         float* __restrict__ C, int32_t* __restrict__ partials, int M,
@@ -221,7 +248,11 @@ __global__ void __launch_bounds__(256) gemm_w8a8_kernel(const int8_t* __restrict
             int r = i >> 3, c = i & 7;
             int gm = m0 + r, gn = n0 + r;
             As[c][r] = gm < M ? reinterpret_cast<const int*>(qa + (size_t)gm * K + b * 32)[c] : 0;
-            Ws[c][r] = gn < N ? reinterpret_cast<const int*>(qw + (size_t)gn * K + b * 32)[c] : 0;
+            if constexpr (W4)   // 16 bytes of packed codes per block row: bytes 2c, 2c + 1 hold elements 4c..4c+3
+                Ws[c][r] = gn < N ? unpack4x4(reinterpret_cast<const uint16_t*>(qw + ((size_t)gn * K + b * 32) / 2)[c])
+                                  : 0;
+            else
+                Ws[c][r] = gn < N ? reinterpret_cast<const int*>(qw + (size_t)gn * K + b * 32)[c] : 0;
         }
         __syncthreads();
         int iacc[4][4];
@@ -303,10 +334,11 @@ cudaError_t launch_attention_simple(const void* qkv, bool bf16_act, const int32_
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_weight_blocks(const float* w, int8_t* q, float* d, int N, int K, cudaStream_t s) {
+cudaError_t launch_quant_weight_blocks(const float* w, int8_t* q, float* d, int N, int K, bool w4, cudaStream_t s) {
     size_t n = (size_t)N * (K / 32);
     if (n == 0) return cudaSuccess;
-    quant_weight_blocks_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(w, q, d, N, K);
+    if (w4) quant_weight_blocks_kernel<true><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(w, q, d, N, K);
+    else quant_weight_blocks_kernel<false><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(w, q, d, N, K);
     return cudaGetLastError();
 }
 
@@ -316,16 +348,19 @@ cudaError_t launch_quant_rows7(const float* x, int M, int K, int8_t* q, float* s
     return cudaGetLastError();
 }
 
+template <bool W4>
+void launch_w8a8_t(dim3 grid, const int8_t* qa, const float* sa, const int8_t* qw, const float* dw, float* C,
+                   int32_t* partials, int M, int N, int K, int epi, cudaStream_t s) {
+    if (partials) gemm_w8a8_kernel<0, true, W4><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, partials, M, N, K);
+    else if (epi == 0) gemm_w8a8_kernel<0, false, W4><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, nullptr, M, N, K);
+    else gemm_w8a8_kernel<1, false, W4><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, nullptr, M, N, K);
+}
+
 cudaError_t launch_gemm_w8a8(const int8_t* qa, const float* sa, const int8_t* qw, const float* dw, float* C,
-                             int32_t* partials, int M, int N, int K, int epi, cudaStream_t s) {
+                             int32_t* partials, int M, int N, int K, int epi, bool w4, cudaStream_t s) {
     if (M == 0 || N == 0) return cudaSuccess;
     dim3 grid((N + 63) / 64, (M + 63) / 64);
-    if (partials) {
-        gemm_w8a8_kernel<0, true><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, partials, M, N, K);
-    } else if (epi == 0) {
-        gemm_w8a8_kernel<0, false><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, nullptr, M, N, K);
-    } else {
-        gemm_w8a8_kernel<1, false><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, nullptr, M, N, K);
-    }
+    if (w4) launch_w8a8_t<true>(grid, qa, sa, qw, dw, C, partials, M, N, K, epi, s);
+    else launch_w8a8_t<false>(grid, qa, sa, qw, dw, C, partials, M, N, K, epi, s);
     return cudaGetLastError();
 }

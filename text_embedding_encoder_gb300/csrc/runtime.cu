@@ -81,7 +81,8 @@ int validate_config(const tee_config* c) {
     if (c->window < 0) return fail(nullptr, TEE_EINVAL, "window must be >= 0");
     if (!(c->rope_base_global > 0.f) || !(c->rope_base_local > 0.f)) return fail(nullptr, TEE_EINVAL, "RoPE bases must be > 0");
     if (!(c->ln_eps >= 0.f)) return fail(nullptr, TEE_EINVAL, "ln_eps must be >= 0");
-    if (c->dtype != TEE_F32 && c->dtype != TEE_BF16 && c->dtype != TEE_W8A8) return fail(nullptr, TEE_EINVAL, "unknown dtype");
+    if (c->dtype != TEE_F32 && c->dtype != TEE_BF16 && c->dtype != TEE_W8A8 && c->dtype != TEE_W4A8)
+        return fail(nullptr, TEE_EINVAL, "unknown dtype");
     if (c->max_tokens < 1 || c->max_texts < 1) return fail(nullptr, TEE_EINVAL, "max_tokens and max_texts must be >= 1");
     if (c->max_tokens > (1 << 24)) return fail(nullptr, TEE_EINVAL, "max_tokens must be <= 2^24");
     if ((c->emb_norm != 0 && c->emb_norm != 1) || (c->final_norm != 0 && c->final_norm != 1))
@@ -106,7 +107,7 @@ size_t carve_workspace(tee_ctx* c, void* base) {
     c->u = cv.take<char>(T * 2 * I, A);
     c->z = cv.take<char>(T * I, A);
     c->out = cv.take<float>((size_t)g.max_texts * H);
-    if (g.dtype == TEE_W8A8) {
+    if (is_int_path(g)) {
         c->qa = cv.take<int8_t>(T * std::max(H, I));
         c->qs = cv.take<float>(T);
     } else {
@@ -133,6 +134,8 @@ size_t carve_weights(tee_ctx* c, void* base) {
     const size_t H = g.hidden;
     Carve cv(base);
     const size_t esz = g.dtype == TEE_BF16 ? 2 : (g.dtype == TEE_F32 ? 4 : 1);
+    // bytes of an [N, K] projection: packed 4-bit codes take half a byte per weight
+    auto wbytes = [&](size_t n_k) { return g.dtype == TEE_W4A8 ? n_k / 2 : n_k * esz; };
     c->emb = cv.take<char>((size_t)g.vocab * H, g.dtype == TEE_BF16 ? 2 : 4);
     c->layers.assign(g.n_layers, LayerWeights{});
     for (int l = 0; l < g.n_layers; ++l) {
@@ -142,14 +145,14 @@ size_t carve_weights(tee_ctx* c, void* base) {
         for (int w = 0; w < 4; ++w) {
             int N, K;
             wshape(g, w, &N, &K);
-            L.w[w] = cv.take<char>((size_t)N * K, esz);
-            L.wd[w] = g.dtype == TEE_W8A8 ? cv.take<float>((size_t)N * K / 32) : nullptr;
+            L.w[w] = cv.take<char>(wbytes((size_t)N * K));
+            L.wd[w] = is_int_path(g) ? cv.take<float>((size_t)N * K / 32) : nullptr;
         }
     }
     c->ln_emb = g.emb_norm ? cv.take<float>(H) : nullptr;
     c->ln_final = g.final_norm ? cv.take<float>(H) : nullptr;
-    c->w_proj = g.proj_dim ? cv.take<char>((size_t)g.proj_dim * H, esz) : nullptr;
-    c->w_proj_d = g.proj_dim && g.dtype == TEE_W8A8 ? cv.take<float>((size_t)g.proj_dim * H / 32) : nullptr;
+    c->w_proj = g.proj_dim ? cv.take<char>(wbytes((size_t)g.proj_dim * H)) : nullptr;
+    c->w_proj_d = g.proj_dim && is_int_path(g) ? cv.take<float>((size_t)g.proj_dim * H / 32) : nullptr;
     return cv.off;
 }
 
@@ -291,12 +294,12 @@ int step_linear(tee_ctx* ctx, int layer, int which, const void* A, void* C, int 
     wshape(g, which, &N, &K);
     const LayerWeights& L = ctx->layers[layer];
     const double flops = 2.0 * T * N * K;
-    if (g.dtype == TEE_W8A8) {
+    if (is_int_path(g)) {
         LAUNCH(TEE_K_QUANT, 0, (double)T * K * 5 + T * 4.0,
                launch_quant_rows7((const float*)A, T, K, ctx->qa, ctx->qs, s));
         LAUNCH(TEE_K_GEMM, flops, (double)T * K + (double)N * K + (double)T * N * 4 * (epi ? 2 : 1),
                launch_gemm_w8a8(ctx->qa, ctx->qs, (const int8_t*)L.w[which], L.wd[which], (float*)C, nullptr, T, N,
-                                K, epi, s));
+                                K, epi, g.dtype == TEE_W4A8, s));
         return TEE_OK;
     }
     if (g.dtype == TEE_BF16) {
@@ -440,11 +443,11 @@ int run_tokens(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const in
     const int H = g.hidden, P = g.proj_dim, D = P ? P : H;
     if (!P) {
         CK(cudaMemcpyAsync(d_out, ctx->x, (size_t)T * H * 4, cudaMemcpyDeviceToDevice, s));
-    } else if (g.dtype == TEE_W8A8) {
+    } else if (is_int_path(g)) {
         LAUNCH(TEE_K_QUANT, 0, (double)T * H * 5 + T * 4.0, launch_quant_rows7(ctx->x, T, H, ctx->qa, ctx->qs, s));
         LAUNCH(TEE_K_GEMM, 2.0 * T * P * H, (double)T * H + (double)P * H + (double)T * P * 4,
                launch_gemm_w8a8(ctx->qa, ctx->qs, (const int8_t*)ctx->w_proj, ctx->w_proj_d, d_out, nullptr, T, P, H,
-                                0, s));
+                                0, g.dtype == TEE_W4A8, s));
     } else if (g.dtype == TEE_BF16) {
         // the projection's A operand in bf16, accumulated into a zeroed fp32 output
         LAUNCH(TEE_K_ELEMENTWISE, 0, (double)T * H * 6,
@@ -554,7 +557,7 @@ int tee_load_weights(tee_ctx* ctx, const tee_weights* w) {
         }
         CK(cudaMemcpyAsync(stage, src, n * sizeof(float), cudaMemcpyHostToDevice, s));
         if (kind == 1) CK(launch_convert_f32_bf16(stage, (bf16*)dst, n, s));
-        else CK(launch_quant_weight_blocks(stage, (int8_t*)dst, dscale, N, K, s));
+        else CK(launch_quant_weight_blocks(stage, (int8_t*)dst, dscale, N, K, g.dtype == TEE_W4A8, s));
         CK(cudaStreamSynchronize(s));
         return TEE_OK;
     };
@@ -827,26 +830,37 @@ int tee_op_w8a8_partials(tee_ctx* ctx, int layer, int which, const int8_t* d_q, 
                          void* stream) {
     int rc = check_ready(ctx);
     if (rc || (rc = check_layer(ctx, layer))) return rc;
-    if (ctx->cfg.dtype != TEE_W8A8) return fail(ctx, TEE_EINVAL, "context is not W8A8");
+    if (!is_int_path(ctx->cfg)) return fail(ctx, TEE_EINVAL, "context is not W8A8 / W4A8");
     int N, K;
     if (wshape(ctx->cfg, which, &N, &K)) return fail(ctx, TEE_EINVAL, "bad projection selector");
     if (M < 0) return fail(ctx, TEE_EINVAL, "bad M");
     const LayerWeights& L = ctx->layers[layer];
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_GEMM, 0, 0,
-           launch_gemm_w8a8(d_q, nullptr, (const int8_t*)L.w[which], L.wd[which], nullptr, d_partials, M, N, K, 0, s));
+           launch_gemm_w8a8(d_q, nullptr, (const int8_t*)L.w[which], L.wd[which], nullptr, d_partials, M, N, K, 0,
+                            ctx->cfg.dtype == TEE_W4A8, s));
     return TEE_OK;
 }
 
 int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d) {
     int rc = check_ready(ctx);
     if (rc || (rc = check_layer(ctx, layer))) return rc;
-    if (ctx->cfg.dtype != TEE_W8A8) return fail(ctx, TEE_EINVAL, "context is not W8A8");
+    if (!is_int_path(ctx->cfg)) return fail(ctx, TEE_EINVAL, "context is not W8A8 / W4A8");
     int N, K;
     if (wshape(ctx->cfg, which, &N, &K)) return fail(ctx, TEE_EINVAL, "bad projection selector");
     if (!h_q || !h_d) return fail(ctx, TEE_EINVAL, "NULL output");
     CK(cudaSetDevice(ctx->device));
-    CK(cudaMemcpy(h_q, ctx->layers[layer].w[which], (size_t)N * K, cudaMemcpyDeviceToHost));
+    if (ctx->cfg.dtype == TEE_W4A8) {   // widen the packed nibbles: element 2i low, 2i + 1 high
+        std::vector<uint8_t> packed((size_t)N * K / 2);
+        CK(cudaMemcpy(packed.data(), ctx->layers[layer].w[which], packed.size(), cudaMemcpyDeviceToHost));
+        for (size_t i = 0; i < packed.size(); ++i) {
+            const int lo = packed[i] & 15, hi = packed[i] >> 4;
+            h_q[2 * i] = (int8_t)((lo ^ 8) - 8);
+            h_q[2 * i + 1] = (int8_t)((hi ^ 8) - 8);
+        }
+    } else {
+        CK(cudaMemcpy(h_q, ctx->layers[layer].w[which], (size_t)N * K, cudaMemcpyDeviceToHost));
+    }
     CK(cudaMemcpy(h_d, ctx->layers[layer].wd[which], (size_t)N * K / 32 * 4, cudaMemcpyDeviceToHost));
     return TEE_OK;
 }
