@@ -351,10 +351,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 }
-                if (kt == 0 && pend && !finalize()) {   // previous unit, overlapped with this first softmax
-                    ok = false;
-                    break;
-                }
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
                 float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -372,6 +368,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_before();
                 mbar_arrive(bar(B_PF + sb));
                 l += sum;
+                // the previous unit's output, once this tile's P is handed over
+                if (kt == 0 && pend && !finalize()) {
+                    ok = false;
+                    break;
+                }
             }
             if (!ok) break;
             l_p = l;
