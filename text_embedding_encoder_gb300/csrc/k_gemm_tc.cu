@@ -159,11 +159,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool armed[S::STAGES];
             for (int s = 0; s < S::STAGES; ++s) armed[s] = false, armed_parity[s] = 0;
             bool ok = true;
+            // one CTA per tile (the short-K residual projection): A's tiles are
+            // prefetched into L2 PF k-steps ahead of their staging loads, so the
+            // shallower ring of this mode waits on L2 rather than DRAM (CTA
+            // pairs measured no gain from it)
+            constexpr int PF = S::STAGES + 4;
+            constexpr bool PREFETCH = !PAIR;
             for (int u = unit0; u < num_units && ok; u += ustride) {
                 const int n_t = u % num_n, m_t = unit_m(u);
+                if (PREFETCH && num_k > S::STAGES)
+                    for (int j = S::STAGES; j < PF && j < num_k; ++j) tma_prefetch_l2_2d(&tmA, j * BK, m_t * BM);
                 for (int kb = 0; kb < num_k; ++kb, ++g) {
                     const int s = g % S::STAGES;
                     const uint32_t r = g / S::STAGES;
+                    if (PREFETCH && num_k > S::STAGES && kb + PF < num_k)
+                        tma_prefetch_l2_2d(&tmA, (kb + PF) * BK, m_t * BM);
                     if (!mbar_wait(bar(EMPTY + s), (r & 1) ^ 1, abort_flag)) {
                         ok = false;
                         break;
