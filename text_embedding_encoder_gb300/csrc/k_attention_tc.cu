@@ -117,6 +117,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the prologue above may overlap the previous kernel; global memory only after it completes
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -443,6 +446,7 @@ cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, cons
     AttnParams p{d_items, n_units, n_heads, H, is_global ? 1 : 0, window, 1.4426950408889634f / 8.0f, (bf16*)o,
                  status};
     const int grid = n_units < g_num_sms ? n_units : g_num_sms;
-    attn_tc_kernel<<<grid, NUM_THREADS, SMEM_TOTAL, s>>>(tm, p);
+    cudaError_t e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_TOTAL, s, tm, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

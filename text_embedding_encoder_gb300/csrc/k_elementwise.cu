@@ -29,6 +29,8 @@ __device__ __forceinline__ int text_of(const int32_t* cu, int n_texts, int t) {
 }
 
 __global__ void convert_f32_bf16_kernel(const float* __restrict__ src, bf16* __restrict__ dst, size_t n) {
+    pdl_wait();
+    pdl_trigger();
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     size_t stride = (size_t)gridDim.x * blockDim.x;
     for (; i < n; i += stride) dst[i] = __float2bfloat16_rn(src[i]);
@@ -39,6 +41,8 @@ __global__ void convert_f32_bf16_kernel(const float* __restrict__ src, bf16* __r
 template <typename TE>
 __global__ void embed_kernel(const TE* __restrict__ emb, const int32_t* __restrict__ ids, int T, int H, int V,
                              float* __restrict__ x, unsigned int* status) {
+    pdl_wait();
+    pdl_trigger();
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
@@ -71,6 +75,8 @@ __global__ void embed_kernel(const TE* __restrict__ emb, const int32_t* __restri
 
 // pos[t] = t - cu[text(t)]
 __global__ void positions_kernel(const int32_t* __restrict__ cu, int n_texts, int T, int32_t* __restrict__ pos) {
+    pdl_wait();
+    pdl_trigger();
     int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     pos[t] = t - cu[text_of(cu, n_texts, t)];
@@ -80,6 +86,8 @@ __global__ void positions_kernel(const int32_t* __restrict__ cu, int n_texts, in
 // y may be x itself (fp32 output): a warp reads its whole row before writing it.
 template <typename TY>
 __global__ void layernorm_kernel(const float* x, const float* __restrict__ gamma, TY* y, int T, int H, float eps) {
+    pdl_wait();
+    pdl_trigger();
     int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     int lane = threadIdx.x & 31;
     if (warp >= T) return;
@@ -228,6 +236,8 @@ __global__ void pool_partial_kernel(const float* __restrict__ x, const int32_t* 
 __global__ void pool_fused_kernel(const float* __restrict__ x, const int32_t* __restrict__ cu,
                                   const int32_t* __restrict__ chunk_off, int n_texts, int H, float* partial,
                                   unsigned int* counters, float* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[32];
     __shared__ int is_last;
     const int chunk = blockIdx.x;
@@ -377,6 +387,8 @@ __global__ void pool_finish_kernel(const float* __restrict__ partial, const int3
 // One warp per row: x[r] /= max(|x[r]|, 1e-12), D a multiple of 4 and <= 1024;
 // the sum of squares in a fixed order (per-lane partials, then the shuffle tree).
 __global__ void l2_rows_kernel(float* x, int M, int D) {
+    pdl_wait();
+    pdl_trigger();
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= M) return;
@@ -445,7 +457,8 @@ cudaError_t launch_convert_f32_bf16(const float* src, bf16* dst, size_t n, cudaS
     if (n == 0) return cudaSuccess;
     size_t blocks = (n + 255) / 256;
     if (blocks > 152 * 64) blocks = 152 * 64;
-    convert_f32_bf16_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, dst, n);
+    cudaError_t e = launch_pdl(convert_f32_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, s, src, dst, n);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -454,15 +467,14 @@ cudaError_t launch_embed(const void* emb, bool emb_bf16, const int32_t* ids, int
     if (T == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((T + 7) / 8);   // one warp per token
     if (emb_bf16)
-        embed_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)emb, ids, T, H, V, x, status);
-    else
-        embed_kernel<float><<<blocks, 256, 0, s>>>((const float*)emb, ids, T, H, V, x, status);
-    return cudaGetLastError();
+        return launch_pdl(embed_kernel<bf16>, dim3(blocks), dim3(256), 0, s, (const bf16*)emb, ids, T, H, V, x, status);
+    return launch_pdl(embed_kernel<float>, dim3(blocks), dim3(256), 0, s, (const float*)emb, ids, T, H, V, x, status);
 }
 
 cudaError_t launch_positions(const int32_t* cu, int n_texts, int T, int32_t* pos, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    positions_kernel<<<(T + 255) / 256, 256, 0, s>>>(cu, n_texts, T, pos);
+    cudaError_t e = launch_pdl(positions_kernel, dim3((T + 255) / 256), dim3(256), 0, s, cu, n_texts, T, pos);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -471,10 +483,8 @@ cudaError_t launch_layernorm(const float* x, const float* gamma, void* y, bool y
     if (T == 0) return cudaSuccess;
     int blocks = (T + 7) / 8;   // 8 warps per block, one row per warp
     if (y_bf16)
-        layernorm_kernel<bf16><<<blocks, 256, 0, s>>>(x, gamma, (bf16*)y, T, H, eps);
-    else
-        layernorm_kernel<float><<<blocks, 256, 0, s>>>(x, gamma, (float*)y, T, H, eps);
-    return cudaGetLastError();
+        return launch_pdl(layernorm_kernel<bf16>, dim3(blocks), dim3(256), 0, s, x, gamma, (bf16*)y, T, H, eps);
+    return launch_pdl(layernorm_kernel<float>, dim3(blocks), dim3(256), 0, s, x, gamma, (float*)y, T, H, eps);
 }
 
 cudaError_t launch_rope(void* qkv, bool bf16_act, const int32_t* pos, const float* cos_t, const float* sin_t, int T,
@@ -503,7 +513,8 @@ cudaError_t launch_geglu(const void* u, void* z, bool bf16_act, int T, int I, cu
 cudaError_t launch_l2_rows(float* x, int M, int D, cudaStream_t s) {
     if (M == 0) return cudaSuccess;
     if (D % 4 || D > 1024) return cudaErrorInvalidValue;
-    l2_rows_kernel<<<(M + 7) / 8, 256, 0, s>>>(x, M, D);
+    cudaError_t e = launch_pdl(l2_rows_kernel, dim3((M + 7) / 8), dim3(256), 0, s, x, M, D);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -512,7 +523,9 @@ cudaError_t launch_pool_l2_fused(const float* x, const int32_t* cu, const int32_
                                  cudaStream_t s) {
     if (n_texts == 0) return cudaSuccess;
     if (H % 4 || H > 1024) return cudaErrorInvalidValue;
-    pool_fused_kernel<<<n_chunks, H / 4, 0, s>>>(x, cu, chunk_off, n_texts, H, partial, counters, out);
+    cudaError_t e = launch_pdl(pool_fused_kernel, dim3(n_chunks), dim3(H / 4), 0, s, x, cu, chunk_off, n_texts, H,
+                               partial, counters, out);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -150,6 +150,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if constexpr (CL) cluster_sync();   // the peer's copies and commits may target these barriers only after init
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the prologue above may overlap the previous kernel; global memory only after it completes
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -478,16 +481,18 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
     constexpr uint32_t smem = Smem<BN, EPI, MODE>::TOTAL;
     auto kernel = gemm_tc_kernel<BN, EPI, MODE>;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL ? 2 : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (!max_grid) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

@@ -85,6 +85,33 @@ struct tee_ctx {
     tee_kernel_stat prof_acc[TEE_K_COUNT];
 };
 
+// ---- programmatic dependent launch -----------------------------------------
+// The pass's kernels are launched with programmatic stream serialization: a
+// kernel may start (and run its prologue: barrier init, TMEM allocation) while
+// the previous kernel in the stream finishes.  Every such kernel calls
+// pdl_wait() before it touches global memory: it returns once the previous
+// kernel has completed and its writes are visible, and since that kernel did
+// the same, every earlier kernel has completed too.  pdl_trigger() lets the
+// next kernel launch once every block of this one has started.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- helpers ------------------------------------------------------------
 inline bool act_is_bf16(const tee_ctx* c) { return c->cfg.dtype == TEE_BF16; }
 // the integer paths: int8 (W8A8) or packed 4-bit (W4A8) weight blocks, 7-bit activations
