@@ -225,3 +225,20 @@ def test_gemm_bf16_shapes(lib, M, N, K, epi):
         enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 1, 0)
         np.testing.assert_allclose(to_np(c), c0.astype(np.float64) + ref, atol=2e-3 * max(1.0, np.abs(ref).max()))
     enc.close()
+
+
+@pytest.mark.parametrize("M", [2048, 8192, 20000])
+def test_gemm_residual_long_k_tile_choices(lib, M):
+    # the FFN out-projection shape at row counts whose wave model picks single
+    # CTAs on 128 columns (2048), CTA pairs on 192 (8192) and on 256 (20000)
+    N, K = 768, 3072
+    enc = binding.Encoder(synth.TINY, "bf16", max_tokens=16, max_texts=4)
+    rng = np.random.default_rng(M)
+    a = dev(rng.standard_normal((M, K)).astype(np.float32), torch.bfloat16)
+    w = dev((rng.standard_normal((N, K)) * 0.05).astype(np.float32), torch.bfloat16)
+    c0 = rng.standard_normal((M, N)).astype(np.float32)
+    c = dev(c0)
+    enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 1, 0)
+    ref = to_np(a) @ to_np(w).T
+    np.testing.assert_allclose(to_np(c), c0.astype(np.float64) + ref, atol=2e-3 * max(1.0, np.abs(ref).max()))
+    enc.close()

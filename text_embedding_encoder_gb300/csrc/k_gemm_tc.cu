@@ -525,22 +525,34 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.W) | reinterpret_cast<uintptr_t>(a.C)) & 15)
         return cudaErrorMisalignedAddress;
     if (a.M == 0) return cudaSuccess;
-    // Residual add: short-K projections use 128-column tiles (many tiles for
-    // N = 768) and stage each warp's whole 32 x 128 fp32 slice through TMA;
-    // long-K ones use the widest tile N allows (256, else 192: less operand
-    // traffic per FLOP) and stage the slice in a ring of 32-column boxes.
-    // Other epilogues use 256-column tiles where N allows.
-    const bool add_long = a.epi == GEMM_EPI_ADD_F32 && a.K > 1024;
-    const int add_bn = !add_long ? 128 : (a.N % 256 == 0 ? 256 : (a.N % 192 == 0 ? 192 : 128));
-    const bool add_wide = add_bn > 128;
-    const int BN = a.epi == GEMM_EPI_ADD_F32 ? add_bn : ((a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128);
     const int num_m = (a.M + BM - 1) / BM;
-    // CTA pairs compute 256-row tiles when there are at least two row tiles,
-    // except for the short-K residual projection, whose fp32 residual traffic
-    // per tile is large next to its MMA time: paired CTAs wait on each other's
-    // residual loads and measured slower than independent ones
-    const bool pair_ok = !(a.epi == GEMM_EPI_ADD_F32 && !add_wide);
-    const int mode = num_m >= 2 && pair_ok ? MODE_PAIR : MODE_SINGLE;
+    // Residual add, short K: 128-column tiles, one CTA per tile (each warp's
+    // whole 32 x 128 fp32 slice staged through TMA; paired CTAs wait on each
+    // other's residual loads and measured slower).  Residual add, long K:
+    // CTA pairs on 256- or 192-column tiles, or single CTAs on 128-column
+    // tiles, whichever a wave model says finishes first: waves of units over
+    // the SMs (or SM pairs) times the tile width times a per-configuration
+    // cost per column measured on the 310m shape (pairs on 256 columns 0.87,
+    // on 192 columns 1.0, single CTAs on 128 columns 1.05).  Few rows leave
+    // most SMs idle with wide pair tiles, so small batches get narrow single
+    // tiles.  Other epilogues: CTA pairs on 256-column tiles where N allows
+    // (GeGLU always), else 128.
+    const bool add_long = a.epi == GEMM_EPI_ADD_F32 && a.K > 1024;
+    int BN = a.epi == GEMM_EPI_ADD_F32 ? 128 : ((a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128);
+    int mode = num_m >= 2 && a.epi != GEMM_EPI_ADD_F32 ? MODE_PAIR : MODE_SINGLE;
+    if (add_long) {
+        const int pairs = (num_m + 1) / 2, clusters = g_num_sms / 2;
+        auto waves = [](long units, long slots) { return (units + slots - 1) / slots; };
+        double best = (double)waves((long)num_m * (a.N / 128), g_num_sms) * 128 * 1.05;
+        if (num_m >= 2 && a.N % 256 == 0) {
+            const double c = (double)waves((long)pairs * (a.N / 256), clusters) * 256 * 0.87;
+            if (c < best) best = c, BN = 256, mode = MODE_PAIR;
+        }
+        if (num_m >= 2 && a.N % 192 == 0) {
+            const double c = (double)waves((long)pairs * (a.N / 192), clusters) * 192 * 1.0;
+            if (c < best) best = c, BN = 192, mode = MODE_PAIR;
+        }
+    }
     const int b_rows = mode == MODE_SINGLE ? BN : BN / 2;
     CUtensorMap ma, mb, mc_map;
     if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, b_rows)) return cudaErrorInvalidValue;
@@ -555,8 +567,8 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
 #define TEE_GEMM_DISPATCH(BN_, EPI_)                                                                  \
     return mode == MODE_PAIR ? launch_t<BN_, EPI_, MODE_PAIR>(ma, mb, mc_map, p, units, s)           \
                              : launch_t<BN_, EPI_, MODE_SINGLE>(ma, mb, mc_map, p, units, s)
-    if (add_bn == 256) TEE_GEMM_DISPATCH(256, GEMM_EPI_ADD_F32);
-    if (add_bn == 192) TEE_GEMM_DISPATCH(192, GEMM_EPI_ADD_F32);
+    if (a.epi == GEMM_EPI_ADD_F32 && BN == 256) TEE_GEMM_DISPATCH(256, GEMM_EPI_ADD_F32);
+    if (a.epi == GEMM_EPI_ADD_F32 && BN == 192) TEE_GEMM_DISPATCH(192, GEMM_EPI_ADD_F32);
     if (BN == 256) {
         switch (a.epi) {
             case GEMM_EPI_STORE_BF16: TEE_GEMM_DISPATCH(256, GEMM_EPI_STORE_BF16);
