@@ -395,8 +395,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int g = 0; g < BN / 128; ++g) {
                     const int col = g * 64;
                     float a[64], gt[64];
-                    tmem_ld64(taddr + col, a);
-                    tmem_ld64(taddr + BN / 2 + col, gt);
+                    // both loads in flight before one wait
+                    tmem_ld64_issue(taddr + col, a);
+                    tmem_ld64_issue(taddr + BN / 2 + col, gt);
+                    tmem_wait_ld();
+                    tmem_tie64(a);
+                    tmem_tie64(gt);
 #pragma unroll
                     for (int j = 0; j < 64; ++j) a[j] = gelu_as(a[j]) * gt[j];
                     store64(a, n_t * (BN / 2) + col, y_box);
