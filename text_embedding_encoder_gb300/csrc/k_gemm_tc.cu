@@ -319,26 +319,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
                 tc_fence_after();
                 bool ok = true;
-#pragma unroll 1
+                // chunk c + 1's accumulator columns are loaded from TMEM while
+                // chunk c is added and stored (two register sets, loop unrolled)
+                float v[2][32];
+                tmem_ld32_issue(taddr, v[0]);
+#pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     const int g = it * NC + c;
                     const int b = g % RB;
                     if (!mbar_wait(res_bar(b), (g / RB) & 1, abort_flag)) {
+                        tmem_wait_ld();
                         ok = false;
                         break;
                     }
                     res_done = g + 1;
-                    float v[32];
-                    tmem_ld32(taddr + c * 32, v);
+                    tmem_wait_ld();
+                    tmem_tie32(v[c & 1]);
+                    if (c + 1 < NC) tmem_ld32_issue(taddr + (c + 1) * 32, v[(c + 1) & 1]);
                     uint8_t* rp = rslice + b * 4096 + lane * 128;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         float4* q = reinterpret_cast<float4*>(rp + ((k ^ (lane & 7)) << 4));
                         float4 o = *q;
-                        o.x += v[4 * k + 0];
-                        o.y += v[4 * k + 1];
-                        o.z += v[4 * k + 2];
-                        o.w += v[4 * k + 3];
+                        o.x += v[c & 1][4 * k + 0];
+                        o.y += v[c & 1][4 * k + 1];
+                        o.z += v[c & 1][4 * k + 2];
+                        o.w += v[c & 1][4 * k + 3];
                         *q = o;
                     }
                     fence_proxy_async_smem();
