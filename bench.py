@@ -70,7 +70,7 @@ def peaks():
 # kernel sources with this digest; otherwise reported as null.
 GEMM_TRAFFIC_BYTES = 234.07e6
 GEMM_TRAFFIC_SOURCES = ['text_embedding_encoder_gb300/csrc/k_gemm_tc.cu', 'text_embedding_encoder_gb300/csrc/tc_ptx.cuh', 'text_embedding_encoder_gb300/csrc/gemm_tc.cuh']
-GEMM_TRAFFIC_DIGEST = "a6f2e8f9d1439c0e"
+GEMM_TRAFFIC_DIGEST = "debe6a97968f1642"
 
 
 def gemm_traffic():
