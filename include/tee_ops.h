@@ -82,7 +82,8 @@ int tee_op_ffn_out(tee_ctx* ctx, int layer, const void* d_z, float* d_x, int T, 
 int tee_op_gemm_bf16(tee_ctx* ctx, const void* d_a, const void* d_w, void* d_c, int M, int N, int K, int epilogue,
                      void* stream);
 
-/* out float[n*H] = L2-normalised per-text mean of x float[T*H]. */
+/* out float[n*H] = L2-normalised per-text mean of x float[T*H]; d_x and d_out
+ * 16-byte aligned (else TEE_EINVAL). */
 int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts,
                    float* d_out, void* stream);
 

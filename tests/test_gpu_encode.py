@@ -110,6 +110,24 @@ def test_ruri_sweep_32k_sampled(ruri_bf16, ruri_oracle_bf16):
     np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
 
 
+@pytest.mark.parametrize("budget,batch", [(2048, 3), (8192, 7)])
+def test_ruri_small_sweeps_sampled(ruri_bf16, ruri_oracle_bf16, budget, batch):
+    """The 2048- and 8192-token sweep sizes take other GEMM tilings (single
+    CTAs and 192-column CTA pairs on the long-K projection) and fewer
+    attention units than 32768; sampled texts against the oracle."""
+    ids, cu = synth.sweep_batch(budget, batch, synth.RURI_310M.vocab)
+    n = len(cu) - 1
+    out = torch.empty(n, synth.RURI_310M.hidden, device="cuda")
+    ruri_bf16.encode_device(dev(ids), dev(cu), cu, out, 0)
+    torch.cuda.synchronize()
+    got = to_np(out)
+    lens = np.diff(cu)
+    sample = sorted({0, int(np.argmin(lens)), int(np.argmax(lens)), n - 1})
+    ref = oracle.encode_packed(ids, cu, ruri_oracle_bf16, texts=sample)
+    assert_embeddings_close(got[sample], ref[sample], "bf16")
+    np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
+
+
 def test_ruri_long_docs_sampled(ruri_bf16, ruri_oracle_bf16):
     ids, cu = synth.make_batch(synth.LONG_DOC_LENGTHS, synth.RURI_310M.vocab, seed=0)
     got = ruri_bf16.encode(ids, cu)

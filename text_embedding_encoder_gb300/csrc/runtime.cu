@@ -385,6 +385,8 @@ int prepare_pool_chunks(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cudaStre
 int step_pool(tee_ctx* ctx, const float* x, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int T, float* out,
               cudaStream_t s) {
     const tee_config& g = ctx->cfg;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
+        return fail(ctx, TEE_EINVAL, "pool: x and out must be 16-byte aligned");
     int rc = prepare_pool_chunks(ctx, h_cu, n_texts, s);
     if (rc) return rc;
     const int n_chunks = ctx->h_chunk_off[n_texts];
