@@ -8,26 +8,31 @@
 // Work unit = (text, 128-query tile) x head; the host lists the (text, tile)
 // items with their key range [k_lo, k_hi) (whole text, or the window clipped to
 // the text), longest first.  The kernel is persistent: one CTA per SM walks
-// the units u = blockIdx.x, blockIdx.x + gridDim.x, ...  Six warps:
+// the units u = blockIdx.x, blockIdx.x + gridDim.x, ...  Ten warps:
 //   warp 0 lane 0   TMA: each unit's Q tile (double-buffered, so the next
 //                   unit's Q arrives early), then its K and V tiles (128 keys)
-//                   into a 3-stage ring, straight from the packed qkv rows;
+//                   into a KV_STAGES-deep ring, straight from the packed qkv
+//                   rows;
 //   warp 1          TMEM allocation; lane 0 issues S = Q K^T (M=128, N=128,
-//                   K=64) into one of two TMEM S buffers, and O_t = P_t V_t
-//                   (M=128, N=64, K=128; V read as an MN-major operand, no
-//                   transpose) into one of two TMEM O buffers.  S of tile t+1
-//                   is issued before P_t V_t, across unit boundaries too, so
-//                   the softmax of one tile overlaps the QK^T of the next;
+//                   K=64) into one of two TMEM S buffers, and O += P_t V_t
+//                   (M=128, N=64, K=128) with P read from tensor memory (the
+//                   A operand) and V from shared memory as an MN-major operand
+//                   (no transpose), into the unit's TMEM O buffer (two, by
+//                   unit).  S of tile t+1 is issued before P_t V_t, across
+//                   unit boundaries too, so the softmax of one tile overlaps
+//                   the QK^T of the next;
 //   warps 2-9       two threads per query row (a warp may read only its
 //                   32-lane TMEM quadrant, so warps w and w+4 share one and
 //                   split the 128 key columns, and the 64 output dimensions,
 //                   in halves): one 64-column TMEM load of S, the mask as a
 //                   per-row interval of visible keys, the tile's row maximum
 //                   exchanged through shared memory with a pair barrier, the
-//                   online softmax in fp32 with exp2 (scale folded into one
-//                   FMA), P as bf16 into shared memory in the 128-byte swizzle
-//                   layout, O = O * corr + P_t V_t in registers, O / l stored
-//                   as bf16.
+//                   softmax in fp32 with exp2 (scale folded into one FMA)
+//                   against a reference maximum that moves only when a tile's
+//                   maximum exceeds it by more than 2^8 (then that row of O is
+//                   rescaled in TMEM), P as bf16 pairs stored into TMEM for the
+//                   P V MMA; a unit's O / l is read and stored as bf16 after
+//                   the next unit's first P hand-off.
 // Pipeline counters run across units; every wait is bounded.
 #include "tee_internal.cuh"
 
@@ -119,8 +124,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            bool q_armed[2] = {false, false}, kv_armed[KV_STAGES] = {false, false, false};
-            uint32_t q_par[2] = {0, 0}, kv_par[KV_STAGES] = {0, 0, 0};
+            bool q_armed[2] = {false, false}, kv_armed[KV_STAGES] = {};
+            uint32_t q_par[2] = {0, 0}, kv_par[KV_STAGES] = {};
             uint32_t g = 0;   // KV tiles issued
             int ui = 0;
             bool ok = true;
