@@ -227,6 +227,23 @@ def test_gemm_bf16_shapes(lib, M, N, K, epi):
     enc.close()
 
 
+@pytest.mark.parametrize("M", [2048, 24000, 32768])
+def test_gemm_residual_short_k_tile_choices(lib, M):
+    # the attention out-projection shape at row counts whose wave model picks
+    # 128-column tiles (2048) and 192-column tiles (24000, 32768), one CTA each
+    N, K = 768, 768
+    enc = binding.Encoder(synth.TINY, "bf16", max_tokens=16, max_texts=4)
+    rng = np.random.default_rng(M + 1)
+    a = dev(rng.standard_normal((M, K)).astype(np.float32), torch.bfloat16)
+    w = dev((rng.standard_normal((N, K)) * 0.05).astype(np.float32), torch.bfloat16)
+    c0 = rng.standard_normal((M, N)).astype(np.float32)
+    c = dev(c0)
+    enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 1, 0)
+    ref = to_np(a) @ to_np(w).T
+    np.testing.assert_allclose(to_np(c), c0.astype(np.float64) + ref, atol=2e-3 * max(1.0, np.abs(ref).max()))
+    enc.close()
+
+
 @pytest.mark.parametrize("M", [2048, 8192, 20000])
 def test_gemm_residual_long_k_tile_choices(lib, M):
     # the FFN out-projection shape at row counts whose wave model picks single
