@@ -70,7 +70,7 @@ def peaks():
 # kernel sources with this digest; otherwise reported as null.
 GEMM_TRAFFIC_BYTES = 232.94e6
 GEMM_TRAFFIC_SOURCES = ['text_embedding_encoder_gb300/csrc/k_gemm_tc.cu', 'text_embedding_encoder_gb300/csrc/tc_ptx.cuh', 'text_embedding_encoder_gb300/csrc/gemm_tc.cuh']
-GEMM_TRAFFIC_DIGEST = "ce02d2a1824d91b3"
+GEMM_TRAFFIC_DIGEST = "920454dc26e00e89"
 
 
 def gemm_traffic():

@@ -145,6 +145,33 @@ int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d
  * `stream`. */
 int tee_selftest_wait_timeout(tee_ctx* ctx, long long wait_cycles, void* stream);
 
+/* ---- host-only planning (no device, no context) -------------------------
+ * The decisions a pass takes on the host before it launches, exported so that
+ * they can be checked without a GPU.  Errors return a negative TEE_E* code with
+ * a message in tee_last_error(NULL). */
+
+/* Attention work items, as the pass lists them for the varlen attention
+ * kernel (packing paragraph of §何が動くか: attention stays inside each text;
+ * §エンコーダ: the whole text on global layers, +-window tokens otherwise):
+ * one item per (text j, 128-query tile), {q_start, q_len, k_lo, k_hi} with
+ * q_start = cu[j] + 128 i, q_len = min(128, cu[j+1] - q_start) and [k_lo, k_hi)
+ * the keys that any query of the tile may see -- [cu[j], cu[j+1]) if
+ * is_global, else [max(cu[j], q_start - window), min(cu[j+1], q_start + q_len
+ * + window)).  The global list is ordered by q_len * (k_hi - k_lo), largest
+ * first, ties in text order; the window list is in text order.  h_cu host
+ * int32[n_texts + 1] (cu[0] == 0, strictly increasing).  items: host
+ * int32[4 * max_items], or NULL to ask for the count only.  Returns the
+ * number of items (TEE_ETOOLONG if it exceeds max_items). */
+int tee_plan_attention(const int32_t* h_cu, int n_texts, int window, int is_global, int32_t* items, int max_items);
+
+/* Tile shape of the bf16 tensor-core projection C[M, N] = A[M, K] W^T: *bn =
+ * tile width in columns (128, 192 or 256), *pair = 1 when 2-CTA clusters
+ * compute 256-row tiles, 0 for one CTA per 128-row tile, as the library
+ * chooses it on a GPU with num_sms SMs.  epi: 0 bf16 store, 1 fp32 residual
+ * add, 2 QKV with RoPE, 3 GeGLU (N % 256 == 0).  M >= 1, N % 128 == 0,
+ * K % 64 == 0, num_sms >= 2. */
+int tee_plan_gemm(int M, int N, int K, int epi, int num_sms, int* bn, int* pair);
+
 /* Synchronise the context's device status word: TEE_OK, or TEE_EINVAL if a
  * kernel met an out-of-range token id since the last call (the word is then
  * cleared), or TEE_ETIMEOUT if a bounded device wait gave up. */

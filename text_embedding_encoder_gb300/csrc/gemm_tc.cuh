@@ -26,6 +26,12 @@ struct GemmTcArgs {
 
 cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s);
 
+// Tile width (*bn) and CTA pairing (*pair: 1 = 2-CTA clusters on 256-row
+// tiles, 0 = one CTA per 128-row tile) that launch_gemm_tc uses for an
+// [M, N] x K product with epilogue `epi` on a GPU of num_sms SMs (host only;
+// arguments as launch_gemm_tc accepts them).
+void gemm_tc_choose_tiles(int M, int N, int K, int epi, int num_sms, int* bn, int* pair);
+
 // Row permutation of Wi used by GEMM_EPI_GEGLU: stored row r holds original row
 // geglu_source_row(r, I).
 inline int geglu_source_row(int r, int I) {

@@ -526,16 +526,8 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
 
 }  // namespace
 
-cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
-    std::call_once(g_once, init_once);
-    if (g_init_err != cudaSuccess) return g_init_err;
-    if (a.M < 0 || a.N <= 0 || a.K <= 0 || a.N % 128 || a.K % BK) return cudaErrorInvalidValue;
-    if (a.epi == GEMM_EPI_GEGLU && a.N % 256) return cudaErrorInvalidValue;
-    if (a.epi < GEMM_EPI_STORE_BF16 || a.epi > GEMM_EPI_GEGLU) return cudaErrorInvalidValue;
-    if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.W) | reinterpret_cast<uintptr_t>(a.C)) & 15)
-        return cudaErrorMisalignedAddress;
-    if (a.M == 0) return cudaSuccess;
-    const int num_m = (a.M + BM - 1) / BM;
+void gemm_tc_choose_tiles(int M, int N, int K, int epi, int num_sms, int* bn, int* pair) {
+    const int num_m = (M + BM - 1) / BM;
     // Residual add, short K: one CTA per tile (paired CTAs wait on each
     // other's residual loads and measured slower) on 128- or 192-column tiles,
     // whichever takes fewer column-waves (waves of tiles over the SMs times the
@@ -551,25 +543,42 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     // most SMs idle with wide pair tiles, so small batches get narrow single
     // tiles.  Other epilogues: CTA pairs on 256-column tiles where N allows
     // (GeGLU always), else 128.
-    const bool add_long = a.epi == GEMM_EPI_ADD_F32 && a.K > 1024;
-    int BN = a.epi == GEMM_EPI_ADD_F32 ? 128 : ((a.epi == GEMM_EPI_GEGLU || a.N % 256 == 0) ? 256 : 128);
-    int mode = num_m >= 2 && a.epi != GEMM_EPI_ADD_F32 ? MODE_PAIR : MODE_SINGLE;
+    const bool add_long = epi == GEMM_EPI_ADD_F32 && K > 1024;
+    int BN = epi == GEMM_EPI_ADD_F32 ? 128 : ((epi == GEMM_EPI_GEGLU || N % 256 == 0) ? 256 : 128);
+    int mode = num_m >= 2 && epi != GEMM_EPI_ADD_F32 ? MODE_PAIR : MODE_SINGLE;
     auto waves = [](long units, long slots) { return (units + slots - 1) / slots; };
-    if (a.epi == GEMM_EPI_ADD_F32 && !add_long && a.N % 192 == 0 &&
-        waves((long)num_m * (a.N / 192), g_num_sms) * 192 < waves((long)num_m * (a.N / 128), g_num_sms) * 128)
+    if (epi == GEMM_EPI_ADD_F32 && !add_long && N % 192 == 0 &&
+        waves((long)num_m * (N / 192), num_sms) * 192 < waves((long)num_m * (N / 128), num_sms) * 128)
         BN = 192;
     if (add_long) {
-        const int pairs = (num_m + 1) / 2, clusters = g_num_sms / 2;
-        double best = (double)waves((long)num_m * (a.N / 128), g_num_sms) * 128 * 1.05;
-        if (num_m >= 2 && a.N % 256 == 0) {
-            const double c = (double)waves((long)pairs * (a.N / 256), clusters) * 256 * 0.87;
+        const int pairs = (num_m + 1) / 2, clusters = num_sms / 2;
+        double best = (double)waves((long)num_m * (N / 128), num_sms) * 128 * 1.05;
+        if (num_m >= 2 && N % 256 == 0) {
+            const double c = (double)waves((long)pairs * (N / 256), clusters) * 256 * 0.87;
             if (c < best) best = c, BN = 256, mode = MODE_PAIR;
         }
-        if (num_m >= 2 && a.N % 192 == 0) {
-            const double c = (double)waves((long)pairs * (a.N / 192), clusters) * 192 * 1.0;
+        if (num_m >= 2 && N % 192 == 0) {
+            const double c = (double)waves((long)pairs * (N / 192), clusters) * 192 * 1.0;
             if (c < best) best = c, BN = 192, mode = MODE_PAIR;
         }
     }
+    *bn = BN;
+    *pair = mode == MODE_PAIR;
+}
+
+cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
+    std::call_once(g_once, init_once);
+    if (g_init_err != cudaSuccess) return g_init_err;
+    if (a.M < 0 || a.N <= 0 || a.K <= 0 || a.N % 128 || a.K % BK) return cudaErrorInvalidValue;
+    if (a.epi == GEMM_EPI_GEGLU && a.N % 256) return cudaErrorInvalidValue;
+    if (a.epi < GEMM_EPI_STORE_BF16 || a.epi > GEMM_EPI_GEGLU) return cudaErrorInvalidValue;
+    if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.W) | reinterpret_cast<uintptr_t>(a.C)) & 15)
+        return cudaErrorMisalignedAddress;
+    if (a.M == 0) return cudaSuccess;
+    const int num_m = (a.M + BM - 1) / BM;
+    int BN = 128, pair = 0;
+    gemm_tc_choose_tiles(a.M, a.N, a.K, a.epi, g_num_sms, &BN, &pair);
+    const int mode = pair ? MODE_PAIR : MODE_SINGLE;
     const int b_rows = mode == MODE_SINGLE ? BN : BN / 2;
     CUtensorMap ma, mb, mc_map;
     if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, b_rows)) return cudaErrorInvalidValue;

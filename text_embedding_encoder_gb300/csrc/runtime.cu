@@ -210,21 +210,24 @@ double attention_pairs(const int32_t* h_cu, int n_texts, bool is_global, int w) 
 // key range the queries of that tile may see.  List 0 (global layers): the
 // whole text, longest texts first so the heavy CTAs start early; list 1
 // (window layers): the window around the tile, clipped to the text.
-int prepare_attention_items(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cudaStream_t s) {
-    const int w = ctx->cfg.window;
-    for (int b = 0; b < 2; ++b) ctx->h_items[b].clear();
+void plan_attention_items(const int32_t* h_cu, int n_texts, int w, std::vector<int4> (&items)[2]) {
+    for (int b = 0; b < 2; ++b) items[b].clear();
     for (int j = 0; j < n_texts; ++j) {
         const int s0 = h_cu[j], s1 = h_cu[j + 1];
         for (int q0 = s0; q0 < s1; q0 += 128) {
             const int ql = std::min(128, s1 - q0);
-            ctx->h_items[0].push_back(make_int4(q0, ql, s0, s1));
-            ctx->h_items[1].push_back(make_int4(q0, ql, std::max(s0, q0 - w), std::min(s1, q0 + ql + w)));
+            items[0].push_back(make_int4(q0, ql, s0, s1));
+            items[1].push_back(make_int4(q0, ql, std::max(s0, q0 - w), std::min(s1, q0 + ql + w)));
         }
     }
-    std::stable_sort(ctx->h_items[0].begin(), ctx->h_items[0].end(), [](const int4& a, const int4& b) {
+    std::stable_sort(items[0].begin(), items[0].end(), [](const int4& a, const int4& b) {
         const long long ca = (long long)a.y * (a.w - a.z), cb = (long long)b.y * (b.w - b.z);
         return ca > cb;
     });
+}
+
+int prepare_attention_items(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cudaStream_t s) {
+    plan_attention_items(h_cu, n_texts, ctx->cfg.window, ctx->h_items);
     for (int b = 0; b < 2; ++b) {
         if ((int)ctx->h_items[b].size() > ctx->max_items)
             return fail(ctx, TEE_ETOOLONG, "too many attention work items");
@@ -693,6 +696,39 @@ void tee_destroy(tee_ctx* ctx) {
     if (ctx->tok_out) cudaFree(ctx->tok_out);
     if (ctx->stream) cudaStreamDestroy(ctx->stream);
     delete ctx;
+}
+
+// ---- host-only planning (no device, no context) ---------------------------
+
+int tee_plan_attention(const int32_t* h_cu, int n_texts, int window, int is_global, int32_t* items, int max_items) {
+    if (!h_cu) return tee_set_global_error(TEE_EINVAL, "plan_attention: cu_seqlens is NULL");
+    if (n_texts < 1) return tee_set_global_error(TEE_EINVAL, "plan_attention: n_texts must be >= 1");
+    if (window < 0) return tee_set_global_error(TEE_EINVAL, "plan_attention: window must be >= 0");
+    if (h_cu[0] != 0) return tee_set_global_error(TEE_EINVAL, "plan_attention: cu_seqlens[0] must be 0");
+    for (int j = 0; j < n_texts; ++j)
+        if (h_cu[j + 1] <= h_cu[j])
+            return tee_set_global_error(TEE_EINVAL, "plan_attention: cu_seqlens must be strictly increasing");
+    std::vector<int4> lists[2];
+    plan_attention_items(h_cu, n_texts, window, lists);
+    const std::vector<int4>& v = lists[is_global ? 0 : 1];
+    if (!items) return (int)v.size();
+    if ((int)v.size() > max_items) return tee_set_global_error(TEE_ETOOLONG, "plan_attention: more items than max_items");
+    for (size_t i = 0; i < v.size(); ++i) {
+        items[4 * i + 0] = v[i].x;
+        items[4 * i + 1] = v[i].y;
+        items[4 * i + 2] = v[i].z;
+        items[4 * i + 3] = v[i].w;
+    }
+    return (int)v.size();
+}
+
+int tee_plan_gemm(int M, int N, int K, int epi, int num_sms, int* bn, int* pair) {
+    if (!bn || !pair) return tee_set_global_error(TEE_EINVAL, "plan_gemm: NULL output");
+    if (M < 1 || N < 128 || N % 128 || K < 64 || K % 64 || epi < GEMM_EPI_STORE_BF16 || epi > GEMM_EPI_GEGLU ||
+        (epi == GEMM_EPI_GEGLU && N % 256) || num_sms < 2)
+        return tee_set_global_error(TEE_EINVAL, "plan_gemm: shape, epilogue or SM count out of range");
+    gemm_tc_choose_tiles(M, N, K, epi, num_sms, bn, pair);
+    return TEE_OK;
 }
 
 int tee_profile_enable(tee_ctx* ctx, int on) {
