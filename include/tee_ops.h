@@ -12,7 +12,11 @@
  *   (uint16 bit patterns).  The residual stream x is always float.
  * Shapes: T = rows (tokens), H = hidden, I = intermediate, row-major.
  * Return codes as in tee.h.  Buffers are borrowed for the duration of the
- * stream work only.
+ * stream work only.  Device buffers must be non-NULL and 16-byte aligned
+ * (int32 arrays -- ids, cu_seqlens, positions, block sums -- 4-byte aligned,
+ * activation scales 4-byte aligned); otherwise the call returns TEE_EINVAL
+ * before launching anything.  A call with no rows (T or M == 0) launches
+ * nothing and checks no device pointer.
  *
  * Steps (tensai page "テキスト埋め込み", §何が動くか):
  *   embed       x[t] = E[id[t]]                                   (token embedding)

@@ -259,3 +259,39 @@ def test_gemm_residual_long_k_tile_choices(lib, M):
     ref = to_np(a) @ to_np(w).T
     np.testing.assert_allclose(to_np(c), c0.astype(np.float64) + ref, atol=2e-3 * max(1.0, np.abs(ref).max()))
     enc.close()
+
+
+def test_step_entry_points_reject_unaligned_and_null_buffers(lib):
+    # every check returns before anything is launched; the context stays usable
+    shape = synth.TINY
+    enc = make_encoder(shape, "bf16", synth.make_weights(shape, seed=0), max_tokens=64, max_texts=4)
+    T, H = 16, shape.hidden
+    cu = np.array([0, T], np.int32)
+    buf = torch.zeros(3 * T * shape.intermediate + 64, dtype=torch.float32, device="cuda")
+    good = buf.data_ptr()
+    bad = good + 4                      # 4-byte aligned, not 16
+    d_cu, ids, pos = dev(cu), dev(np.ones(T, np.int32)), dev(np.zeros(T, np.int32))
+    calls = [
+        ("tee_op_embed", lambda p: (ids, T, p, 0)),
+        ("tee_op_layernorm", lambda p: (0, 0, p, good, T, 0)),
+        ("tee_op_layernorm", lambda p: (0, 0, good, p, T, 0)),
+        ("tee_op_qkv", lambda p: (0, p, pos, good, T, 0)),
+        ("tee_op_attention", lambda p: (0, p, d_cu, cu, 1, good, 0)),
+        ("tee_op_out_proj", lambda p: (0, p, good, T, 0)),
+        ("tee_op_ffn_in", lambda p: (0, good, p, T, 0)),
+        ("tee_op_ffn_out", lambda p: (0, good, p, T, 0)),
+        ("tee_op_pool_l2", lambda p: (p, d_cu, cu, 1, good, 0)),
+    ]
+    for name, args in calls:
+        for p in (bad, 0):
+            with pytest.raises(binding.TeeError) as e:
+                enc.op(name, *args(p))
+            assert e.value.code == binding.TEE_EINVAL, (name, p)
+    with pytest.raises(binding.TeeError) as e:   # int32 arrays: 4-byte alignment
+        enc.op("tee_op_positions", d_cu, cu, 1, good + 2, 0)
+    assert e.value.code == binding.TEE_EINVAL
+    x = torch.empty(T, H, device="cuda")
+    enc.op("tee_op_embed", ids, T, x, 0)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np(x), np.broadcast_to(to_np(x)[:1], (T, H)))   # every id is 1
+    enc.close()

@@ -16,6 +16,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <initializer_list>
 #include <new>
 
 namespace {
@@ -489,6 +490,19 @@ int check_layer(tee_ctx* ctx, int layer) {
     return TEE_OK;
 }
 
+// Device buffers handed to a per-step entry point: non-NULL and aligned to
+// `align` bytes (16 for activations, which the kernels move as 16-byte
+// vectors or TMA tiles; 4 for int32 arrays).  Checked when the step has work.
+int check_dev(tee_ctx* ctx, long long n, int align, std::initializer_list<const void*> ptrs) {
+    if (n <= 0) return TEE_OK;
+    for (const void* p : ptrs) {
+        if (!p) return fail(ctx, TEE_EINVAL, "device buffer is NULL");
+        if (reinterpret_cast<uintptr_t>(p) % (uintptr_t)align)
+            return fail(ctx, TEE_EINVAL, "device buffer is not %d-byte aligned", align);
+    }
+    return TEE_OK;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -764,6 +778,7 @@ int tee_op_embed(tee_ctx* ctx, const int32_t* d_ids, int T, float* d_x, void* st
     int rc = check_ready(ctx);
     if (rc) return rc;
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    if ((rc = check_dev(ctx, T, 16, {d_x})) || (rc = check_dev(ctx, T, 4, {d_ids}))) return rc;
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_EMBED, 0, 0,
            launch_embed(ctx->emb, act_is_bf16(ctx), d_ids, T, ctx->cfg.hidden, ctx->cfg.vocab, d_x, ctx->d_status, s));
@@ -774,7 +789,7 @@ int tee_op_positions(tee_ctx* ctx, const int32_t* d_cu, const int32_t* h_cu, int
                      void* stream) {
     if (!ctx) return TEE_EINVAL;
     int T = 0, rc = check_cu(ctx, h_cu, n_texts, &T);
-    if (rc) return rc;
+    if (rc || (rc = check_dev(ctx, T, 4, {d_cu, d_pos}))) return rc;
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_EMBED, 0, 0, launch_positions(d_cu, n_texts, T, d_pos, s));
     return TEE_OK;
@@ -785,6 +800,7 @@ int tee_op_layernorm(tee_ctx* ctx, int layer, int which, const float* d_x, void*
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     if (which != TEE_LN_ATTN && which != TEE_LN_MLP) return fail(ctx, TEE_EINVAL, "bad LayerNorm selector");
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    if ((rc = check_dev(ctx, T, 16, {d_x, d_y}))) return rc;
     return step_layernorm(ctx, layer, which, d_x, d_y, T, (cudaStream_t)stream);
 }
 
@@ -792,6 +808,7 @@ int tee_op_qkv(tee_ctx* ctx, int layer, const void* d_y, const int32_t* d_pos, v
     int rc = check_ready(ctx);
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    if ((rc = check_dev(ctx, T, 16, {d_y, d_qkv})) || (rc = check_dev(ctx, T, 4, {d_pos}))) return rc;
     return step_qkv(ctx, layer, d_y, d_pos, d_qkv, T, (cudaStream_t)stream);
 }
 
@@ -801,6 +818,7 @@ int tee_op_attention(tee_ctx* ctx, int layer, const void* d_qkv, const int32_t* 
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     int T = 0;
     if ((rc = check_cu(ctx, h_cu, n_texts, &T))) return rc;
+    if ((rc = check_dev(ctx, T, 16, {d_qkv, d_o})) || (rc = check_dev(ctx, T, 4, {d_cu}))) return rc;
     if (ctx->cfg.dtype == TEE_BF16 && (rc = prepare_attention_items(ctx, h_cu, n_texts, (cudaStream_t)stream)))
         return rc;
     return step_attention(ctx, layer, d_qkv, d_cu, h_cu, n_texts, T, d_o, (cudaStream_t)stream);
@@ -810,6 +828,7 @@ int tee_op_out_proj(tee_ctx* ctx, int layer, const void* d_o, float* d_x, int T,
     int rc = check_ready(ctx);
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    if ((rc = check_dev(ctx, T, 16, {d_o, d_x}))) return rc;
     return step_linear(ctx, layer, TEE_W_OUT, d_o, d_x, T, 1, GEMM_EPI_ADD_F32, nullptr, (cudaStream_t)stream);
 }
 
@@ -817,6 +836,7 @@ int tee_op_ffn_in(tee_ctx* ctx, int layer, const void* d_y, void* d_z, int T, vo
     int rc = check_ready(ctx);
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    if ((rc = check_dev(ctx, T, 16, {d_y, d_z}))) return rc;
     return step_ffn_in(ctx, layer, d_y, d_z, T, (cudaStream_t)stream);
 }
 
@@ -824,6 +844,7 @@ int tee_op_ffn_out(tee_ctx* ctx, int layer, const void* d_z, float* d_x, int T, 
     int rc = check_ready(ctx);
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
+    if ((rc = check_dev(ctx, T, 16, {d_z, d_x}))) return rc;
     return step_linear(ctx, layer, TEE_W_FFN_OUT, d_z, d_x, T, 1, GEMM_EPI_ADD_F32, nullptr, (cudaStream_t)stream);
 }
 
@@ -852,13 +873,15 @@ int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const in
                    float* d_out, void* stream) {
     if (!ctx) return TEE_EINVAL;
     int T = 0, rc = check_cu(ctx, h_cu, n_texts, &T);
-    if (rc) return rc;
+    if (rc || (rc = check_dev(ctx, T, 16, {d_x, d_out})) || (rc = check_dev(ctx, T, 4, {d_cu}))) return rc;
     return step_pool(ctx, d_x, d_cu, h_cu, n_texts, T, d_out, (cudaStream_t)stream);
 }
 
 int tee_op_quant_rows7(tee_ctx* ctx, const float* d_x, int M, int K, int8_t* d_q, float* d_s, void* stream) {
     if (!ctx) return TEE_EINVAL;
     if (M < 0 || K < 1) return fail(ctx, TEE_EINVAL, "bad M/K");
+    int rc = check_dev(ctx, M, 16, {d_x, d_q});
+    if (rc || (rc = check_dev(ctx, M, 4, {d_s}))) return rc;
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_QUANT, 0, 0, launch_quant_rows7(d_x, M, K, d_q, d_s, s));
     return TEE_OK;
@@ -872,6 +895,7 @@ int tee_op_w8a8_partials(tee_ctx* ctx, int layer, int which, const int8_t* d_q, 
     int N, K;
     if (wshape(ctx->cfg, which, &N, &K)) return fail(ctx, TEE_EINVAL, "bad projection selector");
     if (M < 0) return fail(ctx, TEE_EINVAL, "bad M");
+    if ((rc = check_dev(ctx, M, 16, {d_q})) || (rc = check_dev(ctx, M, 4, {d_partials}))) return rc;
     const LayerWeights& L = ctx->layers[layer];
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_GEMM, 0, 0,
