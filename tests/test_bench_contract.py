@@ -49,6 +49,23 @@ def test_reference_arm_prints_the_contract_line():
     assert "workload" in d["config"]
 
 
+def test_reference_arm_under_torchrun_prints_once():
+    # two ranks: rank 0 alone runs the oracle and prints; the other exits 0 without work
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    assert json.loads(lines[0])["impl"] == "reference"
+
+
 @pytest.mark.skipif(_cuda_available(), reason="checks the behaviour without a GPU")
 def test_library_refuses_to_run_without_a_gpu():
     try:
