@@ -152,9 +152,11 @@ int tee_encode(tee_ctx* ctx, const int32_t* token_ids, const int32_t* cu_seqlens
  *          sizing).  ids are not range-checked on the host on this path: the
  *          gather kernel turns an out-of-range id into a zero row and sets
  *          the context's device status word (tee_device_status, tee_ops.h);
- *   d_out  device float[n_texts * hidden].
+ *   d_out  device float[n_texts * hidden], 16-byte aligned.
  * All device buffers must stay valid until the stream reaches the end of
- * the pass.  Errors: TEE_EINVAL, TEE_ETOOLONG, TEE_ENOTLOADED, TEE_ECUDA.
+ * the pass.  Errors: TEE_EINVAL (also for a NULL device pointer or a
+ * misaligned d_out, before anything is launched), TEE_ETOOLONG,
+ * TEE_ENOTLOADED, TEE_ECUDA.
  */
 int tee_encode_device(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const int32_t* h_cu,
                       int n_texts, float* d_out, void* stream);

@@ -655,6 +655,7 @@ int tee_encode_device(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, c
     int rc = check_ready(ctx);
     if (rc) return rc;
     if (!d_ids || !d_cu || !d_out) return fail(ctx, TEE_EINVAL, "device pointer is NULL");
+    if (reinterpret_cast<uintptr_t>(d_out) & 15) return fail(ctx, TEE_EINVAL, "d_out must be 16-byte aligned");
     int T = 0;
     if ((rc = check_cu(ctx, h_cu, n_texts, &T))) return rc;
     CK(cudaSetDevice(ctx->device));
