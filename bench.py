@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-leg", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the chosen workload (not the sweep's other sizes and the long documents)")
     ap.add_argument("--workload", default="sweep32k", choices=sorted(WORKLOADS))
     ap.add_argument("--output", default="pooled", choices=["pooled", "tokens"],
                     help="pooled: one unit vector per text (the headline); tokens: one per token")
@@ -183,6 +185,105 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 
+def make_batches(workload, vocab, rank=0, world=1):
+    """The 20 seeded batches of a workload; rank r takes batches r, r+N, ..."""
+    from text_embedding_encoder_gb300 import synth
+    budget, _ = WORKLOADS[workload]
+    batches = []
+    for b in range(rank, synth.SWEEP_BATCHES * world, world):
+        if workload == "long":
+            ids, cu = synth.make_batch(synth.LONG_DOC_LENGTHS, vocab, seed=b)
+        else:
+            ids, cu = synth.sweep_batch(budget, b % synth.SWEEP_BATCHES + (b // synth.SWEEP_BATCHES) * 100, vocab)
+        batches.append((ids, cu))
+    return batches
+
+
+def stage(batches, tokens_out, width):
+    """Inputs resident in HBM before any timed region: (d_ids, d_cu, h_cu, d_out) per batch."""
+    import torch
+    out = []
+    for ids, cu in batches:
+        rows = len(ids) if tokens_out else len(cu) - 1
+        out.append((torch.from_numpy(ids).cuda(), torch.from_numpy(cu).cuda(), cu,
+                    torch.empty(rows, width, device="cuda")))
+    return out
+
+
+def measure(enc, d_batches, steps, warmup, tokens_out, dist=None, clocks=None):
+    """W warm-up passes, then two timed regions of K passes each between CUDA
+    events on the launching stream (barrier + synchronize on both sides, max
+    over ranks): the first un-instrumented (the throughput; clocks sampled
+    during it), the second with CUDA events around every launch (per-kernel
+    split, launch count, rooflines).  Returns (ms, ms_profiled, prof, clk)."""
+    import torch
+    stream = torch.cuda.current_stream().cuda_stream
+    encode_device = enc.encode_tokens_device if tokens_out else enc.encode_device
+
+    def step(i):
+        d_ids, d_cu, h_cu, d_out = d_batches[i % len(d_batches)]
+        encode_device(d_ids, d_cu, h_cu, d_out, stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+
+    def timed_region(profile: bool):
+        enc.profile_enable(profile)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        ev0.record()
+        for i in range(steps):
+            step(i)
+        ev1.record()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t_ms = ev0.elapsed_time(ev1)
+        if dist:
+            t = torch.tensor([t_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_ms = float(t.item())
+        return t_ms
+
+    if clocks:
+        clocks.start()
+    ms = timed_region(profile=False)
+    clk = clocks.stop() if clocks else None
+    ms_profiled = timed_region(profile=True)
+    prof = enc.profile_read()
+    enc.profile_enable(False)
+    return ms, ms_profiled, prof, clk
+
+
+def gemm_rate(prof):
+    """Algorithmic GEMM FLOPs of the profiled steps / their summed CUDA-event durations (TFLOP/s)."""
+    g = prof["gemm"]
+    if not g["launches"] or g["total_ms"] <= 0:
+        return None
+    return g["flops"] / (g["total_ms"] / 1e3) / 1e12
+
+
+def hbm_rates(prof, peak_gbs):
+    """Algorithmic HBM bytes / summed CUDA-event durations of the memory-bound kernel classes."""
+    out = {}
+    names = {"layernorm": "layernorm_kernel (both LayerNorms of every layer)",
+             "embed": "embed_kernel + positions_kernel", "pool": "pool_fused_kernel (mean-pool + L2)"}
+    for k, desc in names.items():
+        v = prof.get(k, {})
+        if v.get("launches") and v["total_ms"] > 0 and v["bytes"] > 0:
+            gbs = v["bytes"] / (v["total_ms"] / 1e3) / 1e9
+            out[k] = {"kernel": desc, "achieved": round(gbs, 1), "peak": peak_gbs, "unit": "GB/s",
+                      "frac": round(gbs / peak_gbs, 4), "launches": v["launches"],
+                      "bytes_per_launch": round(v["bytes"] / v["launches"], 1),
+                      "us_per_launch": round(1e3 * v["total_ms"] / v["launches"], 2)}
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -200,73 +301,22 @@ def run_ours(args):
     shape = synth.Shape(**{**synth.RURI_310M.as_dict(), "emb_norm": args.norms, "final_norm": args.norms,
                            "proj_dim": args.proj_dim if tokens_out else 0})
 
-    # workload: the 20 seeded batches of the chosen size; rank r takes batches r, r+N, ...
     budget, desc = WORKLOADS[args.workload]
-    batches = []
-    for b in range(rank, synth.SWEEP_BATCHES * world, world):
-        if args.workload == "long":
-            ids, cu = synth.make_batch(synth.LONG_DOC_LENGTHS, shape.vocab, seed=b)
-        else:
-            ids, cu = synth.sweep_batch(budget, b % synth.SWEEP_BATCHES + (b // synth.SWEEP_BATCHES) * 100,
-                                        shape.vocab)
-        batches.append((ids, cu))
-    max_texts = max(len(cu) - 1 for _, cu in batches)
+    batches = make_batches(args.workload, shape.vocab, rank, world)
+    # the other workloads of the sweep, timed in the same run (one GPU only)
+    extra = [w for w in ("sweep2k", "sweep8k", "long") if w != args.workload] if world == 1 and not args.no_extra else []
+    extra_batches = {w: make_batches(w, shape.vocab) for w in extra}
+    max_tokens = max([budget] + [WORKLOADS[w][0] for w in extra])
+    max_texts = max(len(cu) - 1 for bl in [batches] + list(extra_batches.values()) for _, cu in bl)
     weights = synth.make_weights(shape, seed=0)
-    enc = binding.Encoder(shape, "bf16", max_tokens=budget, max_texts=max_texts, device=local)
+    enc = binding.Encoder(shape, "bf16", max_tokens=max_tokens, max_texts=max_texts, device=local)
     enc.load_weights(weights)
     del weights
 
     width = enc.token_width if tokens_out else shape.hidden   # columns of one output row
-    d_batches = []
-    for ids, cu in batches:
-        rows = len(ids) if tokens_out else len(cu) - 1
-        d_batches.append((torch.from_numpy(ids).cuda(), torch.from_numpy(cu).cuda(), cu,
-                          torch.empty(rows, width, device="cuda")))
-    stream = torch.cuda.current_stream().cuda_stream
-    encode_device = enc.encode_tokens_device if tokens_out else enc.encode_device
-
-    def step(i):
-        d_ids, d_cu, h_cu, d_out = d_batches[i % len(d_batches)]
-        encode_device(d_ids, d_cu, h_cu, d_out, stream)
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-
-    def timed_region(profile: bool):
-        """K steps between CUDA events on the launching stream, barrier and
-        synchronize on both sides; returns the max over ranks in ms."""
-        enc.profile_enable(profile)
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        ev0.record()
-        for i in range(args.steps):
-            step(i)
-        ev1.record()
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        t_ms = ev0.elapsed_time(ev1)
-        if dist:
-            t = torch.tensor([t_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_ms = float(t.item())
-        return t_ms
-
-    # region 1: the throughput (no instrumentation), with clocks sampled during it
-    clocks = ClockSampler(local)
-    clocks.start()
-    ms = timed_region(profile=False)
-    clk = clocks.stop()
-    # region 2: the same K steps with CUDA events around every launch, for the
-    # per-kernel split, the launch count and the GEMM roofline
-    ms_profiled = timed_region(profile=True)
-    prof = enc.profile_read()
-    enc.profile_enable(False)
+    d_batches = stage(batches, tokens_out, width)
+    ms, ms_profiled, prof, clk = measure(enc, d_batches, args.steps, args.warmup, tokens_out, dist,
+                                         ClockSampler(local))
     tokens_per_rank = budget * args.steps
     value = tokens_per_rank * world / (ms / 1e3)
 
@@ -298,15 +348,19 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
     e2e_value = tokens_per_rank * world / e2e_s
+    del pinned
 
     pk = peaks()
-    g = prof["gemm"]
-    gemm_ms_avg = g["total_ms"] / max(1, g["launches"])
-    gemm_flops_avg = g["flops"] / max(1, g["launches"])
-    achieved_tflops = gemm_flops_avg / (gemm_ms_avg / 1e3) / 1e12 if g["launches"] else None
-    peak = pk["bf16_tflops_sustained"]
+    achieved_tflops = gemm_rate(prof)
+    # the GEMM rate comes from CUDA events around each single launch (a kernel
+    # timed alone, tens to hundreds of microseconds), so the burst peak applies
+    peak = pk["bf16_tflops"]
     launches = sum(v["launches"] for v in prof.values())
-    flops_per_token = gemm_flops_per_token(shape, tokens_out) + prof["attention"]["flops"] / (budget * args.steps)
+
+    def pct_peak(v, prof_, tokens_step):
+        fpt = gemm_flops_per_token(shape, tokens_out) + prof_["attention"]["flops"] / (tokens_step * args.steps)
+        return round(100.0 * v * fpt / (pk["bf16_tflops"] * 1e12), 2)
+
     kernel_share = {k: round(v["total_ms"] / max(1e-9, sum(x["total_ms"] for x in prof.values())), 4)
                     for k, v in prof.items() if v["launches"]}
 
@@ -331,24 +385,52 @@ def run_ours(args):
                               else "one unit vector per text (mean pool + L2)"),
                    "norms": "embedding + final LayerNorm" if args.norms else "none (the page's encoder)",
                    "l2": "inputs larger than L2 (weights 472 MB + activations per pass)"},
-        "pct_tensor_peak": round(100.0 * value / world * flops_per_token / (pk["bf16_tflops"] * 1e12), 2),
+        "pct_tensor_peak": pct_peak(value / world, prof, budget),
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d // args.steps,
                 "d2h_bytes_per_step": d2h // args.steps},
         "gpu_launches": launches,
         "profiled_region": {"ms_per_step": round(ms_profiled / args.steps, 4),
                             "note": "a second timed region of the same K steps with CUDA events around every "
-                                    "launch; kernel_share, kernel_ms_per_step, gpu_launches and roofline come "
-                                    "from it"},
+                                    "launch; kernel_share, kernel_ms_per_step, gpu_launches and the rooflines "
+                                    "come from it"},
         "roofline": {"bound": "tensor", "kernel": "gemm_tc (tcgen05 bf16 projections)",
                      "achieved": round(achieved_tflops, 1) if achieved_tflops else None,
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved_tflops / peak, 4) if achieved_tflops else None,
-                     "peak_source": f"{pk['source']} sustained bf16", "traffic": gemm_traffic(),
+                     "peak_source": f"{pk['source']} burst bf16 (per-launch CUDA events time each GEMM alone)",
+                     "frac_of_sustained": (round(achieved_tflops / pk["bf16_tflops_sustained"], 4)
+                                           if achieved_tflops else None),
+                     "traffic": gemm_traffic(),
                      "traffic_unit": "bytes per launch (DRAM read + write, ncu)"},
+        "roofline_hbm": hbm_rates(prof, pk["hbm_gbs"]),
         "kernel_share": kernel_share,
         "kernel_ms_per_step": {k: round(v["total_ms"] / args.steps, 4) for k, v in prof.items() if v["launches"]},
     }
+
+    if extra:
+        # the sweep's other sizes and the long documents, same protocol, same
+        # context (its capacity is the largest workload's)
+        sampler = ClockSampler(local)
+        sampler.start()
+        workloads = {}
+        for w in extra:
+            steps_w = args.steps if w != "long" else max(3, args.steps // 5)
+            db = stage(extra_batches[w], tokens_out, width)
+            ms_w, _, prof_w, _ = measure(enc, db, steps_w, max(3, args.warmup), tokens_out)
+            tok = WORKLOADS[w][0]
+            v_w = tok * steps_w / (ms_w / 1e3)
+            r_w = gemm_rate(prof_w)
+            workloads[w] = {"workload": WORKLOADS[w][1], "value": round(v_w, 1), "unit": UNIT, "steps": steps_w,
+                            "ms_per_step": round(ms_w / steps_w, 4), "pct_tensor_peak": pct_peak(v_w, prof_w, tok),
+                            "gemm_tflops": round(r_w, 1) if r_w else None,
+                            "gemm_frac": round(r_w / peak, 4) if r_w else None,
+                            "kernel_ms_per_step": {k: round(v["total_ms"] / steps_w, 4) for k, v in prof_w.items()
+                                                   if v["launches"]}}
+            del db
+        result["workloads"] = workloads
+        result["workloads_clocks"] = sampler.stop()
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
             leg = run_cpu_leg_subprocess(20.0)

@@ -99,11 +99,16 @@ int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const in
  * cannot afford the implicit synchronisation of an allocation.  It needs no
  * context and calls no cudaMalloc, cudaFree or other allocating routine.
  *
- * Computes the same result as tee_op_pool_l2 with the same kernels:
- *   d_x    device float[T * hidden], T = h_cu[n_texts];
- *   d_cu   device int32[n_texts + 1];  h_cu: host copy of the same array
- *          (validated, and used to size the launch);
- *   d_out  device float[n_texts * hidden];  async on `stream`.
+ * Computes the same result as tee_op_pool_l2 (per-text mean, scaled to unit
+ * length) with the same chunked sums, in two launches:
+ *   d_x    device float[T * hidden], T = h_cu[n_texts], 16-byte aligned;
+ *   d_cu   device int32[n_texts + 1], 4-byte aligned;  h_cu: host copy of the
+ *          same array (validated, and used to size the launch).  The two must
+ *          hold the same values; the kernels clamp every row and chunk index
+ *          to the sizes taken from h_cu, so a disagreeing d_cu gives wrong
+ *          vectors but no access outside d_x or the scratch;
+ *   d_out  device float[n_texts * hidden], 16-byte aligned;  async on `stream`.
+ * A NULL or misaligned pointer returns TEE_EINVAL before anything is launched.
  * Its scratch (chunk offsets and the partial sums of 64-row chunks) lives in
  * file-scope device arrays of fixed size that every GPU loading the library
  * holds until the process exits (about 4 MiB).  Limits: n_texts <=
@@ -113,8 +118,10 @@ int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const in
  * tee_last_error(NULL).  Every call on a device shares the same scratch and
  * overwrites all of it that it reads, so calls that overlap on the GPU (for
  * instance on two streams) race.  The first call on a device looks up the
- * arrays' device addresses (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.
+ * arrays' device addresses (cudaGetSymbolAddress) with that device current
+ * and keeps them for the life of the process; make that first call before any
+ * stream capture, and do not call this entry point on a device after a
+ * cudaDeviceReset of that device (the arrays are reloaded at new addresses).
  */
 #define TEE_POOL_NOALLOC_MAX_TEXTS   8192
 #define TEE_POOL_NOALLOC_MAX_PARTIAL 1048576   /* floats */
@@ -148,6 +155,17 @@ int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d
  * returns once the limit expires; the context stays usable.  Asynchronous on
  * `stream`. */
 int tee_selftest_wait_timeout(tee_ctx* ctx, long long wait_cycles, void* stream);
+
+/* GELU self-test.  y[i] = GELU(a[i]) = a * Phi(a), evaluated exactly as the
+ * GeGLU epilogue of the bf16 tensor-core feed-forward projection does it (erf
+ * by the rational approximation of Abramowitz & Stegun formula 7.1.26 on the
+ * hardware reciprocal and exp2), so that this restatement of erf can be checked
+ * against an exact GELU over a dense range.  (tensai page, §何が動くか /
+ * エンコーダ: the feed-forward is GeGLU; reading: the erf form of GELU.)
+ * d_a, d_y: device float[n], 4-byte aligned; context-free, on the current
+ * device, asynchronous on `stream`.  Errors: TEE_EINVAL (NULL, misaligned,
+ * n < 0; message in tee_last_error(NULL)), TEE_ECUDA. */
+int tee_selftest_gelu(const float* d_a, float* d_y, long long n, void* stream);
 
 /* ---- host-only planning (no device, no context) -------------------------
  * The decisions a pass takes on the host before it launches, exported so that

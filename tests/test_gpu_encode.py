@@ -1,8 +1,9 @@
 """End-to-end encoder passes through the C ABI on the GPU, against the oracle.
 
 Covers the five workloads (tiny fp32; the 310m shape in bf16 on the
-7-text accuracy batch; sampled texts of a full 32768-token sweep batch and of
-the 8 x 8192 long-document batch; the W8A8 path with outlier channels), the
+7-text accuracy batch; every text of a full 32768-token sweep batch and of the
+2048- and 8192-token sizes; two documents of the 8 x 8192 long-document batch;
+the W8A8 path with outlier channels), the
 packing invariance the method states (a text's vector does not depend on the
 other texts packed with it), edge lengths around the tile and window sizes,
 and host-side rejection of malformed input.
@@ -17,6 +18,8 @@ torch = pytest.importorskip("torch")
 from gpu_util import BF16_COS, assert_embeddings_close, dev, make_encoder, to_np  # noqa: E402
 
 pytestmark = pytest.mark.gpu
+
+W8A8_VS_FP32_COS = 0.99   # W8A8 embeddings against the fp32 path, no outliers
 
 
 @pytest.fixture(scope="module")
@@ -94,46 +97,72 @@ def test_ruri_accuracy_batch_bf16(ruri_bf16, ruri_oracle_bf16):
     print(f"310m bf16 accuracy batch: max abs {err:.2e}, min cos {cos.min():.6f}")
 
 
-def test_ruri_sweep_32k_sampled(ruri_bf16, ruri_oracle_bf16):
+def test_ruri_sweep_32k_every_text(ruri_bf16, ruri_oracle_bf16):
     """Full 32768-token sweep batch in the bench's launch configuration
-    (device buffers, tee_encode_device); sampled texts checked by the oracle."""
+    (device buffers, tee_encode_device); every text checked by the oracle.
+    The attention work list is sorted longest first and spread over persistent
+    CTAs, so a scheduling mistake could hit any text."""
     ids, cu = synth.sweep_batch(32768, 0, synth.RURI_310M.vocab)
     n = len(cu) - 1
     out = torch.empty(n, synth.RURI_310M.hidden, device="cuda")
     ruri_bf16.encode_device(dev(ids), dev(cu), cu, out, 0)
     torch.cuda.synchronize()
     got = to_np(out)
-    lens = np.diff(cu)
-    sample = sorted({int(np.argmin(lens)), int(np.argmax(lens)), int(np.argsort(lens)[n // 2]), n - 1})
-    ref = oracle.encode_packed(ids, cu, ruri_oracle_bf16, texts=sample)
-    assert_embeddings_close(got[sample], ref[sample], "bf16")
+    ref = oracle.encode_packed(ids, cu, ruri_oracle_bf16)
+    err = assert_embeddings_close(got, ref, "bf16")
+    cos = np.sum(got * ref, axis=1)
+    print(f"32k sweep batch 0, {n} texts: max abs {err:.2e}, min cos {cos.min():.6f}")
     np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
 
 
 @pytest.mark.parametrize("budget,batch", [(2048, 3), (8192, 7)])
-def test_ruri_small_sweeps_sampled(ruri_bf16, ruri_oracle_bf16, budget, batch):
+def test_ruri_small_sweeps_every_text(ruri_bf16, ruri_oracle_bf16, budget, batch):
     """The 2048- and 8192-token sweep sizes take other GEMM tilings (single
     CTAs and 192-column CTA pairs on the long-K projection) and fewer
-    attention units than 32768; sampled texts against the oracle."""
+    attention units than 32768; every text against the oracle."""
     ids, cu = synth.sweep_batch(budget, batch, synth.RURI_310M.vocab)
-    n = len(cu) - 1
-    out = torch.empty(n, synth.RURI_310M.hidden, device="cuda")
+    out = torch.empty(len(cu) - 1, synth.RURI_310M.hidden, device="cuda")
     ruri_bf16.encode_device(dev(ids), dev(cu), cu, out, 0)
     torch.cuda.synchronize()
     got = to_np(out)
-    lens = np.diff(cu)
-    sample = sorted({0, int(np.argmin(lens)), int(np.argmax(lens)), n - 1})
+    ref = oracle.encode_packed(ids, cu, ruri_oracle_bf16)
+    assert_embeddings_close(got, ref, "bf16")
+    np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
+
+
+def test_ruri_long_docs_two_texts(ruri_bf16, ruri_oracle_bf16):
+    """8 x 8192 tokens: the first and a middle document against the oracle
+    (each alone is a full 8192-token global-attention text)."""
+    ids, cu = synth.make_batch(synth.LONG_DOC_LENGTHS, synth.RURI_310M.vocab, seed=0)
+    got = ruri_bf16.encode(ids, cu)
+    sample = [0, 5]
     ref = oracle.encode_packed(ids, cu, ruri_oracle_bf16, texts=sample)
     assert_embeddings_close(got[sample], ref[sample], "bf16")
     np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
 
 
-def test_ruri_long_docs_sampled(ruri_bf16, ruri_oracle_bf16):
-    ids, cu = synth.make_batch(synth.LONG_DOC_LENGTHS, synth.RURI_310M.vocab, seed=0)
-    got = ruri_bf16.encode(ids, cu)
-    ref = oracle.encode_packed(ids, cu, ruri_oracle_bf16, texts=[5])
-    assert_embeddings_close(got[[5]], ref[[5]], "bf16")
-    np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
+def test_two_contexts_interleaved_on_one_device(lib, tiny_weights):
+    """Two contexts (different shapes and arithmetic) used alternately in one
+    process: each entry point makes its own context's device current and puts
+    the caller's back, and the launchers keep their per-device state apart."""
+    odd = synth.Shape(n_layers=2, hidden=384, n_heads=6, head_dim=64, intermediate=640, vocab=1000)
+    w_odd = synth.make_weights(odd, seed=4)
+    a = make_encoder(synth.TINY, "bf16", tiny_weights, max_tokens=512, max_texts=16)
+    b = make_encoder(odd, "bf16", w_odd, max_tokens=512, max_texts=16)
+    c = make_encoder(synth.TINY, "fp32", tiny_weights, max_tokens=512, max_texts=16)
+    ids_t, cu_t = synth.make_batch([37, 150, 8, 64], synth.TINY.vocab, seed=2)
+    ids_o, cu_o = synth.make_batch([129, 3, 200], odd.vocab, seed=3)
+    ref_a = oracle.encode_packed(ids_t, cu_t, oracle.OracleModel(tiny_weights, synth.TINY, "bf16"))
+    ref_b = oracle.encode_packed(ids_o, cu_o, oracle.OracleModel(w_odd, odd, "bf16"))
+    ref_c = oracle.encode_packed(ids_t, cu_t, oracle.OracleModel(tiny_weights, synth.TINY, "fp32"))
+    before = torch.cuda.current_device()
+    for _ in range(3):
+        assert_embeddings_close(a.encode(ids_t, cu_t), ref_a, "bf16")
+        assert_embeddings_close(b.encode(ids_o, cu_o), ref_b, "bf16")
+        assert_embeddings_close(c.encode(ids_t, cu_t), ref_c, "fp32")
+    assert torch.cuda.current_device() == before
+    for e in (a, b, c):
+        e.close()
 
 
 @pytest.mark.parametrize("outliers", [False, True])
@@ -176,6 +205,16 @@ def test_ruri_w8a8(lib, outliers):
           f"{cos_f.min():.6f} (W8A8 oracle vs fp32 oracle: {cos_oracles.min():.6f})")
     assert cos_int.min() >= (0.95 if outliers else BF16_COS)
     np.testing.assert_allclose(np.linalg.norm(got, axis=1), 1.0, atol=1e-5)
+    if not outliers:
+        # against the fp32 path: the page's -q8 stays at cosine >= 0.9912 of the
+        # unquantised model on its trained weights; the bar here is 0.99
+        assert cos_f.min() >= W8A8_VS_FP32_COS, cos_f.min()
+    else:
+        # with 20x outlier channels the outliers set every row's 7-bit scale, so
+        # the other channels keep a few levels each and the W8A8 procedure itself
+        # is far from fp32 (the W8A8 oracle is at about 0.76 of the fp32 oracle);
+        # the GPU must not be further from fp32 than that procedure is
+        assert cos_f.min() >= cos_oracles.min() - 0.05, (cos_f.min(), cos_oracles.min())
 
 
 def test_host_validation_and_recovery(lib, tiny_weights):

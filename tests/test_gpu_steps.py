@@ -295,3 +295,30 @@ def test_step_entry_points_reject_unaligned_and_null_buffers(lib):
     torch.cuda.synchronize()
     np.testing.assert_array_equal(to_np(x), np.broadcast_to(to_np(x)[:1], (T, H)))   # every id is 1
     enc.close()
+
+
+def test_geglu_epilogue_gelu_dense_range(lib):
+    """The GeGLU epilogue of the tensor-core feed-forward projection evaluates
+    GELU with its own erf (Abramowitz & Stegun 7.1.26 on the hardware
+    reciprocal and exp2).  Checked over a dense range against the oracle's
+    GELU (scipy erf in fp64): the formula's own error (|erf error| <= 1.5e-7,
+    times |a| / 2 in GELU) plus the half-ulp rounding of the fp32 result."""
+    rng = np.random.default_rng(5)
+    a = np.concatenate([np.linspace(-10.0, 10.0, 1_000_001), rng.uniform(-10.0, 10.0, 1_000_000),
+                        np.array([0.0, -0.0, 1e-30, -1e-30, 1e-8, -1e-8, 12.0, -12.0, 14.0, -14.0, 30.0, -30.0])])
+    a = a.astype(np.float32)
+    d_a = dev(a)
+    d_y = torch.full_like(d_a, float("nan"))
+    rc = lib.tee_selftest_gelu(d_a.data_ptr(), d_y.data_ptr(), a.size, 0)
+    assert rc == binding.TEE_OK, lib.tee_last_error(None).decode()
+    torch.cuda.synchronize()
+    got = to_np(d_y)
+    ref = oracle.gelu(a.astype(np.float64))
+    err = np.abs(got - ref)
+    bound = 6e-7 + 2.0 ** -24 * np.abs(ref)
+    worst = int(np.argmax(err - bound))
+    print(f"GELU epilogue: max abs err {err.max():.3e} (at a = {a[int(np.argmax(err))]:.4f})")
+    assert np.all(err <= bound), (float(a[worst]), float(err[worst]), float(bound[worst]))
+    assert got[np.where(a == 0.0)[0]].tolist() == [0.0, 0.0]
+    # misaligned buffers are refused before any launch
+    assert lib.tee_selftest_gelu(d_a.data_ptr() + 2, d_y.data_ptr(), 4, 0) == binding.TEE_EINVAL

@@ -2,10 +2,10 @@
 world-size-2 `gloo` process groups (no GPU involved).
 
 Each rank stands in for one GPU: it encodes its texts with a per-text
-function that depends on the text alone (here: a deterministic unit vector
-from the text's ids), exactly the property that makes the encoder shard by
-text.  The gathered result must equal the single-process result in input
-order.
+function that depends on the text alone (a deterministic unit vector from the
+text's ids, or the CPU oracle's encoder on the tiny shape), exactly the
+property that makes the encoder shard by text.  The gathered result must
+equal the single-process result in input order.
 """
 import os
 import socket
@@ -84,3 +84,52 @@ def test_two_rank_gather_matches_single_process(lengths):
         assert p.exitcode == 0
     for r in range(2):
         np.testing.assert_array_equal(results[r], want)
+
+
+def _oracle_worker(rank, world, port, ids, cu, q):
+    import torch.distributed as dist
+    import oracle
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        model = oracle.OracleModel(synth.make_weights(synth.TINY, seed=0), synth.TINY, "fp32")
+        calls = []
+
+        def encode_fn(sub_ids, sub_cu):
+            calls.append(len(sub_cu) - 1)
+            return oracle.encode_packed(sub_ids, sub_cu, model)
+
+        full = sharding.encode_sharded(encode_fn, ids, cu, synth.TINY.hidden)
+        q.put((rank, full, calls))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("lengths", [[37, 150, 8, 64, 129, 3], [60]])   # [60]: rank 1 encodes nothing
+def test_encode_sharded_with_the_oracle_as_encoder(lengths):
+    """encode_sharded, the multi-GPU helper the library's Encoder.encode plugs
+    into, run over two gloo ranks with the oracle as each rank's encoder: the
+    gathered vectors equal the oracle's single-process encoding of the batch."""
+    import oracle
+    ids, cu = synth.make_batch(lengths, synth.TINY.vocab, seed=3)
+    model = oracle.OracleModel(synth.make_weights(synth.TINY, seed=0), synth.TINY, "fp32")
+    want = oracle.encode_packed(ids, cu, model).astype(np.float32)
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_oracle_worker, args=(r, 2, port, ids, cu, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = {}
+    for _ in range(2):
+        r, full, calls = q.get(timeout=300)
+        results[r] = (full, calls)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in range(2):
+        np.testing.assert_array_equal(results[r][0], want)
+    assert sum(sum(c) for _, c in results.values()) == len(lengths)   # every text encoded exactly once
+    if len(lengths) == 1:
+        assert results[1][1] == []

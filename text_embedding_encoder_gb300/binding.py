@@ -90,6 +90,7 @@ SIGNATURES = {
     "tee_device_status": (_i, [_ctx]),
     "tee_pool_l2_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp]),
     "tee_selftest_wait_timeout": (_i, [_ctx, ctypes.c_longlong, _vp]),
+    "tee_selftest_gelu": (_i, [_vp, _vp, ctypes.c_longlong, _vp]),
     "tee_plan_attention": (_i, [_vp, _i, _i, _i, _vp, _i]),
     "tee_plan_gemm": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
 }

@@ -399,8 +399,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 cudaError_t g_init_err = cudaSuccess;
-bool g_attr_set = false;
-int g_num_sms = 0;
+std::mutex g_attr_mu;
+bool g_attr_set[TEE_MAX_DEVICES] = {};   // the kernel's shared-memory attribute, per device
 
 void init_once() {
     cudaDriverEntryPointQueryResult q;
@@ -411,10 +411,6 @@ void init_once() {
         return;
     }
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    int dev = 0;
-    cudaGetDevice(&dev);
-    e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) g_init_err = e;
 }
 
 }  // namespace
@@ -435,16 +431,22 @@ cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, cons
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (!g_attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_TOTAL);
-        if (e != cudaSuccess) return e;
-        g_attr_set = true;
+    int dev = 0, num_sms = 0;
+    cudaError_t de = tee_current_device(&dev, &num_sms);
+    if (de != cudaSuccess) return de;
+    {
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        if (!g_attr_set[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)SMEM_TOTAL);
+            if (e != cudaSuccess) return e;
+            g_attr_set[dev] = true;
+        }
     }
     const int n_units = n_items * n_heads;
     AttnParams p{d_items, n_units, n_heads, H, is_global ? 1 : 0, window, 1.4426950408889634f / 8.0f, (bf16*)o,
                  status};
-    const int grid = n_units < g_num_sms ? n_units : g_num_sms;
+    const int grid = n_units < num_sms ? n_units : num_sms;
     cudaError_t e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_TOTAL, s, tm, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -184,13 +184,15 @@ __global__ void geglu_kernel(const TA* __restrict__ u, TA* __restrict__ z, int T
 // text; thread c4 sums float4 column group c4 over the chunk's rows and writes
 // the partial sum.  chunk_off[j] is the first chunk of text j (chunk_off[n] =
 // total chunks).
+// Rows are clamped to [0, T): a device cu_seqlens that disagrees with the host
+// copy the launch was sized from cannot move the reads outside x.
 __global__ void pool_partial_kernel(const float* __restrict__ x, const int32_t* __restrict__ cu,
-                                    const int32_t* __restrict__ chunk_off, int n_texts, int H,
+                                    const int32_t* __restrict__ chunk_off, int n_texts, int T, int H,
                                     float* __restrict__ partial) {
     const int chunk = blockIdx.x;
     const int j = text_of(chunk_off, n_texts, chunk);
-    const int r0 = cu[j] + (chunk - chunk_off[j]) * POOL_CHUNK;
-    const int r1 = min(cu[j + 1], r0 + POOL_CHUNK);
+    const int r0 = max(0, cu[j] + (chunk - chunk_off[j]) * POOL_CHUNK);
+    const int r1 = min(min(cu[j + 1], r0 + POOL_CHUNK), T);
     for (int c4 = threadIdx.x; c4 < H / 4; c4 += blockDim.x) {
         // eight independent accumulators keep eight row loads in flight
         float4 acc[8];
@@ -339,11 +341,13 @@ __global__ void pool_fused_kernel(const float* __restrict__ x, const int32_t* __
 // into eight accumulators, combined in a fixed order, so the result is
 // deterministic and eight loads per column are in flight), divides by the
 // length and scales to unit norm (norm floored at 1e-12).  H <= 4 * blockDim.x.
+// The chunk range is clamped to the n_chunks partials the first pass wrote.
 __global__ void pool_finish_kernel(const float* __restrict__ partial, const int32_t* __restrict__ cu,
-                                   const int32_t* __restrict__ chunk_off, int H, float* __restrict__ out) {
+                                   const int32_t* __restrict__ chunk_off, int n_chunks, int H,
+                                   float* __restrict__ out) {
     __shared__ float red[32];
     const int j = blockIdx.x;
-    const int k0 = chunk_off[j], k1 = chunk_off[j + 1];
+    const int k0 = max(0, chunk_off[j]), k1 = min(chunk_off[j + 1], n_chunks);
     const float inv_len = 1.0f / (float)(cu[j + 1] - cu[j]);
     float acc[4];
 #pragma unroll
@@ -530,13 +534,13 @@ cudaError_t launch_pool_l2_fused(const float* x, const int32_t* cu, const int32_
 }
 
 cudaError_t launch_pool_l2(const float* x, const int32_t* cu, const int32_t* chunk_off, int n_texts, int n_chunks,
-                           int H, float* partial, float* out, cudaStream_t s) {
+                           int T, int H, float* partial, float* out, cudaStream_t s) {
     if (n_texts == 0) return cudaSuccess;
     const int threads = H / 4 < 256 ? H / 4 : 256;
-    pool_partial_kernel<<<n_chunks, threads, 0, s>>>(x, cu, chunk_off, n_texts, H, partial);
+    pool_partial_kernel<<<n_chunks, threads, 0, s>>>(x, cu, chunk_off, n_texts, T, H, partial);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    pool_finish_kernel<<<n_texts, 256, 0, s>>>(partial, cu, chunk_off, H, out);
+    pool_finish_kernel<<<n_texts, 256, 0, s>>>(partial, cu, chunk_off, n_chunks, H, out);
     return cudaGetLastError();
 }
 
@@ -546,7 +550,9 @@ cudaError_t launch_pool_l2(const float* x, const int32_t* cu, const int32_t* chu
 // these fixed-size device arrays, which every GPU that loads the library
 // holds until the process exits.  Host code may not use the arrays' names as
 // device addresses: the addresses come from cudaGetSymbolAddress, once per
-// device, on the first call made on that device.
+// device, on the first call made on that device, and are kept for the life of
+// the process -- so the entry point must not be used on a device after a
+// cudaDeviceReset there (the module, and with it the arrays, is reloaded).
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) int32_t g_noalloc_chunk_off[TEE_POOL_NOALLOC_MAX_TEXTS + 1];
 static __device__ __align__(256) float g_noalloc_partial[TEE_POOL_NOALLOC_MAX_PARTIAL];
@@ -561,6 +567,11 @@ float* g_noalloc_partial_ptr[kMaxDevices] = {};
 extern "C" int tee_pool_l2_noalloc(const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts,
                                    int hidden, float* d_out, void* stream) {
     if (!d_x || !d_cu || !h_cu || !d_out) return tee_set_global_error(TEE_EINVAL, "pool_l2_noalloc: NULL pointer");
+    // the kernels move rows of x and out as 16-byte vectors and read cu as int32
+    if ((reinterpret_cast<uintptr_t>(d_x) | reinterpret_cast<uintptr_t>(d_out)) & 15)
+        return tee_set_global_error(TEE_EINVAL, "pool_l2_noalloc: d_x and d_out must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(d_cu) & 3)
+        return tee_set_global_error(TEE_EINVAL, "pool_l2_noalloc: d_cu must be 4-byte aligned");
     if (n_texts < 1) return tee_set_global_error(TEE_EINVAL, "pool_l2_noalloc: n_texts must be >= 1");
     if (n_texts > TEE_POOL_NOALLOC_MAX_TEXTS)
         return tee_set_global_error(TEE_ETOOLONG, "pool_l2_noalloc: n_texts exceeds TEE_POOL_NOALLOC_MAX_TEXTS");
@@ -601,7 +612,8 @@ extern "C" int tee_pool_l2_noalloc(const float* d_x, const int32_t* d_cu, const 
     cudaStream_t s = (cudaStream_t)stream;
     pool_chunk_offsets_kernel<<<1, 1024, 0, s>>>(d_cu, n_texts, off_ptr);
     e = cudaGetLastError();
-    if (e == cudaSuccess) e = launch_pool_l2(d_x, d_cu, off_ptr, n_texts, (int)n_chunks, hidden, partial_ptr, d_out, s);
+    if (e == cudaSuccess) e = launch_pool_l2(d_x, d_cu, off_ptr, n_texts, (int)n_chunks, h_cu[n_texts], hidden, partial_ptr,
+                                              d_out, s);
     if (e != cudaSuccess) return tee_set_global_error(TEE_ECUDA, cudaGetErrorString(e));
     return TEE_OK;
 }

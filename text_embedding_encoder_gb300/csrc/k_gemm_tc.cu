@@ -440,7 +440,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // host side
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-int g_num_sms = 0;
 std::once_flag g_once;
 cudaError_t g_init_err = cudaSuccess;
 
@@ -453,10 +452,6 @@ void init_once() {
         return;
     }
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    int dev = 0;
-    cudaGetDevice(&dev);
-    e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) g_init_err = e;
 }
 
 // Output map [rows, cols] of 2- or 4-byte elements, boxes of 32 rows x 128 bytes, 128B swizzle.
@@ -485,9 +480,12 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, int K, int box_rows) 
 
 template <int BN, int EPI, int MODE>
 cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const Params& p, int units,
-                     cudaStream_t s) {
+                     int dev, int num_sms, cudaStream_t s) {
     constexpr bool CL = MODE != MODE_SINGLE;
-    static int max_grid = 0;   // CTAs that can be resident at once (a multiple of 2 when clustered)
+    // per device: CTAs that can be resident at once (a multiple of 2 when
+    // clustered), set together with the kernel's shared-memory attribute
+    static std::mutex mu;
+    static int max_grid_of[TEE_MAX_DEVICES] = {};
     constexpr uint32_t smem = Smem<BN, EPI, MODE>::TOTAL;
     auto kernel = gemm_tc_kernel<BN, EPI, MODE>;
     cudaLaunchConfig_t cfg = {};
@@ -503,18 +501,23 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (!max_grid) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        if (CL) {
-            int clusters = 0;
-            cfg.gridDim = dim3(2 * g_num_sms);
-            e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    int max_grid;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!max_grid_of[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            max_grid = 2 * (clusters > 0 ? clusters : 1);
-        } else {
-            max_grid = g_num_sms;
+            if (CL) {
+                int clusters = 0;
+                cfg.gridDim = dim3(2 * num_sms);
+                e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+                if (e != cudaSuccess) return e;
+                max_grid_of[dev] = 2 * (clusters > 0 ? clusters : 1);
+            } else {
+                max_grid_of[dev] = num_sms;
+            }
         }
+        max_grid = max_grid_of[dev];
     }
     const int per_unit = CL ? 2 : 1;
     const int grid = units * per_unit < max_grid ? units * per_unit : max_grid;
@@ -575,9 +578,12 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.W) | reinterpret_cast<uintptr_t>(a.C)) & 15)
         return cudaErrorMisalignedAddress;
     if (a.M == 0) return cudaSuccess;
+    int dev = 0, num_sms = 0;
+    cudaError_t de = tee_current_device(&dev, &num_sms);
+    if (de != cudaSuccess) return de;
     const int num_m = (a.M + BM - 1) / BM;
     int BN = 128, pair = 0;
-    gemm_tc_choose_tiles(a.M, a.N, a.K, a.epi, g_num_sms, &BN, &pair);
+    gemm_tc_choose_tiles(a.M, a.N, a.K, a.epi, num_sms, &BN, &pair);
     const int mode = pair ? MODE_PAIR : MODE_SINGLE;
     const int b_rows = mode == MODE_SINGLE ? BN : BN / 2;
     CUtensorMap ma, mb, mc_map;
@@ -591,8 +597,8 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status};
     const int units = (mode != MODE_SINGLE ? (num_m + 1) / 2 : num_m) * (a.N / BN);
 #define TEE_GEMM_DISPATCH(BN_, EPI_)                                                                  \
-    return mode == MODE_PAIR ? launch_t<BN_, EPI_, MODE_PAIR>(ma, mb, mc_map, p, units, s)           \
-                             : launch_t<BN_, EPI_, MODE_SINGLE>(ma, mb, mc_map, p, units, s)
+    return mode == MODE_PAIR ? launch_t<BN_, EPI_, MODE_PAIR>(ma, mb, mc_map, p, units, dev, num_sms, s)  \
+                             : launch_t<BN_, EPI_, MODE_SINGLE>(ma, mb, mc_map, p, units, dev, num_sms, s)
     if (a.epi == GEMM_EPI_ADD_F32 && BN == 256) TEE_GEMM_DISPATCH(256, GEMM_EPI_ADD_F32);
     if (a.epi == GEMM_EPI_ADD_F32 && BN == 192) TEE_GEMM_DISPATCH(192, GEMM_EPI_ADD_F32);
     if (BN == 256) {

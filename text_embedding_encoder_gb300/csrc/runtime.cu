@@ -17,6 +17,7 @@
 
 #include <algorithm>
 #include <initializer_list>
+#include <mutex>
 #include <new>
 
 namespace {
@@ -241,6 +242,21 @@ int prepare_attention_items(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cuda
 }  // namespace
 
 int tee_set_global_error(int code, const char* msg) { return fail(nullptr, code, "%s", msg); }
+
+cudaError_t tee_current_device(int* dev, int* num_sms) {
+    static std::mutex mu;
+    static int sms[TEE_MAX_DEVICES] = {};
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (*dev < 0 || *dev >= TEE_MAX_DEVICES) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!sms[*dev]) {
+        e = cudaDeviceGetAttribute(&sms[*dev], cudaDevAttrMultiProcessorCount, *dev);
+        if (e != cudaSuccess) return e;
+    }
+    *num_sms = sms[*dev];
+    return cudaSuccess;
+}
 
 // ---------------------------------------------------------------------------
 // profiling
@@ -503,6 +519,26 @@ int check_dev(tee_ctx* ctx, long long n, int align, std::initializer_list<const 
     return TEE_OK;
 }
 
+// Makes the context's device current for one entry point and restores the
+// caller's current device on the way out, so a process may interleave
+// contexts on several devices.
+struct DeviceScope {
+    int prev = -1;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceScope(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) err = cudaSetDevice(dev);
+    }
+    ~DeviceScope() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+#define ON_DEVICE(ctx)                                                            \
+    DeviceScope _dscope((ctx)->device);                                           \
+    if (_dscope.err != cudaSuccess) return cuda_fail((ctx), _dscope.err, "cudaSetDevice")
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -524,9 +560,10 @@ int tee_create(const tee_config* cfg, int device, tee_ctx** out) {
         tee_destroy(ctx);
         return code;
     };
-    cudaError_t e = cudaSetDevice(device);
-    if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaSetDevice"));
+    DeviceScope dscope(device);
+    if (dscope.err != cudaSuccess) return bail(cuda_fail(ctx, dscope.err, "cudaSetDevice"));
     ctx->ws_bytes = carve_workspace(ctx, nullptr);
+    cudaError_t e;
     e = cudaMalloc(&ctx->ws_arena, ctx->ws_bytes);
     if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaMalloc(workspace)"));
     carve_workspace(ctx, ctx->ws_arena);
@@ -552,7 +589,7 @@ int tee_load_weights(tee_ctx* ctx, const tee_weights* w) {
             return fail(ctx, TEE_EINVAL, "layer %d has a NULL weight pointer", l);
     if ((g.emb_norm && !w->ln_emb) || (g.final_norm && !w->ln_final) || (g.proj_dim && !w->w_proj))
         return fail(ctx, TEE_EINVAL, "an enabled optional weight (ln_emb, ln_final, w_proj) is NULL");
-    CK(cudaSetDevice(ctx->device));
+    ON_DEVICE(ctx);
     ctx->loaded = false;
     if (ctx->weight_arena) {
         CK(cudaFree(ctx->weight_arena));
@@ -640,7 +677,7 @@ int tee_encode(tee_ctx* ctx, const int32_t* token_ids, const int32_t* cu_seqlens
         if (token_ids[t] < 0 || token_ids[t] >= ctx->cfg.vocab)
             return fail(ctx, TEE_EINVAL, "token id %d at position %d is outside [0, %d)", token_ids[t], t,
                         ctx->cfg.vocab);
-    CK(cudaSetDevice(ctx->device));
+    ON_DEVICE(ctx);
     cudaStream_t s = ctx->stream;
     CK(cudaMemcpyAsync(ctx->d_ids, token_ids, (size_t)T * 4, cudaMemcpyHostToDevice, s));
     CK(cudaMemcpyAsync(ctx->d_cu, cu_seqlens, (size_t)(n_texts + 1) * 4, cudaMemcpyHostToDevice, s));
@@ -658,7 +695,7 @@ int tee_encode_device(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, c
     if (reinterpret_cast<uintptr_t>(d_out) & 15) return fail(ctx, TEE_EINVAL, "d_out must be 16-byte aligned");
     int T = 0;
     if ((rc = check_cu(ctx, h_cu, n_texts, &T))) return rc;
-    CK(cudaSetDevice(ctx->device));
+    ON_DEVICE(ctx);
     return run_pass(ctx, d_ids, d_cu, h_cu, n_texts, T, d_out, (cudaStream_t)stream);
 }
 
@@ -672,7 +709,7 @@ int tee_encode_tokens(tee_ctx* ctx, const int32_t* token_ids, const int32_t* cu_
         if (token_ids[t] < 0 || token_ids[t] >= ctx->cfg.vocab)
             return fail(ctx, TEE_EINVAL, "token id %d at position %d is outside [0, %d)", token_ids[t], t,
                         ctx->cfg.vocab);
-    CK(cudaSetDevice(ctx->device));
+    ON_DEVICE(ctx);
     const size_t D = ctx->cfg.proj_dim ? ctx->cfg.proj_dim : ctx->cfg.hidden;
     if (!ctx->tok_out) CK(cudaMalloc(&ctx->tok_out, (size_t)ctx->cfg.max_tokens * D * sizeof(float)));
     cudaStream_t s = ctx->stream;
@@ -692,7 +729,7 @@ int tee_encode_tokens_device(tee_ctx* ctx, const int32_t* d_ids, const int32_t* 
     if (reinterpret_cast<uintptr_t>(d_out) & 15) return fail(ctx, TEE_EINVAL, "d_out must be 16-byte aligned");
     int T = 0;
     if ((rc = check_cu(ctx, h_cu, n_texts, &T))) return rc;
-    CK(cudaSetDevice(ctx->device));
+    ON_DEVICE(ctx);
     return run_tokens(ctx, d_ids, d_cu, h_cu, n_texts, T, d_out, (cudaStream_t)stream);
 }
 
@@ -700,7 +737,7 @@ const char* tee_last_error(const tee_ctx* ctx) { return ctx ? ctx->err.c_str() :
 
 void tee_destroy(tee_ctx* ctx) {
     if (!ctx) return;
-    cudaSetDevice(ctx->device);
+    DeviceScope dscope(ctx->device);
     if (ctx->stream) cudaStreamSynchronize(ctx->stream);
     for (auto& sl : ctx->prof_slots) {
         cudaEventDestroy(sl.start);
@@ -756,7 +793,7 @@ int tee_profile_enable(tee_ctx* ctx, int on) {
 
 int tee_profile_read(tee_ctx* ctx, tee_kernel_stat* stats) {
     if (!ctx || !stats) return TEE_EINVAL;
-    CK(cudaSetDevice(ctx->device));
+    ON_DEVICE(ctx);
     for (size_t i = 0; i < ctx->prof_used; ++i) {
         ProfileSlot& sl = ctx->prof_slots[i];
         CK(cudaEventSynchronize(sl.stop));
@@ -780,6 +817,7 @@ int tee_op_embed(tee_ctx* ctx, const int32_t* d_ids, int T, float* d_x, void* st
     if (rc) return rc;
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
     if ((rc = check_dev(ctx, T, 16, {d_x})) || (rc = check_dev(ctx, T, 4, {d_ids}))) return rc;
+    ON_DEVICE(ctx);
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_EMBED, 0, 0,
            launch_embed(ctx->emb, act_is_bf16(ctx), d_ids, T, ctx->cfg.hidden, ctx->cfg.vocab, d_x, ctx->d_status, s));
@@ -791,6 +829,7 @@ int tee_op_positions(tee_ctx* ctx, const int32_t* d_cu, const int32_t* h_cu, int
     if (!ctx) return TEE_EINVAL;
     int T = 0, rc = check_cu(ctx, h_cu, n_texts, &T);
     if (rc || (rc = check_dev(ctx, T, 4, {d_cu, d_pos}))) return rc;
+    ON_DEVICE(ctx);
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_EMBED, 0, 0, launch_positions(d_cu, n_texts, T, d_pos, s));
     return TEE_OK;
@@ -802,6 +841,7 @@ int tee_op_layernorm(tee_ctx* ctx, int layer, int which, const float* d_x, void*
     if (which != TEE_LN_ATTN && which != TEE_LN_MLP) return fail(ctx, TEE_EINVAL, "bad LayerNorm selector");
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
     if ((rc = check_dev(ctx, T, 16, {d_x, d_y}))) return rc;
+    ON_DEVICE(ctx);
     return step_layernorm(ctx, layer, which, d_x, d_y, T, (cudaStream_t)stream);
 }
 
@@ -810,6 +850,7 @@ int tee_op_qkv(tee_ctx* ctx, int layer, const void* d_y, const int32_t* d_pos, v
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
     if ((rc = check_dev(ctx, T, 16, {d_y, d_qkv})) || (rc = check_dev(ctx, T, 4, {d_pos}))) return rc;
+    ON_DEVICE(ctx);
     return step_qkv(ctx, layer, d_y, d_pos, d_qkv, T, (cudaStream_t)stream);
 }
 
@@ -820,6 +861,7 @@ int tee_op_attention(tee_ctx* ctx, int layer, const void* d_qkv, const int32_t* 
     int T = 0;
     if ((rc = check_cu(ctx, h_cu, n_texts, &T))) return rc;
     if ((rc = check_dev(ctx, T, 16, {d_qkv, d_o})) || (rc = check_dev(ctx, T, 4, {d_cu}))) return rc;
+    ON_DEVICE(ctx);
     if (ctx->cfg.dtype == TEE_BF16 && (rc = prepare_attention_items(ctx, h_cu, n_texts, (cudaStream_t)stream)))
         return rc;
     return step_attention(ctx, layer, d_qkv, d_cu, h_cu, n_texts, T, d_o, (cudaStream_t)stream);
@@ -830,6 +872,7 @@ int tee_op_out_proj(tee_ctx* ctx, int layer, const void* d_o, float* d_x, int T,
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
     if ((rc = check_dev(ctx, T, 16, {d_o, d_x}))) return rc;
+    ON_DEVICE(ctx);
     return step_linear(ctx, layer, TEE_W_OUT, d_o, d_x, T, 1, GEMM_EPI_ADD_F32, nullptr, (cudaStream_t)stream);
 }
 
@@ -838,6 +881,7 @@ int tee_op_ffn_in(tee_ctx* ctx, int layer, const void* d_y, void* d_z, int T, vo
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
     if ((rc = check_dev(ctx, T, 16, {d_y, d_z}))) return rc;
+    ON_DEVICE(ctx);
     return step_ffn_in(ctx, layer, d_y, d_z, T, (cudaStream_t)stream);
 }
 
@@ -846,6 +890,7 @@ int tee_op_ffn_out(tee_ctx* ctx, int layer, const void* d_z, float* d_x, int T, 
     if (rc || (rc = check_layer(ctx, layer))) return rc;
     if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
     if ((rc = check_dev(ctx, T, 16, {d_z, d_x}))) return rc;
+    ON_DEVICE(ctx);
     return step_linear(ctx, layer, TEE_W_FFN_OUT, d_z, d_x, T, 1, GEMM_EPI_ADD_F32, nullptr, (cudaStream_t)stream);
 }
 
@@ -865,6 +910,7 @@ int tee_op_gemm_bf16(tee_ctx* ctx, const void* d_a, const void* d_w, void* d_c, 
     a.K = K;
     a.epi = epilogue == 0 ? GEMM_EPI_STORE_BF16 : GEMM_EPI_ADD_F32;
     a.status = ctx->d_status;
+    ON_DEVICE(ctx);
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_GEMM, 2.0 * M * N * K, 0, launch_gemm_tc(a, s));
     return TEE_OK;
@@ -875,6 +921,7 @@ int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const in
     if (!ctx) return TEE_EINVAL;
     int T = 0, rc = check_cu(ctx, h_cu, n_texts, &T);
     if (rc || (rc = check_dev(ctx, T, 16, {d_x, d_out})) || (rc = check_dev(ctx, T, 4, {d_cu}))) return rc;
+    ON_DEVICE(ctx);
     return step_pool(ctx, d_x, d_cu, h_cu, n_texts, T, d_out, (cudaStream_t)stream);
 }
 
@@ -883,6 +930,7 @@ int tee_op_quant_rows7(tee_ctx* ctx, const float* d_x, int M, int K, int8_t* d_q
     if (M < 0 || K < 1) return fail(ctx, TEE_EINVAL, "bad M/K");
     int rc = check_dev(ctx, M, 16, {d_x, d_q});
     if (rc || (rc = check_dev(ctx, M, 4, {d_s}))) return rc;
+    ON_DEVICE(ctx);
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_QUANT, 0, 0, launch_quant_rows7(d_x, M, K, d_q, d_s, s));
     return TEE_OK;
@@ -898,6 +946,7 @@ int tee_op_w8a8_partials(tee_ctx* ctx, int layer, int which, const int8_t* d_q, 
     if (M < 0) return fail(ctx, TEE_EINVAL, "bad M");
     if ((rc = check_dev(ctx, M, 16, {d_q})) || (rc = check_dev(ctx, M, 4, {d_partials}))) return rc;
     const LayerWeights& L = ctx->layers[layer];
+    ON_DEVICE(ctx);
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_GEMM, 0, 0,
            launch_gemm_w8a8(d_q, nullptr, (const int8_t*)L.w[which], L.wd[which], nullptr, d_partials, M, N, K, 0,
@@ -912,7 +961,7 @@ int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d
     int N, K;
     if (wshape(ctx->cfg, which, &N, &K)) return fail(ctx, TEE_EINVAL, "bad projection selector");
     if (!h_q || !h_d) return fail(ctx, TEE_EINVAL, "NULL output");
-    CK(cudaSetDevice(ctx->device));
+    ON_DEVICE(ctx);
     if (ctx->cfg.dtype == TEE_W4A8) {   // widen the packed nibbles: element 2i low, 2i + 1 high
         std::vector<uint8_t> packed((size_t)N * K / 2);
         CK(cudaMemcpy(packed.data(), ctx->layers[layer].w[which], packed.size(), cudaMemcpyDeviceToHost));
@@ -932,14 +981,14 @@ int tee_selftest_wait_timeout(tee_ctx* ctx, long long wait_cycles, void* stream)
     if (!ctx) return TEE_EINVAL;
     if (wait_cycles < 1000) wait_cycles = 1000;
     if (wait_cycles > 10000000000LL) wait_cycles = 10000000000LL;
-    CK(cudaSetDevice(ctx->device));
+    ON_DEVICE(ctx);
     CK(launch_selftest_wait(wait_cycles, ctx->d_status, (cudaStream_t)stream));
     return TEE_OK;
 }
 
 int tee_device_status(tee_ctx* ctx) {
     if (!ctx) return TEE_EINVAL;
-    CK(cudaSetDevice(ctx->device));
+    ON_DEVICE(ctx);
     unsigned int st = 0;
     CK(cudaDeviceSynchronize());
     CK(cudaMemcpy(&st, ctx->d_status, 4, cudaMemcpyDeviceToHost));

@@ -122,6 +122,14 @@ inline int layer_is_global(const tee_ctx* c, int l) { return (l % c->cfg.global_
 // Record the message returned by tee_last_error(NULL) for context-free calls; returns `code`.
 int tee_set_global_error(int code, const char* msg);
 
+// One process may drive several devices (one context each), so everything the
+// launchers cache about a device -- its SM count, the kernels' shared-memory
+// attributes, occupancy-derived grid sizes -- is kept per device index, under
+// a lock.  Device indices must be below TEE_MAX_DEVICES.
+#define TEE_MAX_DEVICES 64
+// The current device's index and SM count (looked up once per device).
+cudaError_t tee_current_device(int* dev, int* num_sms);
+
 // Profiling brackets: record events around one launch when profiling is on.
 int prof_begin(tee_ctx* c, cudaStream_t s, int kclass, double flops, double bytes);
 void prof_end(tee_ctx* c, cudaStream_t s, int slot);
@@ -141,7 +149,7 @@ cudaError_t launch_geglu(const void* u, void* z, bool bf16_act, int T, int I, cu
 // (float [n_chunks * H]), then per text the ordered sum, mean and scaling.
 #define POOL_CHUNK 64
 #define POOL_CHUNK_FUSED 64   // rows per block of the single-launch pool (launch_pool_l2_fused)
-cudaError_t launch_pool_l2(const float* x, const int32_t* cu, const int32_t* chunk_off, int n_texts, int n_chunks,
+cudaError_t launch_pool_l2(const float* x, const int32_t* cu, const int32_t* chunk_off, int n_texts, int n_chunks, int T,
                            int H, float* partial, float* out, cudaStream_t s);
 // The same in one launch: the last chunk of each text to finish combines that
 // text's partials; counters (unsigned [n_texts], all zero) are left zero.

@@ -76,3 +76,31 @@ def gather_embeddings(local_out, texts, n_texts: int, width: int, group=None):
         keep = i >= 0
         result[i[keep].numpy()] = o[keep].numpy()
     return result
+
+
+def encode_sharded(encode_fn, ids, cu_seqlens, width: int, group=None):
+    """Encode a packed batch over all ranks of a process group, one GPU per rank.
+
+    Every rank calls this with the same host batch (ids int32[T], cu_seqlens
+    int32[n + 1]).  The texts are partitioned by `partition_texts`, this rank
+    encodes its own sub-batch with `encode_fn(sub_ids, sub_cu) -> [n_r, width]`
+    (one row per text: for the library, ``Encoder.encode`` of a context on this
+    rank's GPU), and the vectors are all-gathered back into input order.  A rank that
+    receives no text does not call `encode_fn`.  Every rank returns the full
+    [n, width] float32 result.  There is no exchange during the pass itself:
+    texts are independent (positions restart per text and attention stays
+    inside it).
+    """
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    rank = dist.get_rank(group)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    n = cu.shape[0] - 1
+    texts = partition_texts(cu, world)[rank]
+    if len(texts):
+        sub_ids, sub_cu = shard_batch(ids, cu, texts)
+        local = np.asarray(encode_fn(sub_ids, sub_cu), dtype=np.float32).reshape(len(texts), width)
+    else:
+        local = np.zeros((0, width), dtype=np.float32)
+    return gather_embeddings(local, texts, n, width, group=group)
