@@ -46,7 +46,6 @@ from .encoder import (  # noqa: F401
     encode_packed,
     encode_text_tokens,
     encode_packed_tokens,
-    cosine,
 )
 from .precision import round_to_bf16  # noqa: F401
 from .w8a8 import (  # noqa: F401

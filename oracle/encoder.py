@@ -137,12 +137,6 @@ def layer_is_global(layer: int, shape) -> bool:
     return layer % shape.global_every == 0
 
 
-def cosine(a, b) -> float:
-    a = np.asarray(a, dtype=np.float64).ravel()
-    b = np.asarray(b, dtype=np.float64).ravel()
-    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
-
-
 # --------------------------------------------------------------------------
 # The encoder
 # --------------------------------------------------------------------------

@@ -1,6 +1,6 @@
 """Time each step of the pass on its own, through the C ABI (per-step entry points).
 
-    python -m text_embedding_encoder_gb300.profile_steps [--tokens 32768] [--reps 10] [--only STEP]
+    python profile_steps.py [--tokens 32768] [--reps 10] [--only STEP]
 
 Builds a 310m-shape bf16 context with seeded random weights, stages one
 sweep batch of the given token budget, and times every step (LayerNorm, the
@@ -12,11 +12,14 @@ from __future__ import annotations
 
 import argparse
 import json
+import os
+import sys
 
 import numpy as np
 import torch
 
-from . import binding, synth
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+from text_embedding_encoder_gb300 import binding, synth  # noqa: E402
 
 STEPS = ["embed", "layernorm", "qkv", "attn_global", "attn_window", "out_proj", "ffn_in", "ffn_out", "pool"]
 PLAIN = ["plain_qkv", "plain_out_proj", "plain_ffn_in", "plain_ffn_out"]
