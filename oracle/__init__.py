@@ -52,6 +52,7 @@ from .w8a8 import (  # noqa: F401
     quantize_rows7,
     quantize_weight_blocks,
     quantize_weight_blocks4,
+    quantize_weight_blocks6,
     int_block_partials,
     w8a8_linear,
 )

@@ -150,6 +150,7 @@ class OracleModel:
     variant "w8a8": projections go through the integer procedure of
                     ``oracle.w8a8``; embedding and gains stay fp32.
     variant "w4a8": the same with 4-bit weight blocks (codes in [-7, 7]).
+    variant "w6a8": the same with 6-bit weight blocks (codes in [-31, 31]).
 
     ``weights`` needs attributes tok_emb, ln_attn, wqkv, wo, ln_mlp, wi,
     wo_ffn (lists per layer), in the layouts documented by the C header, and
@@ -159,7 +160,7 @@ class OracleModel:
     """
 
     def __init__(self, weights, shape, variant: str = "fp32"):
-        if variant not in ("fp32", "bf16", "w8a8", "w4a8"):
+        if variant not in ("fp32", "bf16", "w8a8", "w4a8", "w6a8"):
             raise ValueError(variant)
         self.shape = shape
         self.variant = variant
@@ -172,9 +173,10 @@ class OracleModel:
         self.ln_final = wide(weights.ln_final) if getattr(shape, "final_norm", False) else None
         names = ("wqkv", "wo", "wi", "wo_ffn")
         proj = [weights.w_proj] if getattr(shape, "proj_dim", 0) else []
-        if variant in ("w8a8", "w4a8"):
-            from .w8a8 import quantize_weight_blocks, quantize_weight_blocks4
-            quant = quantize_weight_blocks if variant == "w8a8" else quantize_weight_blocks4
+        if variant in ("w8a8", "w4a8", "w6a8"):
+            from .w8a8 import quantize_weight_blocks, quantize_weight_blocks4, quantize_weight_blocks6
+            quant = {"w8a8": quantize_weight_blocks, "w4a8": quantize_weight_blocks4,
+                     "w6a8": quantize_weight_blocks6}[variant]
             self.q = {name: [quant(np.asarray(w, np.float32)) for w in getattr(weights, name)] for name in names}
             self.q["w_proj"] = [quant(np.asarray(w, np.float32)) for w in proj]
         else:
@@ -183,7 +185,7 @@ class OracleModel:
 
     def linear(self, name: str, layer: int, x) -> np.ndarray:
         """y = x W^T (no bias: the page mentions none on any projection)."""
-        if self.variant in ("w8a8", "w4a8"):
+        if self.variant in ("w8a8", "w4a8", "w6a8"):
             from .w8a8 import w8a8_linear
             qw, d = self.q[name][layer]
             return w8a8_linear(x, qw, d)

@@ -13,10 +13,12 @@ Readings (the page fixes no formulas):
   y[m, n] = s_m * sum_b d[n, b] * I[m, n, b].
 
 The -q4 path of the same section repacks the file's 4- and 6-bit block formats
-unchanged; the page names those formats but does not define them.  Reading: a
-4-bit analogue of the 8-bit blocks defined here -- blocks of 32 K elements,
-d = max|w| / 7, q = clamp(rint(w / d), -7, 7) -- with the same 7-bit
-activations and the same exact block sums (variant "w4a8").
+unchanged; the page names those formats but does not define them.  Reading:
+4- and 6-bit analogues of the 8-bit blocks defined here -- blocks of 32 K
+elements, d = max|w| / L, q = clamp(rint(w / d), -L, L) with L = 7 (variant
+"w4a8") or L = 31 (variant "w6a8") -- with the same 7-bit activations and the
+same exact block sums.  A file of the -q4 kind mixes the two widths; each
+variant here uses one width for every projection.
 
 The quantisers decide integers from floating point, so they compute in fp32
 (IEEE division, round-half-even), the precision of the device kernels; the
@@ -27,6 +29,7 @@ import numpy as np
 ACT_LEVELS = 63
 WEIGHT_LEVELS = 127
 WEIGHT_LEVELS_4 = 7
+WEIGHT_LEVELS_6 = 31
 BLOCK = 32
 
 
@@ -47,7 +50,7 @@ def quantize_rows7(x):
 
 def quantize_weight_blocks(w, levels: int = WEIGHT_LEVELS):
     """Blockwise quantisation of a weight matrix [N, K], K a multiple of 32,
-    to integers in [-levels, levels] (127: int8 blocks; 7: 4-bit blocks).
+    to integers in [-levels, levels] (127: int8 blocks; 31: 6-bit; 7: 4-bit).
 
     Returns (q int8[N, K], d float32[N, K/32]).
     """
@@ -67,6 +70,11 @@ def quantize_weight_blocks(w, levels: int = WEIGHT_LEVELS):
 def quantize_weight_blocks4(w):
     """4-bit blocks (the -q4 reading): codes in [-7, 7], d = max|w| / 7 per block of 32."""
     return quantize_weight_blocks(w, WEIGHT_LEVELS_4)
+
+
+def quantize_weight_blocks6(w):
+    """6-bit blocks (the -q4 reading): codes in [-31, 31], d = max|w| / 31 per block of 32."""
+    return quantize_weight_blocks(w, WEIGHT_LEVELS_6)
 
 
 def _block_product(qa, qw, b) -> np.ndarray:

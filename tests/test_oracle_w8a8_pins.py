@@ -84,6 +84,40 @@ def test_quantize_weight_blocks4_range_and_error():
     assert np.all(err <= d[:, :, None] / 2 * (1 + 1e-6))
 
 
+def test_quantize_weight_blocks6_hand_cases():
+    # 6-bit blocks: d = max|w| / 31, codes rint(w / d) clamped to +-31, ties to even
+    w = np.zeros((2, 64), np.float32)
+    w[0, :32] = np.linspace(-31, 31, 32)   # d = 1: codes are the rounded values themselves
+    w[0, 32] = 0.5        # tie -> 0 (even)
+    w[0, 33] = 1.5        # tie -> 2 (even)
+    w[0, 34] = 14.5       # tie -> 14 (even)
+    w[0, 35] = 31.0       # the block maximum: d = 1
+    w[0, 36] = -30.5      # tie -> -30 (even)
+    w[1, 40] = -3.0       # alone in its block: d = 3/31, code -31
+    q, d = oracle.quantize_weight_blocks6(w)
+    assert d[0, 0] == 1.0 and d[0, 1] == 1.0 and d[1, 0] == 0.0
+    np.testing.assert_array_equal(q[0, :32], np.rint(np.linspace(-31, 31, 32)).astype(np.int8))
+    assert q[0, 32] == 0 and q[0, 33] == 2 and q[0, 34] == 14 and q[0, 35] == 31 and q[0, 36] == -30
+    np.testing.assert_array_equal(q[1, :32], 0)                            # an all-zero block
+    assert q[1, 40] == -31 and d[1, 1] == np.float32(3.0) / np.float32(31.0)
+
+
+def test_quantize_weight_blocks6_range_and_error():
+    rng = np.random.default_rng(6)
+    w = (rng.standard_normal((16, 128)) * rng.uniform(0.001, 1.0, (16, 1))).astype(np.float32)
+    q, d = oracle.quantize_weight_blocks6(w)
+    assert q.min() >= -31 and q.max() <= 31
+    # every block reaches +-31 at its maximum, and the rounding error is at most d / 2
+    np.testing.assert_array_equal(np.abs(q.reshape(16, 4, 32)).max(axis=2), 31)
+    err = np.abs(w.reshape(16, 4, 32) - q.reshape(16, 4, 32) * d[:, :, None])
+    assert np.all(err <= d[:, :, None] / 2 * (1 + 1e-6))
+    # finer than 4-bit blocks, coarser than 8-bit ones on the same weights
+    e4 = np.abs(w - oracle.quantize_weight_blocks4(w)[0] * np.repeat(oracle.quantize_weight_blocks4(w)[1], 32, 1))
+    e8 = np.abs(w - oracle.quantize_weight_blocks(w)[0] * np.repeat(oracle.quantize_weight_blocks(w)[1], 32, 1))
+    e6 = np.abs(w - q * np.repeat(d, 32, 1))
+    assert e8.mean() < e6.mean() < e4.mean()
+
+
 def test_int_block_partials_against_integer_loops():
     rng = np.random.default_rng(1)
     M, N, K = 5, 4, 96
@@ -160,3 +194,21 @@ def test_w8a8_model_uses_integer_path():
     ref = s[:, None].astype(np.float64) * np.einsum("mnb,nb->mn", w8a8.int_block_partials(qa, qw).astype(np.float64),
                                                     d.astype(np.float64))
     np.testing.assert_allclose(m.linear("wqkv", 1, xin), ref, rtol=1e-13, atol=1e-15)
+
+
+def test_w6a8_model_uses_six_bit_codes():
+    from text_embedding_encoder_gb300 import synth
+    shape = synth.Shape(n_layers=2, hidden=64, n_heads=1, head_dim=64, intermediate=96, vocab=50)
+    w = synth.make_weights(shape, seed=3)
+    m = oracle.OracleModel(w, shape, "w6a8")
+    for name in ("wqkv", "wo", "wi", "wo_ffn"):
+        q, d = m.q[name][1]
+        assert np.abs(q).max() == 31
+        np.testing.assert_array_equal(q, w8a8.quantize_weight_blocks6(getattr(w, name)[1])[0])
+    ids, cu = synth.make_batch([9, 4], shape.vocab, seed=4)
+    e6 = oracle.encode_packed(ids, cu, m)
+    e4 = oracle.encode_packed(ids, cu, oracle.OracleModel(w, shape, "w4a8"))
+    ef = oracle.encode_packed(ids, cu, oracle.OracleModel(w, shape, "fp32"))
+    np.testing.assert_allclose(np.linalg.norm(e6, axis=1), 1.0, atol=1e-14)
+    # finer weights than the 4-bit blocks: closer to the float result
+    assert np.all((e6 * ef).sum(axis=1) > (e4 * ef).sum(axis=1))
