@@ -53,6 +53,9 @@ extern "C" {
 #define TEE_W8A8  2   /* int8 weight blocks x 7-bit per-row activations, exact int32 block sums */
 #define TEE_W4A8  3   /* 4-bit weight blocks (codes in [-7, 7], two per byte, one fp32 scale per 32) x 7-bit
                          per-row activations, exact int32 block sums (this library's reading of the page's -q4) */
+#define TEE_W6A8  4   /* 6-bit weight blocks (codes in [-31, 31], four per three bytes, one fp32 scale per 32)
+                         x 7-bit per-row activations, exact int32 block sums (the page's -q4 repacks 4- and
+                         6-bit blocks; this is this library's 6-bit block) */
 
 /*
  * Encoder shape and run limits.  Readings where the page is silent:
@@ -74,7 +77,7 @@ typedef struct tee_config {
     float rope_base_global;  /* 160000                                               */
     float rope_base_local;   /* 10000                                                */
     float ln_eps;            /* 1e-5                                                 */
-    int   dtype;             /* TEE_F32 | TEE_BF16 | TEE_W8A8 | TEE_W4A8             */
+    int   dtype;             /* TEE_F32 | TEE_BF16 | TEE_W8A8 | TEE_W6A8 | TEE_W4A8  */
     int   max_tokens;        /* capacity of one pass (sum of text lengths), >= 1     */
     int   max_texts;         /* capacity of one pass (number of texts), >= 1         */
     /* optional parts, 0 = off (the page's encoder) */
@@ -123,8 +126,9 @@ int tee_create(const tee_config* cfg, int device, tee_ctx** out);
 /*
  * Copy the host weights to the device and convert them to the context's
  * storage format (fp32, bf16 round-to-nearest-even, or int8 blocks of 32
- * with one fp32 scale each for TEE_W8A8, 4-bit blocks of 32 packed two codes per
- * byte with one fp32 scale each for TEE_W4A8).  May be called again to replace
+ * with one fp32 scale each for TEE_W8A8, 6-bit blocks of 32 packed four codes per
+ * three bytes with one fp32 scale each for TEE_W6A8, 4-bit blocks of 32 packed two
+ * codes per byte with one fp32 scale each for TEE_W4A8).  May be called again to replace
  * the weights.  Synchronous.  Errors: TEE_EINVAL (null pointers), TEE_ENOMEM,
  * TEE_ECUDA.
  */

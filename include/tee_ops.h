@@ -8,7 +8,8 @@
  * runs exactly these steps in this order.
  *
  * Activation buffers use the context's activation type ACT:
- *   TEE_F32, TEE_W8A8 and TEE_W4A8 contexts: float;  TEE_BF16 contexts: bfloat16
+ *   TEE_F32 and the integer-path (TEE_W8A8, TEE_W6A8, TEE_W4A8) contexts: float;
+ *   TEE_BF16 contexts: bfloat16
  *   (uint16 bit patterns).  The residual stream x is always float.
  * Shapes: T = rows (tokens), H = hidden, I = intermediate, row-major.
  * Return codes as in tee.h.  Buffers are borrowed for the duration of the
@@ -128,7 +129,7 @@ int tee_op_pool_l2(tee_ctx* ctx, const float* d_x, const int32_t* d_cu, const in
 int tee_pool_l2_noalloc(const float* d_x, const int32_t* d_cu, const int32_t* h_cu, int n_texts, int hidden,
                         float* d_out, void* stream);
 
-/* ---- integer-path pieces (TEE_W8A8 and TEE_W4A8 contexts) --------------- */
+/* ---- integer-path pieces (TEE_W8A8, TEE_W6A8 and TEE_W4A8 contexts) ------ */
 
 /* Per-row 7-bit quantiser: s[m] = max|x[m,:]| / 63 (IEEE fp32 division),
  * q = clamp(rint(x / s), -63, 63) (ties to even); zero rows give s = 0, q = 0.
@@ -142,7 +143,7 @@ int tee_op_w8a8_partials(tee_ctx* ctx, int layer, int which, const int8_t* d_q, 
                          void* stream);
 
 /* Copy the weight codes of projection `which` of `layer`, widened to int8[N*K]
- * (the 4-bit codes of a TEE_W4A8 context unpacked), and the block scales
+ * (the 6- and 4-bit codes of TEE_W6A8 / TEE_W4A8 contexts unpacked), and the block scales
  * float[N*K/32] to host buffers.  Synchronous. */
 int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d);
 

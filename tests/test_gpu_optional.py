@@ -1,8 +1,8 @@
 """The optional parts of the encoder on the GPU against the oracle: the
 embedding and final LayerNorms (the published ModernBERT layout), the
 per-token (multi-vector) output with and without a projection, in every
-arithmetic of the library, and the 4-bit weight-block integer path (W4A8),
-through the C ABI.
+arithmetic of the library, and the 4- and 6-bit weight-block integer paths
+(W4A8, W6A8), through the C ABI.
 
 Per-token vectors are held to the same bars as the pooled ones: fp32 max
 |GPU - oracle| <= 1e-4; bf16 cosine >= 0.9995 and max abs <= 3e-3 per vector;
@@ -96,21 +96,28 @@ def test_optional_weights_and_output_are_validated(lib):
 
 
 # ---------------------------------------------------------------------------
-# the 4-bit weight-block integer path
+# the 4- and 6-bit weight-block integer paths
 # ---------------------------------------------------------------------------
 
 ODD = synth.Shape(n_layers=2, hidden=384, n_heads=6, head_dim=64, intermediate=640, vocab=1000)
 
 
+QUANT = {"w4a8": oracle.quantize_weight_blocks4, "w6a8": oracle.quantize_weight_blocks6}
+
+
+@pytest.mark.parametrize("variant", ["w4a8", "w6a8"])
 @pytest.mark.parametrize("which,name", [(0, "wqkv"), (1, "wo"), (2, "wi"), (3, "wo_ffn")])
-def test_w4a8_codes_and_block_sums_bit_exact(lib, which, name):
+def test_packed_weight_codes_and_block_sums_bit_exact(lib, variant, which, name):
+    """4- and 6-bit weight blocks: the codes the library packed at load, read
+    back and widened, and the scales equal the oracle's quantiser; the exact
+    int32 block sums of the packed codes equal the oracle's integer sums."""
     shape = ODD
     w = synth.make_weights(shape, seed=21, outliers=True)
-    enc = make_encoder(shape, "w4a8", w, max_tokens=256, max_texts=8)
+    enc = make_encoder(shape, variant, w, max_tokens=256, max_texts=8)
     layer = 1
     Wf = getattr(w, name)[layer]
     N, K = Wf.shape
-    q_ref, d_ref = oracle.quantize_weight_blocks4(Wf)
+    q_ref, d_ref = QUANT[variant](Wf)
     q_gpu = np.empty((N, K), np.int8)
     d_gpu = np.empty((N, K // 32), np.float32)
     enc.check(enc.lib.tee_weight_codes(enc.ctx, layer, which, q_gpu.ctypes.data, d_gpu.ctypes.data))
@@ -126,17 +133,18 @@ def test_w4a8_codes_and_block_sums_bit_exact(lib, which, name):
     enc.close()
 
 
-def test_w4a8_encode_tiny_and_ruri(lib):
+@pytest.mark.parametrize("variant", ["w4a8", "w6a8"])
+def test_packed_weight_encode_tiny_and_ruri(lib, variant):
     for shape, lengths in ((synth.TINY, synth.TINY_LENGTHS), (synth.RURI_310M, synth.ACCURACY_LENGTHS)):
         w = synth.make_weights(shape, seed=0)
         ids, cu = synth.make_batch(lengths, shape.vocab, seed=0)
-        enc = make_encoder(shape, "w4a8", w, max_tokens=2048, max_texts=16)
+        enc = make_encoder(shape, variant, w, max_tokens=2048, max_texts=16)
         got = enc.encode(ids, cu).astype(np.float64)
-        want = oracle.encode_packed(ids, cu, oracle.OracleModel(w, shape, "w4a8"))
+        want = oracle.encode_packed(ids, cu, oracle.OracleModel(w, shape, variant))
         cos = _cos_rows(got, want)
         ref32 = oracle.encode_packed(ids, cu, oracle.OracleModel(w, shape, "fp32"))
-        print(f"{shape.n_layers}-layer w4a8: min cos vs W4A8 oracle {cos.min():.6f}; "
-              f"W4A8 oracle vs fp32 oracle {_cos_rows(want, ref32).min():.4f}")
+        print(f"{shape.n_layers}-layer {variant}: min cos vs {variant} oracle {cos.min():.6f}; "
+              f"{variant} oracle vs fp32 oracle {_cos_rows(want, ref32).min():.4f}")
         assert cos.min() >= BF16_COS, cos.min()
         assert enc.device_status() == 0
         enc.close()

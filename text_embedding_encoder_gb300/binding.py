@@ -22,8 +22,8 @@ TEE_ECUDA = -4
 TEE_ETOOLONG = -5
 TEE_ETIMEOUT = -6
 
-TEE_F32, TEE_BF16, TEE_W8A8, TEE_W4A8 = 0, 1, 2, 3
-DTYPES = {"fp32": TEE_F32, "bf16": TEE_BF16, "w8a8": TEE_W8A8, "w4a8": TEE_W4A8}
+TEE_F32, TEE_BF16, TEE_W8A8, TEE_W4A8, TEE_W6A8 = 0, 1, 2, 3, 4
+DTYPES = {"fp32": TEE_F32, "bf16": TEE_BF16, "w8a8": TEE_W8A8, "w4a8": TEE_W4A8, "w6a8": TEE_W6A8}
 
 TEE_LN_ATTN, TEE_LN_MLP = 0, 1
 TEE_W_QKV, TEE_W_OUT, TEE_W_FFN_IN, TEE_W_FFN_OUT = 0, 1, 2, 3
@@ -92,6 +92,11 @@ SIGNATURES = {
     "tee_selftest_wait_timeout": (_i, [_ctx, ctypes.c_longlong, _vp]),
     "tee_selftest_gelu": (_i, [_vp, _vp, ctypes.c_longlong, _vp]),
     "tee_plan_attention": (_i, [_vp, _i, _i, _i, _vp, _i]),
+    "tee_unigram_create": (_i, [ctypes.POINTER(ctypes.c_char_p), _vp, _i, _i, ctypes.c_float, _i, _i,
+                                ctypes.POINTER(_vp)]),
+    "tee_unigram_encode": (_i, [_vp, ctypes.c_char_p, _i, _vp, _i]),
+    "tee_unigram_destroy": (None, [_vp]),
+    "tee_similarity": (_i, [_vp, _i, _i, _vp]),
     "tee_plan_gemm": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
 }
 
@@ -252,3 +257,78 @@ class Encoder:
     def op(self, name, *args):
         return self.check(getattr(self.lib, name)(self.ctx, *[_ptr(a) if not isinstance(a, (int, float)) else a
                                                               for a in args]))
+
+
+# ---------------------------------------------------------------------------
+# host-side front end (tee_frontend.h)
+# ---------------------------------------------------------------------------
+
+class Unigram:
+    """Unigram max-score segmenter over a vocabulary (tee_unigram_*).
+
+    ``pieces``: list of str (piece i has id i); ``scores``: their scores;
+    ``unk_id`` / ``unk_score``: the unknown piece for uncovered characters;
+    ``bos_id`` / ``eos_id``: ids wrapped around every text (-1 for none).
+    """
+
+    def __init__(self, pieces, scores, unk_id: int, unk_score: float, bos_id: int = -1, eos_id: int = -1):
+        self.lib = load()
+        enc = [p.encode("utf-8") for p in pieces]
+        arr = (ctypes.c_char_p * len(enc))(*enc)
+        sc = np.ascontiguousarray(scores, dtype=np.float32)
+        if sc.shape != (len(enc),):
+            raise ValueError("one score per piece")
+        h = ctypes.c_void_p()
+        rc = self.lib.tee_unigram_create(arr, sc.ctypes.data, len(enc), unk_id, unk_score, bos_id, eos_id,
+                                         ctypes.byref(h))
+        if rc != TEE_OK:
+            raise TeeError(rc, self.lib.tee_last_error(None).decode())
+        self.h = h
+
+    def encode(self, text: str) -> np.ndarray:
+        raw = text.encode("utf-8")
+        n = self.lib.tee_unigram_encode(self.h, raw, len(raw), None, 0)
+        if n < 0:
+            raise TeeError(n, self.lib.tee_last_error(None).decode())
+        ids = np.empty(n, dtype=np.int32)
+        n2 = self.lib.tee_unigram_encode(self.h, raw, len(raw), ids.ctypes.data, n)
+        if n2 != n:
+            raise TeeError(n2, self.lib.tee_last_error(None).decode())
+        return ids
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.tee_unigram_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def pack_texts(id_lists):
+    """Pack per-text id arrays into one batch: (ids int32[T], cu_seqlens int32[n + 1])."""
+    lens = [len(a) for a in id_lists]
+    cu = np.zeros(len(lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    ids = np.concatenate([np.asarray(a, np.int32) for a in id_lists]) if id_lists else np.zeros(0, np.int32)
+    return ids, cu
+
+
+def similarity(vecs) -> np.ndarray:
+    """The [n, n] matrix of dot products of the rows of ``vecs`` (tee_similarity)."""
+    lib = load()
+    v = np.ascontiguousarray(vecs, dtype=np.float32)
+    n, dim = v.shape
+    out = np.empty((n, n), dtype=np.float32)
+    rc = lib.tee_similarity(v.ctypes.data, n, dim, out.ctypes.data)
+    if rc != TEE_OK:
+        raise TeeError(rc, lib.tee_last_error(None).decode())
+    return out
+
+
+def format_similarity(sim) -> str:
+    """The matrix as the `-sim` listing prints it: one row per line, four decimals."""
+    return "\n".join(" ".join(f"{x:.4f}" for x in row) for row in np.asarray(sim))

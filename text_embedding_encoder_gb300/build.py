@@ -1,6 +1,6 @@
 """Build the CUDA library (libtee.so) in-tree for sm_103a.
 
-Each .cu file under csrc/ is compiled in parallel with nvcc, then linked into
+Each .cu (and host-only .cpp) file under csrc/ is compiled in parallel with nvcc, then linked into
 one shared library with the CUDA runtime linked statically (the library
 needs only the driver at run time).  A stamp of the sources' hash and the
 flags skips rebuilding when nothing changed.
@@ -33,7 +33,8 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
+    """CUDA sources (*.cu) and host-only C++ sources (*.cpp), all compiled by nvcc."""
+    return sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _stamp() -> str:
@@ -60,7 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)

@@ -159,12 +159,17 @@ __global__ void __launch_bounds__(256) attention_simple_kernel(const TA* __restr
 // ---------------------------------------------------------------------------
 
 // One thread per (row n, 32-block b): d = max|w| / L, q = clamp(rint(w / d), +-L)
-// with L = 127 (int8 codes, one byte each) or, with W4, L = 7 (4-bit two's
-// complement codes, two per byte: element 2i in the low nibble of byte i).
-template <bool W4>
+// with, by the weight width WB,
+//   8: L = 127, int8 codes, one byte each;
+//   6: L = 31, 6-bit two's complement codes, four per three bytes: codes
+//      4i..4i+3 of a block fill bits 0-5, 6-11, 12-17, 18-23 of bytes 3i..3i+2
+//      (little-endian), so a block of 32 takes 24 bytes and a row K * 3 / 4;
+//   4: L = 7, 4-bit two's complement codes, two per byte: element 2i in the low
+//      nibble of byte i (16 bytes per block).
+template <int WB>
 __global__ void quant_weight_blocks_kernel(const float* __restrict__ w, int8_t* __restrict__ q,
                                            float* __restrict__ d, int N, int K) {
-    constexpr float L = W4 ? 7.0f : 127.0f;
+    constexpr float L = WB == 4 ? 7.0f : (WB == 6 ? 31.0f : 127.0f);
     const int nb = K / 32;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (size_t)N * nb) return;
@@ -181,10 +186,20 @@ __global__ void quant_weight_blocks_kernel(const float* __restrict__ w, int8_t* 
         if (dd > 0.f) v = fminf(fmaxf(rintf(__fdiv_rn(src[i], dd)), -L), L);
         code[i] = (int)v;
     }
-    if constexpr (W4) {
+    if constexpr (WB == 4) {
         uint8_t* dst = reinterpret_cast<uint8_t*>(q) + (n * K + b * 32) / 2;
 #pragma unroll
         for (int i = 0; i < 16; ++i) dst[i] = (uint8_t)((code[2 * i] & 15) | ((code[2 * i + 1] & 15) << 4));
+    } else if constexpr (WB == 6) {
+        uint8_t* dst = reinterpret_cast<uint8_t*>(q) + (n * K + b * 32) / 4 * 3;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t bits = (uint32_t)(code[4 * i] & 63) | ((uint32_t)(code[4 * i + 1] & 63) << 6) |
+                                  ((uint32_t)(code[4 * i + 2] & 63) << 12) | ((uint32_t)(code[4 * i + 3] & 63) << 18);
+            dst[3 * i] = (uint8_t)(bits & 255u);
+            dst[3 * i + 1] = (uint8_t)((bits >> 8) & 255u);
+            dst[3 * i + 2] = (uint8_t)(bits >> 16);
+        }
     } else {
         int8_t* dst = q + n * K + b * 32;
 #pragma unroll
@@ -200,6 +215,19 @@ __device__ __forceinline__ int unpack4x4(uint32_t two_bytes) {
     for (int i = 0; i < 4; ++i) {
         const int v = (int)((two_bytes >> (4 * i)) & 15u);
         const int sv = (v ^ 8) - 8;   // sign-extend the 4-bit two's complement code
+        out |= ((uint32_t)sv & 255u) << (8 * i);
+    }
+    return (int)out;
+}
+
+// Four 6-bit codes (24 bits, element k in bits 6k..6k+5) widened to the four
+// int8 lanes of one dp4a operand.
+__device__ __forceinline__ int unpack6x4(uint32_t three_bytes) {
+    uint32_t out = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int v = (int)((three_bytes >> (6 * i)) & 63u);
+        const int sv = (v ^ 32) - 32;   // sign-extend the 6-bit two's complement code
         out |= ((uint32_t)sv & 255u) << (8 * i);
     }
     return (int)out;
@@ -227,7 +255,7 @@ __global__ void quant_rows7_kernel(const float* __restrict__ x, int M, int K, in
 
 // C[M, N] (+)= s_m * sum_b d[n, b] * I[m, n, b], with I the exact int32 sum of
 // the 32 products of block b (dp4a).  64x64 tile, 4x4 outputs per thread.
-template <int EPI, bool PARTIALS, bool W4>
+template <int EPI, bool PARTIALS, int WB>
 __global__ void __launch_bounds__(256) gemm_w8a8_kernel(const int8_t* __restrict__ qa, const float* __restrict__ sa,
                                                         const int8_t* __restrict__ qw, const float* __restrict__ dw,
                                                         float* __restrict__ C, int32_t* __restrict__ partials, int M,
@@ -248,10 +276,17 @@ __global__ void __launch_bounds__(256) gemm_w8a8_kernel(const int8_t* __restrict
             int r = i >> 3, c = i & 7;
             int gm = m0 + r, gn = n0 + r;
             As[c][r] = gm < M ? reinterpret_cast<const int*>(qa + (size_t)gm * K + b * 32)[c] : 0;
-            if constexpr (W4)   // 16 bytes of packed codes per block row: bytes 2c, 2c + 1 hold elements 4c..4c+3
+            if constexpr (WB == 4)   // 16 bytes of packed codes per block row: bytes 2c, 2c + 1 hold elements 4c..4c+3
                 Ws[c][r] = gn < N ? unpack4x4(reinterpret_cast<const uint16_t*>(qw + ((size_t)gn * K + b * 32) / 2)[c])
                                   : 0;
-            else
+            else if constexpr (WB == 6) {   // 24 bytes per block row: bytes 3c..3c+2 hold elements 4c..4c+3
+                if (gn < N) {
+                    const uint8_t* p = reinterpret_cast<const uint8_t*>(qw) + ((size_t)gn * K + b * 32) / 4 * 3 + 3 * c;
+                    Ws[c][r] = unpack6x4((uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16));
+                } else {
+                    Ws[c][r] = 0;
+                }
+            } else
                 Ws[c][r] = gn < N ? reinterpret_cast<const int*>(qw + (size_t)gn * K + b * 32)[c] : 0;
         }
         __syncthreads();
@@ -334,11 +369,14 @@ cudaError_t launch_attention_simple(const void* qkv, bool bf16_act, const int32_
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_weight_blocks(const float* w, int8_t* q, float* d, int N, int K, bool w4, cudaStream_t s) {
+cudaError_t launch_quant_weight_blocks(const float* w, int8_t* q, float* d, int N, int K, int wbits, cudaStream_t s) {
     size_t n = (size_t)N * (K / 32);
     if (n == 0) return cudaSuccess;
-    if (w4) quant_weight_blocks_kernel<true><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(w, q, d, N, K);
-    else quant_weight_blocks_kernel<false><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(w, q, d, N, K);
+    const unsigned blocks = (unsigned)((n + 255) / 256);
+    if (wbits == 4) quant_weight_blocks_kernel<4><<<blocks, 256, 0, s>>>(w, q, d, N, K);
+    else if (wbits == 6) quant_weight_blocks_kernel<6><<<blocks, 256, 0, s>>>(w, q, d, N, K);
+    else if (wbits == 8) quant_weight_blocks_kernel<8><<<blocks, 256, 0, s>>>(w, q, d, N, K);
+    else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 
@@ -348,19 +386,21 @@ cudaError_t launch_quant_rows7(const float* x, int M, int K, int8_t* q, float* s
     return cudaGetLastError();
 }
 
-template <bool W4>
+template <int WB>
 void launch_w8a8_t(dim3 grid, const int8_t* qa, const float* sa, const int8_t* qw, const float* dw, float* C,
                    int32_t* partials, int M, int N, int K, int epi, cudaStream_t s) {
-    if (partials) gemm_w8a8_kernel<0, true, W4><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, partials, M, N, K);
-    else if (epi == 0) gemm_w8a8_kernel<0, false, W4><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, nullptr, M, N, K);
-    else gemm_w8a8_kernel<1, false, W4><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, nullptr, M, N, K);
+    if (partials) gemm_w8a8_kernel<0, true, WB><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, partials, M, N, K);
+    else if (epi == 0) gemm_w8a8_kernel<0, false, WB><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, nullptr, M, N, K);
+    else gemm_w8a8_kernel<1, false, WB><<<grid, 256, 0, s>>>(qa, sa, qw, dw, C, nullptr, M, N, K);
 }
 
 cudaError_t launch_gemm_w8a8(const int8_t* qa, const float* sa, const int8_t* qw, const float* dw, float* C,
-                             int32_t* partials, int M, int N, int K, int epi, bool w4, cudaStream_t s) {
+                             int32_t* partials, int M, int N, int K, int epi, int wbits, cudaStream_t s) {
     if (M == 0 || N == 0) return cudaSuccess;
     dim3 grid((N + 63) / 64, (M + 63) / 64);
-    if (w4) launch_w8a8_t<true>(grid, qa, sa, qw, dw, C, partials, M, N, K, epi, s);
-    else launch_w8a8_t<false>(grid, qa, sa, qw, dw, C, partials, M, N, K, epi, s);
+    if (wbits == 4) launch_w8a8_t<4>(grid, qa, sa, qw, dw, C, partials, M, N, K, epi, s);
+    else if (wbits == 6) launch_w8a8_t<6>(grid, qa, sa, qw, dw, C, partials, M, N, K, epi, s);
+    else if (wbits == 8) launch_w8a8_t<8>(grid, qa, sa, qw, dw, C, partials, M, N, K, epi, s);
+    else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }

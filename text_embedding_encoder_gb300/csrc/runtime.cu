@@ -83,7 +83,8 @@ int validate_config(const tee_config* c) {
     if (c->window < 0) return fail(nullptr, TEE_EINVAL, "window must be >= 0");
     if (!(c->rope_base_global > 0.f) || !(c->rope_base_local > 0.f)) return fail(nullptr, TEE_EINVAL, "RoPE bases must be > 0");
     if (!(c->ln_eps >= 0.f)) return fail(nullptr, TEE_EINVAL, "ln_eps must be >= 0");
-    if (c->dtype != TEE_F32 && c->dtype != TEE_BF16 && c->dtype != TEE_W8A8 && c->dtype != TEE_W4A8)
+    if (c->dtype != TEE_F32 && c->dtype != TEE_BF16 && c->dtype != TEE_W8A8 && c->dtype != TEE_W4A8 &&
+        c->dtype != TEE_W6A8)
         return fail(nullptr, TEE_EINVAL, "unknown dtype");
     if (c->max_tokens < 1 || c->max_texts < 1) return fail(nullptr, TEE_EINVAL, "max_tokens and max_texts must be >= 1");
     if (c->max_tokens > (1 << 24)) return fail(nullptr, TEE_EINVAL, "max_tokens must be <= 2^24");
@@ -136,8 +137,11 @@ size_t carve_weights(tee_ctx* c, void* base) {
     const size_t H = g.hidden;
     Carve cv(base);
     const size_t esz = g.dtype == TEE_BF16 ? 2 : (g.dtype == TEE_F32 ? 4 : 1);
-    // bytes of an [N, K] projection: packed 4-bit codes take half a byte per weight
-    auto wbytes = [&](size_t n_k) { return g.dtype == TEE_W4A8 ? n_k / 2 : n_k * esz; };
+    // bytes of an [N, K] projection: packed 4-bit codes take half a byte per
+    // weight, packed 6-bit codes three quarters
+    auto wbytes = [&](size_t n_k) {
+        return g.dtype == TEE_W4A8 ? n_k / 2 : (g.dtype == TEE_W6A8 ? n_k / 4 * 3 : n_k * esz);
+    };
     c->emb = cv.take<char>((size_t)g.vocab * H, g.dtype == TEE_BF16 ? 2 : 4);
     c->layers.assign(g.n_layers, LayerWeights{});
     for (int l = 0; l < g.n_layers; ++l) {
@@ -319,7 +323,7 @@ int step_linear(tee_ctx* ctx, int layer, int which, const void* A, void* C, int 
                launch_quant_rows7((const float*)A, T, K, ctx->qa, ctx->qs, s));
         LAUNCH(TEE_K_GEMM, flops, (double)T * K + (double)N * K + (double)T * N * 4 * (epi ? 2 : 1),
                launch_gemm_w8a8(ctx->qa, ctx->qs, (const int8_t*)L.w[which], L.wd[which], (float*)C, nullptr, T, N,
-                                K, epi, g.dtype == TEE_W4A8, s));
+                                K, epi, weight_bits(g), s));
         return TEE_OK;
     }
     if (g.dtype == TEE_BF16) {
@@ -469,7 +473,7 @@ int run_tokens(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const in
         LAUNCH(TEE_K_QUANT, 0, (double)T * H * 5 + T * 4.0, launch_quant_rows7(ctx->x, T, H, ctx->qa, ctx->qs, s));
         LAUNCH(TEE_K_GEMM, 2.0 * T * P * H, (double)T * H + (double)P * H + (double)T * P * 4,
                launch_gemm_w8a8(ctx->qa, ctx->qs, (const int8_t*)ctx->w_proj, ctx->w_proj_d, d_out, nullptr, T, P, H,
-                                0, g.dtype == TEE_W4A8, s));
+                                0, weight_bits(g), s));
     } else if (g.dtype == TEE_BF16) {
         // the projection's A operand in bf16, accumulated into a zeroed fp32 output
         LAUNCH(TEE_K_ELEMENTWISE, 0, (double)T * H * 6,
@@ -613,7 +617,7 @@ int tee_load_weights(tee_ctx* ctx, const tee_weights* w) {
         }
         CK(cudaMemcpyAsync(stage, src, n * sizeof(float), cudaMemcpyHostToDevice, s));
         if (kind == 1) CK(launch_convert_f32_bf16(stage, (bf16*)dst, n, s));
-        else CK(launch_quant_weight_blocks(stage, (int8_t*)dst, dscale, N, K, g.dtype == TEE_W4A8, s));
+        else CK(launch_quant_weight_blocks(stage, (int8_t*)dst, dscale, N, K, weight_bits(g), s));
         CK(cudaStreamSynchronize(s));
         return TEE_OK;
     };
@@ -940,7 +944,7 @@ int tee_op_w8a8_partials(tee_ctx* ctx, int layer, int which, const int8_t* d_q, 
                          void* stream) {
     int rc = check_ready(ctx);
     if (rc || (rc = check_layer(ctx, layer))) return rc;
-    if (!is_int_path(ctx->cfg)) return fail(ctx, TEE_EINVAL, "context is not W8A8 / W4A8");
+    if (!is_int_path(ctx->cfg)) return fail(ctx, TEE_EINVAL, "context is not W8A8 / W6A8 / W4A8");
     int N, K;
     if (wshape(ctx->cfg, which, &N, &K)) return fail(ctx, TEE_EINVAL, "bad projection selector");
     if (M < 0) return fail(ctx, TEE_EINVAL, "bad M");
@@ -950,14 +954,14 @@ int tee_op_w8a8_partials(tee_ctx* ctx, int layer, int which, const int8_t* d_q, 
     cudaStream_t s = (cudaStream_t)stream;
     LAUNCH(TEE_K_GEMM, 0, 0,
            launch_gemm_w8a8(d_q, nullptr, (const int8_t*)L.w[which], L.wd[which], nullptr, d_partials, M, N, K, 0,
-                            ctx->cfg.dtype == TEE_W4A8, s));
+                            weight_bits(ctx->cfg), s));
     return TEE_OK;
 }
 
 int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d) {
     int rc = check_ready(ctx);
     if (rc || (rc = check_layer(ctx, layer))) return rc;
-    if (!is_int_path(ctx->cfg)) return fail(ctx, TEE_EINVAL, "context is not W8A8 / W4A8");
+    if (!is_int_path(ctx->cfg)) return fail(ctx, TEE_EINVAL, "context is not W8A8 / W6A8 / W4A8");
     int N, K;
     if (wshape(ctx->cfg, which, &N, &K)) return fail(ctx, TEE_EINVAL, "bad projection selector");
     if (!h_q || !h_d) return fail(ctx, TEE_EINVAL, "NULL output");
@@ -969,6 +973,16 @@ int tee_weight_codes(tee_ctx* ctx, int layer, int which, int8_t* h_q, float* h_d
             const int lo = packed[i] & 15, hi = packed[i] >> 4;
             h_q[2 * i] = (int8_t)((lo ^ 8) - 8);
             h_q[2 * i + 1] = (int8_t)((hi ^ 8) - 8);
+        }
+    } else if (ctx->cfg.dtype == TEE_W6A8) {   // widen: codes 4i..4i+3 in the 24 bits of bytes 3i..3i+2
+        std::vector<uint8_t> packed((size_t)N * K / 4 * 3);
+        CK(cudaMemcpy(packed.data(), ctx->layers[layer].w[which], packed.size(), cudaMemcpyDeviceToHost));
+        for (size_t i = 0; i < packed.size() / 3; ++i) {
+            const uint32_t bits = packed[3 * i] | ((uint32_t)packed[3 * i + 1] << 8) | ((uint32_t)packed[3 * i + 2] << 16);
+            for (int k = 0; k < 4; ++k) {
+                const int v = (int)((bits >> (6 * k)) & 63u);
+                h_q[4 * i + k] = (int8_t)((v ^ 32) - 32);
+            }
         }
     } else {
         CK(cudaMemcpy(h_q, ctx->layers[layer].w[which], (size_t)N * K, cudaMemcpyDeviceToHost));

@@ -114,8 +114,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // ---- helpers ------------------------------------------------------------
 inline bool act_is_bf16(const tee_ctx* c) { return c->cfg.dtype == TEE_BF16; }
-// the integer paths: int8 (W8A8) or packed 4-bit (W4A8) weight blocks, 7-bit activations
-inline bool is_int_path(const tee_config& g) { return g.dtype == TEE_W8A8 || g.dtype == TEE_W4A8; }
+// the integer paths: int8 (W8A8), packed 6-bit (W6A8) or packed 4-bit (W4A8)
+// weight blocks, 7-bit activations
+inline bool is_int_path(const tee_config& g) {
+    return g.dtype == TEE_W8A8 || g.dtype == TEE_W6A8 || g.dtype == TEE_W4A8;
+}
+// width in bits of the integer path's weight codes
+inline int weight_bits(const tee_config& g) { return g.dtype == TEE_W4A8 ? 4 : (g.dtype == TEE_W6A8 ? 6 : 8); }
 inline size_t act_size(const tee_ctx* c) { return act_is_bf16(c) ? 2 : 4; }
 inline int layer_is_global(const tee_ctx* c, int l) { return (l % c->cfg.global_every) == 0; }
 
@@ -175,11 +180,10 @@ cudaError_t launch_selftest_wait(long long limit_cycles, unsigned int* status, c
 cudaError_t launch_gemm_simt(const void* A, const void* W, void* C, bool bf16_in, int M, int N, int K, int epi,
                              cudaStream_t s);
 
-// W8A8
-// w4: 4-bit codes (L = 7) packed two per byte, else int8 codes (L = 127).
-cudaError_t launch_quant_weight_blocks(const float* w, int8_t* q, float* d, int N, int K, bool w4, cudaStream_t s);
+// Integer paths.  wbits = weight code width: 8 (int8 codes, L = 127), 6 (L = 31,
+// four codes per three bytes) or 4 (L = 7, two codes per byte).
+cudaError_t launch_quant_weight_blocks(const float* w, int8_t* q, float* d, int N, int K, int wbits, cudaStream_t s);
 cudaError_t launch_quant_rows7(const float* x, int M, int K, int8_t* q, float* scale, cudaStream_t s);
 // y = s_m * sum_b d[n,b] * I[m,n,b]; epi 0 store float, 1 add into float; partials (optional) int32 [M][N][K/32]
-// w4: the weight codes are 4-bit, packed two per byte.
 cudaError_t launch_gemm_w8a8(const int8_t* qa, const float* sa, const int8_t* qw, const float* dw, float* C,
-                             int32_t* partials, int M, int N, int K, int epi, bool w4, cudaStream_t s);
+                             int32_t* partials, int M, int N, int K, int epi, int wbits, cudaStream_t s);
