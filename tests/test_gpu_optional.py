@@ -148,3 +148,58 @@ def test_packed_weight_encode_tiny_and_ruri(lib, variant):
         assert cos.min() >= BF16_COS, cos.min()
         assert enc.device_status() == 0
         enc.close()
+
+
+# ---------------------------------------------------------------------------
+# weights from a checkpoint file, and the host front end around the encoder
+# ---------------------------------------------------------------------------
+
+def test_checkpoint_file_gives_identical_embeddings(lib, tmp_path):
+    """Weights written to a safetensors file and read back load into the
+    library bit-identically, so the embeddings are identical (F32 file); a
+    BF16 file gives the embeddings of the bf16-rounded weights."""
+    from text_embedding_encoder_gb300 import weights_io
+    shape = synth.Shape(**{**synth.TINY.as_dict(), "emb_norm": True, "final_norm": True})
+    w = synth.make_weights(shape, seed=8)
+    ids, cu = synth.make_batch([37, 150, 8, 64], shape.vocab, seed=8)
+    p = tmp_path / "ckpt.safetensors"
+    weights_io.save_weights_file(p, w, shape, "F32")
+    for dtype in ("fp32", "bf16"):
+        a = make_encoder(shape, dtype, w, max_tokens=512, max_texts=8)
+        b = make_encoder(shape, dtype, weights_io.load_weights_file(p, shape), max_tokens=512, max_texts=8)
+        np.testing.assert_array_equal(a.encode(ids, cu), b.encode(ids, cu))
+        a.close()
+        b.close()
+    weights_io.save_weights_file(p, w, shape, "BF16")
+    enc = make_encoder(shape, "fp32", weights_io.load_weights_file(p, shape), max_tokens=512, max_texts=8)
+    w16 = weights_io.load_weights_file(p, shape)
+    ref = oracle.encode_packed(ids, cu, oracle.OracleModel(w16, shape, "fp32"))
+    assert_embeddings_close(enc.encode(ids, cu), ref, "fp32")
+    enc.close()
+
+
+def test_front_end_segment_encode_similarity(lib):
+    """Texts segmented by the Unigram front end, packed, encoded, and turned
+    into the similarity matrix: unit diagonal, symmetric, equal to the dot
+    products of the oracle's vectors of the same ids."""
+    rng = np.random.default_rng(12)
+    shape = synth.TINY
+    alphabet = list("川べりでサーフボードを持った人たちがいます瑠璃色はどんな")
+    pieces = ["<unk>", "<s>", "</s>"] + sorted(set(alphabet) | {"".join(rng.choice(alphabet, 2)) for _ in range(300)})
+    pieces = pieces[:shape.vocab]
+    scores = np.concatenate([[0, 0, 0], -rng.uniform(1, 9, len(pieces) - 3)]).astype(np.float32)
+    tok = binding.Unigram(pieces, scores, 0, -20.0, synth.BOS_ID, synth.EOS_ID)
+    texts = ["川べりでサーフボードを持った人たちがいます", "サーフボードを持った人たち", "瑠璃色はどんな色？", "色"]
+    id_lists = [tok.encode(t) for t in texts]
+    ids, cu = binding.pack_texts(id_lists)
+    w = synth.make_weights(shape, seed=0)
+    enc = make_encoder(shape, "bf16", w, max_tokens=512, max_texts=8)
+    vecs = enc.encode(ids, cu)
+    enc.close()
+    sim = binding.similarity(vecs)
+    np.testing.assert_allclose(np.diag(sim), 1.0, atol=2e-6)
+    np.testing.assert_array_equal(sim, sim.T)
+    ref = oracle.encode_packed(ids, cu, oracle.OracleModel(w, shape, "bf16"))
+    np.testing.assert_allclose(sim, ref @ ref.T, atol=2e-3)
+    print(binding.format_similarity(sim))
+    tok.close()
