@@ -175,16 +175,22 @@ int tee_selftest_gelu(const float* d_a, float* d_y, long long n, void* stream);
 
 /* Attention work items, as the pass lists them for the varlen attention
  * kernel (packing paragraph of §何が動くか: attention stays inside each text;
- * §エンコーダ: the whole text on global layers, +-window tokens otherwise):
- * one item per (text j, 128-query tile), {q_start, q_len, k_lo, k_hi} with
- * q_start = cu[j] + 128 i, q_len = min(128, cu[j+1] - q_start) and [k_lo, k_hi)
- * the keys that any query of the tile may see -- [cu[j], cu[j+1]) if
- * is_global, else [max(cu[j], q_start - window), min(cu[j+1], q_start + q_len
- * + window)).  The global list is ordered by q_len * (k_hi - k_lo), largest
- * first, ties in text order; the window list is in text order.  h_cu host
- * int32[n_texts + 1] (cu[0] == 0, strictly increasing).  items: host
- * int32[4 * max_items], or NULL to ask for the count only.  Returns the
- * number of items (TEE_ETOOLONG if it exceeds max_items). */
+ * §エンコーダ: the whole text on global layers, +-window tokens otherwise), each
+ * {q_start, q_len, k_lo, k_hi}: a tile of up to 128 queries and the key range
+ * [k_lo, k_hi) that any of its queries may see.
+ *   is_global != 0: one item per (text j, 128-query tile) -- q_start = cu[j] +
+ *     128 i, q_len = min(128, cu[j+1] - q_start), [k_lo, k_hi) = [cu[j],
+ *     cu[j+1]) -- ordered by q_len * (k_hi - k_lo), largest first, ties in text
+ *     order.
+ *   is_global == 0: one item per 128-query tile of the packed sequence itself
+ *     (q_start = 128 i, q_len = min(128, T - q_start), T = cu[n_texts]), tiles
+ *     shared by consecutive texts; k_lo = max(start of the text holding row
+ *     q_start, q_start - window), k_hi = min(end of the text holding row
+ *     q_start + q_len - 1, q_start + q_len + window); in sequence order.  (The
+ *     kernel masks each row to its own text.)
+ * h_cu host int32[n_texts + 1] (cu[0] == 0, strictly increasing).  items: host
+ * int32[4 * max_items], or NULL to ask for the count only.  Returns the number
+ * of items (TEE_ETOOLONG if it exceeds max_items). */
 int tee_plan_attention(const int32_t* h_cu, int n_texts, int window, int is_global, int32_t* items, int max_items);
 
 /* Tile shape of the bf16 tensor-core projection C[M, N] = A[M, K] W^T: *bn =

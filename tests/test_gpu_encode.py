@@ -79,7 +79,13 @@ def test_packing_invariance(lib, tiny_weights, dtype):
     ids_r = np.concatenate([ids[cu[j]:cu[j + 1]] for j in order])
     cu_r = np.concatenate([[0], np.cumsum([lengths[j] for j in order])]).astype(np.int32)
     rev = enc.encode(ids_r, cu_r)[::-1]
-    tol = 0.0 if dtype == "fp32" else 1e-6
+    # fp32: bit-identical (the SIMT attention visits each row's keys in the same
+    # order however the texts are packed).  bf16: the window layers tile the
+    # packed sequence itself, so which 128-key tile (and which softmax warp's
+    # reference maximum) a key falls in depends on the neighbouring texts; the
+    # bf16 rounding of P then differs, by about 2e-4 on these vectors, well
+    # inside the 3e-3 bar against the oracle
+    tol = 0.0 if dtype == "fp32" else 1e-3
     np.testing.assert_allclose(packed, alone, atol=tol, rtol=0)
     np.testing.assert_allclose(packed, rev, atol=tol, rtol=0)
     sim = packed @ packed.T

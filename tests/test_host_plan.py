@@ -1,8 +1,9 @@
 """Host-side planning of a pass, checked without a GPU through the C ABI.
 
-tee_plan_attention: the attention work items (one per text and 128-query
-tile) with the key range the tile's queries may see, compared with a brute
-force over every query row of the tile (whole text on global layers,
+tee_plan_attention: the attention work items (global layers: one per text
+and 128-query tile; window layers: one per 128-row tile of the packed
+sequence) with the key range the tile's queries may see, compared with a
+brute force over every query row of the tile (whole text on global layers,
 |i - j| <= window inside the text otherwise).  tee_plan_gemm: the tensor-core
 GEMM's tile shapes for the projections of the 310m shape, pinned to values
 worked out by hand from the column-wave rule, plus invariants over a grid of
@@ -38,21 +39,39 @@ def _plan_attention(lib, cu, window, is_global, max_items=None):
     return rc, out[:max(rc, 0)]
 
 
+def _visible(cu, window, is_global):
+    """Dense mask [T, T]: query i may see key j (same text, and |i - j| <= window
+    unless the layer is global)."""
+    T = int(cu[-1])
+    text = np.searchsorted(cu, np.arange(T), side="right") - 1
+    same = text[:, None] == text[None, :]
+    if is_global:
+        return same
+    idx = np.arange(T)
+    return same & (np.abs(idx[:, None] - idx[None, :]) <= window)
+
+
 def _brute_force_items(cu, window, is_global):
-    """Every (text, 128-query tile) with the smallest key interval holding every
-    key that some query row of the tile may attend to."""
+    """Global layers: every (text, 128-query tile); window layers: every 128-row
+    tile of the packed sequence.  Each with the smallest key interval holding
+    every key that some query row of the tile may attend to."""
+    vis = _visible(cu, window, is_global)
     items = []
-    for j in range(len(cu) - 1):
-        s0, s1 = int(cu[j]), int(cu[j + 1])
-        for q0 in range(s0, s1, 128):
-            ql = min(128, s1 - q0)
-            rows = np.arange(q0, q0 + ql)[:, None]
-            keys = np.arange(s0, s1)[None, :]
-            visible = np.broadcast_to(True, (ql, s1 - s0)) if is_global else np.abs(keys - rows) <= window
-            cols = np.nonzero(visible.any(axis=0))[0] + s0
-            items.append((q0, ql, int(cols.min()), int(cols.max()) + 1))
-    if is_global:   # most work first, ties in text order (a stable sort)
-        items = sorted(items, key=lambda it: -it[1] * (it[3] - it[2]))
+
+    def add(q0, ql):
+        cols = np.nonzero(vis[q0:q0 + ql].any(axis=0))[0]
+        items.append((q0, ql, int(cols.min()), int(cols.max()) + 1))
+
+    if is_global:
+        for j in range(len(cu) - 1):
+            s0, s1 = int(cu[j]), int(cu[j + 1])
+            for q0 in range(s0, s1, 128):
+                add(q0, min(128, s1 - q0))
+        items = sorted(items, key=lambda it: -it[1] * (it[3] - it[2]))   # most work first, stable
+    else:
+        T = int(cu[-1])
+        for q0 in range(0, T, 128):
+            add(q0, min(128, T - q0))
     return items
 
 

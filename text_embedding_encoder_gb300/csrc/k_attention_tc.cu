@@ -5,22 +5,27 @@
 // the global layers (layer 0 and every third), |i - j| <= 64 on the others --
 // with scores q.k / sqrt(64) and a softmax over the allowed keys.
 //
-// Work unit = (text, 128-query tile) x head; the host lists the (text, tile)
-// items with their key range [k_lo, k_hi) (whole text, or the window clipped to
-// the text), longest first.  The kernel is persistent: one CTA per SM walks
-// the units u = blockIdx.x, blockIdx.x + gridDim.x, ...  Ten warps:
+// Work unit = (128-query tile, head).  The host lists the query tiles with
+// their key range [k_lo, k_hi): on global layers the tiles of each text (keys =
+// the text), longest first; on window layers the tiles of the packed sequence
+// itself, so short texts share a tile instead of padding one each, with every
+// row masked to its own text through the per-token text bounds row_tb.  The
+// kernel is persistent: one CTA per SM walks the units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ...  Ten warps:
 //   warp 0 lane 0   TMA: each unit's Q tile (double-buffered, so the next
 //                   unit's Q arrives early), then its K and V tiles (128 keys)
 //                   into a KV_STAGES-deep ring, straight from the packed qkv
 //                   rows;
-//   warp 1          TMEM allocation; lane 0 issues S = Q K^T (M=128, N=128,
-//                   K=64) into one of two TMEM S buffers, and O += P_t V_t
-//                   (M=128, N=64, K=128) with P read from tensor memory (the
-//                   A operand) and V from shared memory as an MN-major operand
+//   warp 1          TMEM allocation; lane 0 issues S_t = Q K_t^T (M=128, N=128,
+//                   K=64) into TMEM S/P buffer t % 3, and O += P_t V_t (M=128,
+//                   N=64, K=128) with P read from the first 64 columns of the
+//                   same buffer (the A operand, written there by the softmax
+//                   over S_t) and V from shared memory as an MN-major operand
 //                   (no transpose), into the unit's TMEM O buffer (two, by
-//                   unit).  S of tile t+1 is issued before P_t V_t, across
-//                   unit boundaries too, so the softmax of one tile overlaps
-//                   the QK^T of the next;
+//                   unit).  P V runs two tiles behind S, across unit
+//                   boundaries too, so S_{t+1} is ready when the softmax
+//                   finishes tile t; the MMAs of one thread run in order, so
+//                   S_{t+3} overwrites buffer t % 3 only after P_t V_t read it;
 //   warps 2-9       two threads per query row (a warp may read only its
 //                   32-lane TMEM quadrant, so warps w and w+4 share one and
 //                   split the 128 key columns, and the 64 output dimensions,
@@ -31,8 +36,10 @@
 //                   against a reference maximum that moves only when a tile's
 //                   maximum exceeds it by more than 2^8 (then that row of O is
 //                   rescaled in TMEM), P as bf16 pairs stored into TMEM for the
-//                   P V MMA; a unit's O / l is read and stored as bf16 after
-//                   the next unit's first P hand-off.
+//                   P V MMA (bf16 pairs written over the tile's first 64 S
+//                   columns, once both warps of the pair have read theirs); a
+//                   unit's O / l is read and stored as bf16 after the next
+//                   unit's first P hand-off.
 // Pipeline counters run across units; every wait is bounded.
 #include "tee_internal.cuh"
 
@@ -59,16 +66,18 @@ constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + KV_STAGES * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + KV_STAGES * TILE_BYTES;
 // barrier indices
-constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = B_KVF + KV_STAGES, B_SF = B_KVE + KV_STAGES, B_SE = B_SF + 2,
-              B_PF = B_SE + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_DONE = B_OE + 2, N_BARS = B_DONE + 1;
+constexpr int SP_BUFS = 3;   // TMEM S/P buffers: tile t uses buffer t % 3
+constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = B_KVF + KV_STAGES, B_SF = B_KVE + KV_STAGES,
+              B_PF = B_SF + SP_BUFS, B_OF = B_PF + SP_BUFS, B_OE = B_OF + 2, B_DONE = B_OE + 2, N_BARS = B_DONE + 1;
 constexpr uint32_t OFF_RED = OFF_BAR + N_BARS * 8 + 16;       // row-maximum exchange: [2 tiles][2 halves][128 rows]
 constexpr uint32_t OFF_REDL = OFF_RED + 2 * 2 * 128 * 4;       // row-sum exchange: [2 halves][128 rows]
 constexpr uint32_t SMEM_TOTAL = OFF_REDL + 2 * 128 * 4 + 1024;
-constexpr uint32_t TMEM_COLS = 512;                 // S: 2 x 128 columns (by tile), O: 2 x 64 (by unit)
-constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;   // P: 2 x 64 columns (bf16 pairs), by tile
+constexpr uint32_t TMEM_COLS = 512;                 // S/P: 3 x 128 columns (by tile), O: 2 x 64 (by unit)
+constexpr uint32_t TM_S = 0, TM_O = SP_BUFS * BKV;
 
 struct AttnParams {
-    const int4* items;      // {q_start, q_len, k_lo, k_hi} per (text, query tile)
+    const int4* items;      // {q_start, q_len, k_lo, k_hi} per query tile
+    const int2* row_tb;     // per token: {start, end} of its text (window layers)
     int n_units;            // items x heads
     int n_heads;
     int hidden;
@@ -97,11 +106,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_QF + b), 1);
             mbar_init(bar(B_QE + b), 1);
-            mbar_init(bar(B_SF + b), 1);
-            mbar_init(bar(B_SE + b), SM_THREADS);
-            mbar_init(bar(B_PF + b), SM_THREADS);
             mbar_init(bar(B_OF + b), 1);
             mbar_init(bar(B_OE + b), SM_THREADS);
+        }
+        for (int b = 0; b < SP_BUFS; ++b) {
+            mbar_init(bar(B_SF + b), 1);
+            mbar_init(bar(B_PF + b), SM_THREADS);
         }
         for (int s = 0; s < KV_STAGES; ++s) {
             mbar_init(bar(B_KVF + s), 1);
@@ -172,11 +182,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // tile of a unit overwrites it once the softmax warps have read the
             // unit two back out of that buffer
             auto issue_pv = [&](uint32_t tt, bool first, int ub, uint32_t uuse) -> bool {
-                const int pb = tt & 1, st = tt % KV_STAGES;
-                if (!mbar_wait(bar(B_PF + pb), (tt >> 1) & 1, abort_flag)) return false;
+                const int pb = tt & 1, sb = tt % SP_BUFS, st = tt % KV_STAGES;
+                if (!mbar_wait(bar(B_PF + sb), (tt / SP_BUFS) & 1, abort_flag)) return false;
                 if (first && !mbar_wait(bar(B_OE + ub), (uuse & 1) ^ 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t pbase = tmem_base + TM_P + pb * (BKV / 2);
+                const uint32_t pbase = tmem_base + TM_S + sb * BKV;
                 const uint32_t vbase = sbase + OFF_V + st * TILE_BYTES;
 #pragma unroll
                 for (int s = 0; s < BKV / 16; ++s) {
@@ -187,12 +197,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mma_commit(bar(B_KVE + st));
                 return true;
             };
+            struct Pend {
+                uint32_t t, use;
+                bool first;
+                int ub;
+            };
+            Pend q0{}, q1{};         // tiles whose S is issued and whose P V is not (at most two)
+            int nq = 0;
             uint32_t t = 0;          // tiles whose S has been issued (global)
             bool ok = true;
-            bool pend = false;       // a tile whose P V is still to be issued
-            uint32_t pend_t = 0, pend_use = 0;
-            bool pend_first = false;
-            int pend_ub = 0;
             int ui = 0;
             int4 it_next = p.items[blockIdx.x / p.n_heads];
             for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
@@ -202,9 +215,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait(bar(B_QF + qb), (ui >> 1) & 1, abort_flag)) break;
                 const uint64_t qdesc = sw128_desc(sbase + OFF_Q + qb * TILE_BYTES);
                 for (int kt = 0; kt < nk; ++kt, ++t) {
-                    const int st = t % KV_STAGES, sb = t & 1;
-                    if (!mbar_wait(bar(B_KVF + st), (t / KV_STAGES) & 1, abort_flag) ||
-                        !mbar_wait(bar(B_SE + sb), ((t >> 1) & 1) ^ 1, abort_flag)) {
+                    // buffer t % 3 last held tile t - 3, whose P V was issued
+                    // before this S (and runs before it): no wait for it here
+                    const int st = t % KV_STAGES, sb = t % SP_BUFS;
+                    if (!mbar_wait(bar(B_KVF + st), (t / KV_STAGES) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -215,18 +229,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mma_bf16(tmem_base + TM_S + sb * BKV, qdesc + 2 * k, kdesc + 2 * k, idesc_s, k != 0);
                     mma_commit(bar(B_SF + sb));
                     if (kt == nk - 1) mma_commit(bar(B_QE + qb));   // Q buffer free once these S MMAs finish
-                    if (pend && !issue_pv(pend_t, pend_first, pend_ub, pend_use)) {
-                        ok = false;
-                        break;
+                    const Pend cur{t, (uint32_t)ui >> 1, kt == 0, ui & 1};
+                    if (nq == 2) {   // P V two tiles behind S
+                        if (!issue_pv(q0.t, q0.first, q0.ub, q0.use)) {
+                            ok = false;
+                            break;
+                        }
+                        q0 = q1;
+                        q1 = cur;
+                    } else if (nq == 1) {
+                        q1 = cur;
+                        nq = 2;
+                    } else {
+                        q0 = cur;
+                        nq = 1;
                     }
-                    pend = true;
-                    pend_t = t;
-                    pend_first = kt == 0;
-                    pend_ub = ui & 1;
-                    pend_use = (uint32_t)ui >> 1;
                 }
             }
-            if (ok && pend) issue_pv(pend_t, pend_first, pend_ub, pend_use);
+            if (ok && nq >= 1) ok = issue_pv(q0.t, q0.first, q0.ub, q0.use);
+            if (ok && nq == 2) ok = issue_pv(q1.t, q1.first, q1.ub, q1.use);
             mma_commit(bar(B_DONE));
             mbar_wait_drain(bar(B_DONE), 0);
         }
@@ -292,21 +313,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int nk = n_kv_tiles(it);
             const int qg = q_start + r;
             const int ub = ui & 1;
-            // keys visible to this row: [vis_lo, vis_hi)
-            const int vis_lo = p.is_global ? k_lo : max(k_lo, qg - p.window);
-            const int vis_hi = p.is_global ? k_hi : min(k_hi, qg + p.window + 1);
+            // keys visible to this row: [vis_lo, vis_hi) -- the text on global
+            // layers, the window inside the row's own text otherwise (nothing
+            // for rows past the end of the sequence)
+            int vis_lo = k_lo, vis_hi = k_hi;
+            if (!p.is_global) {
+                if (r < q_len) {
+                    const int2 tb = p.row_tb[qg];
+                    vis_lo = max(tb.x, qg - p.window);
+                    vis_hi = min(tb.y, qg + p.window + 1);
+                } else {
+                    vis_hi = vis_lo;
+                }
+            }
             float m_ref = -INFINITY, l = 0.f;
             for (int kt = 0; kt < nk; ++kt, ++t) {
-                const int sb = t & 1;
-                if (!mbar_wait(bar(B_SF + sb), (t >> 1) & 1, abort_flag)) {
+                const int sb = t % SP_BUFS;
+                if (!mbar_wait(bar(B_SF + sb), (t / SP_BUFS) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 float v[64];
                 tmem_ld64(tmem_base + lane_off + TM_S + sb * BKV + half * 64, v);
-                tc_fence_before();
-                mbar_arrive(bar(B_SE + sb));
                 const int key0 = k_lo + kt * BKV + half * 64;
                 const int lo = vis_lo - key0, hi = vis_hi - key0;   // visible columns [lo, hi)
                 if (lo > 0 || hi < 64) {
@@ -362,12 +391,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     s8[i & 7] += v[i];
                 }
                 const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
-                // P as bf16 pairs into this tile's TMEM P buffer (the A operand
-                // of P V): this half's 64 keys are columns [32 * half, +32)
+                // P as bf16 pairs over the tile's first 64 S columns (the A
+                // operand of P V): this half's 64 keys are columns [32 * half,
+                // +32).  Both warps of the pair have read their S (the row
+                // maximum exchange above), so overwriting the other half's S
+                // columns is safe.
                 uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(v[2 * c], v[2 * c + 1]);
-                tmem_st32_u(tmem_base + lane_off + TM_P + sb * (BKV / 2) + half * 32, pk);
+                tmem_st32_u(tmem_base + lane_off + TM_S + sb * BKV + half * 32, pk);
                 tc_fence_before();
                 mbar_arrive(bar(B_PF + sb));
                 l += sum;
@@ -416,12 +448,14 @@ void init_once() {
 }  // namespace
 
 cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, const int4* d_items, int n_items,
-                                bool is_global, int window, void* o, unsigned int* status, cudaStream_t s) {
+                                bool is_global, int window, const int2* row_tb, void* o, unsigned int* status,
+                                cudaStream_t s) {
     std::call_once(g_once, init_once);
     if (g_init_err != cudaSuccess) return g_init_err;
     if (n_items == 0 || T == 0) return cudaSuccess;
     if (H != n_heads * HD || (reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(o) & 15))
         return cudaErrorInvalidValue;
+    if (!is_global && !row_tb) return cudaErrorInvalidValue;
     CUtensorMap tm;
     cuuint64_t dims[2] = {(cuuint64_t)3 * H, (cuuint64_t)T};
     cuuint64_t strides[1] = {(cuuint64_t)3 * H * 2};
@@ -444,8 +478,8 @@ cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, cons
         }
     }
     const int n_units = n_items * n_heads;
-    AttnParams p{d_items, n_units, n_heads, H, is_global ? 1 : 0, window, 1.4426950408889634f / 8.0f, (bf16*)o,
-                 status};
+    AttnParams p{d_items, row_tb, n_units, n_heads, H, is_global ? 1 : 0, window, 1.4426950408889634f / 8.0f,
+                 (bf16*)o, status};
     const int grid = n_units < num_sms ? n_units : num_sms;
     cudaError_t e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_TOTAL, s, tm, p);
     if (e != cudaSuccess) return e;

@@ -73,13 +73,18 @@ __global__ void embed_kernel(const TE* __restrict__ emb, const int32_t* __restri
     }
 }
 
-// pos[t] = t - cu[text(t)]
-__global__ void positions_kernel(const int32_t* __restrict__ cu, int n_texts, int T, int32_t* __restrict__ pos) {
+// pos[t] = t - cu[text(t)]; row_tb[t] = {cu[text(t)], cu[text(t) + 1]} (the
+// bounds of the text holding token t, for the attention's per-row masks)
+__global__ void positions_kernel(const int32_t* __restrict__ cu, int n_texts, int T, int32_t* __restrict__ pos,
+                                 int2* __restrict__ row_tb) {
     pdl_wait();
     pdl_trigger();
     int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
-    pos[t] = t - cu[text_of(cu, n_texts, t)];
+    const int j = text_of(cu, n_texts, t);
+    const int s0 = cu[j];
+    pos[t] = t - s0;
+    if (row_tb) row_tb[t] = make_int2(s0, cu[j + 1]);
 }
 
 // One warp per row; H a multiple of 128 and <= 1024 (at most 8 float4 per lane).
@@ -475,9 +480,9 @@ cudaError_t launch_embed(const void* emb, bool emb_bf16, const int32_t* ids, int
     return launch_pdl(embed_kernel<float>, dim3(blocks), dim3(256), 0, s, (const float*)emb, ids, T, H, V, x, status);
 }
 
-cudaError_t launch_positions(const int32_t* cu, int n_texts, int T, int32_t* pos, cudaStream_t s) {
+cudaError_t launch_positions(const int32_t* cu, int n_texts, int T, int32_t* pos, int2* row_tb, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    cudaError_t e = launch_pdl(positions_kernel, dim3((T + 255) / 256), dim3(256), 0, s, cu, n_texts, T, pos);
+    cudaError_t e = launch_pdl(positions_kernel, dim3((T + 255) / 256), dim3(256), 0, s, cu, n_texts, T, pos, row_tb);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

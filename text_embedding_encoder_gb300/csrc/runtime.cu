@@ -103,6 +103,7 @@ size_t carve_workspace(tee_ctx* c, void* base) {
     c->d_ids = cv.take<int32_t>(T);
     c->d_cu = cv.take<int32_t>(g.max_texts + 1);
     c->d_pos = cv.take<int32_t>(T);
+    c->d_rowtb = cv.take<int2>(T);
     c->x = cv.take<float>(T * H);
     c->y = cv.take<char>(T * H, A);
     c->qkv = cv.take<char>(T * 3 * H, A);
@@ -122,7 +123,7 @@ size_t carve_workspace(tee_ctx* c, void* base) {
         c->rope_sin[b] = cv.take<float>(T * 32);
     }
     c->d_status = cv.take<unsigned int>(4);
-    c->max_items = (int)(T / 128 + g.max_texts + 1);
+    c->max_items = (int)(T / 128 + g.max_texts + 1);   // bounds both lists
     for (int b = 0; b < 2; ++b) c->d_items[b] = cv.take<int4>(c->max_items);
     c->max_chunks = (int)(T / POOL_CHUNK_FUSED + g.max_texts + 1);
     c->d_chunk_off = cv.take<int32_t>(g.max_texts + 1);
@@ -212,24 +213,33 @@ double attention_pairs(const int32_t* h_cu, int n_texts, bool is_global, int w) 
     return pairs;
 }
 
-// Attention work items of one pass: one per (text, 128-query tile), with the
-// key range the queries of that tile may see.  List 0 (global layers): the
-// whole text, longest texts first so the heavy CTAs start early; list 1
-// (window layers): the window around the tile, clipped to the text.
+// Attention work items of one pass, each a 128-query tile with the key range
+// its queries may see.  List 0 (global layers): the tiles of each text (a
+// tile never holds two texts, so its keys are exactly the text), the most
+// work (queries x keys) first so the heavy CTAs start early.  List 1 (window
+// layers): the tiles of the packed sequence itself, ignoring text boundaries,
+// so short texts share tiles instead of padding one each; a tile's key range
+// runs from the first key its first row may see (the window clipped to that
+// row's text) to the last key its last row may see, and each row is masked to
+// its own text in the kernel.
 void plan_attention_items(const int32_t* h_cu, int n_texts, int w, std::vector<int4> (&items)[2]) {
     for (int b = 0; b < 2; ++b) items[b].clear();
     for (int j = 0; j < n_texts; ++j) {
         const int s0 = h_cu[j], s1 = h_cu[j + 1];
-        for (int q0 = s0; q0 < s1; q0 += 128) {
-            const int ql = std::min(128, s1 - q0);
-            items[0].push_back(make_int4(q0, ql, s0, s1));
-            items[1].push_back(make_int4(q0, ql, std::max(s0, q0 - w), std::min(s1, q0 + ql + w)));
-        }
+        for (int q0 = s0; q0 < s1; q0 += 128) items[0].push_back(make_int4(q0, std::min(128, s1 - q0), s0, s1));
     }
     std::stable_sort(items[0].begin(), items[0].end(), [](const int4& a, const int4& b) {
         const long long ca = (long long)a.y * (a.w - a.z), cb = (long long)b.y * (b.w - b.z);
         return ca > cb;
     });
+    const int T = h_cu[n_texts];
+    int j0 = 0, j1 = 0;   // texts holding the tile's first and last rows
+    for (int q0 = 0; q0 < T; q0 += 128) {
+        const int ql = std::min(128, T - q0);
+        while (h_cu[j0 + 1] <= q0) ++j0;
+        while (h_cu[j1 + 1] <= q0 + ql - 1) ++j1;
+        items[1].push_back(make_int4(q0, ql, std::max(h_cu[j0], q0 - w), std::min(h_cu[j1 + 1], q0 + ql + w)));
+    }
 }
 
 int prepare_attention_items(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cudaStream_t s) {
@@ -373,7 +383,7 @@ int step_attention(tee_ctx* ctx, int layer, const void* qkv, const int32_t* d_cu
         const int b = is_g ? 0 : 1;
         LAUNCH(TEE_K_ATTENTION, flops, bytes,
                launch_attention_tc(qkv, T, g.hidden, g.n_heads, ctx->d_items[b], (int)ctx->h_items[b].size(), is_g,
-                                   g.window, o, ctx->d_status, s));
+                                   g.window, ctx->d_rowtb, o, ctx->d_status, s));
         return TEE_OK;
     }
     LAUNCH(TEE_K_ATTENTION, flops, bytes,
@@ -434,7 +444,8 @@ int run_layers(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const in
     const tee_config& g = ctx->cfg;
     int rc;
     if (g.dtype == TEE_BF16 && (rc = prepare_attention_items(ctx, h_cu, n_texts, s))) return rc;
-    LAUNCH(TEE_K_EMBED, 0, (double)T * 4 * 2, launch_positions(d_cu, n_texts, T, ctx->d_pos, s));
+    LAUNCH(TEE_K_EMBED, 0, (double)T * 4 * 4,
+           launch_positions(d_cu, n_texts, T, ctx->d_pos, ctx->d_rowtb, s));
     LAUNCH(TEE_K_EMBED, 0, (double)T * g.hidden * (4.0 + (act_is_bf16(ctx) ? 2 : 4)) + T * 4.0,
            launch_embed(ctx->emb, act_is_bf16(ctx), d_ids, T, g.hidden, g.vocab, ctx->x, ctx->d_status, s));
     if (g.emb_norm && (rc = step_norm_in_place(ctx, ctx->ln_emb, T, s))) return rc;
@@ -835,7 +846,7 @@ int tee_op_positions(tee_ctx* ctx, const int32_t* d_cu, const int32_t* h_cu, int
     if (rc || (rc = check_dev(ctx, T, 4, {d_cu, d_pos}))) return rc;
     ON_DEVICE(ctx);
     cudaStream_t s = (cudaStream_t)stream;
-    LAUNCH(TEE_K_EMBED, 0, 0, launch_positions(d_cu, n_texts, T, d_pos, s));
+    LAUNCH(TEE_K_EMBED, 0, 0, launch_positions(d_cu, n_texts, T, d_pos, nullptr, s));
     return TEE_OK;
 }
 
@@ -866,8 +877,12 @@ int tee_op_attention(tee_ctx* ctx, int layer, const void* d_qkv, const int32_t* 
     if ((rc = check_cu(ctx, h_cu, n_texts, &T))) return rc;
     if ((rc = check_dev(ctx, T, 16, {d_qkv, d_o})) || (rc = check_dev(ctx, T, 4, {d_cu}))) return rc;
     ON_DEVICE(ctx);
-    if (ctx->cfg.dtype == TEE_BF16 && (rc = prepare_attention_items(ctx, h_cu, n_texts, (cudaStream_t)stream)))
-        return rc;
+    if (ctx->cfg.dtype == TEE_BF16) {
+        // the work items, and the per-row text bounds the window layers' masks take
+        if ((rc = prepare_attention_items(ctx, h_cu, n_texts, (cudaStream_t)stream))) return rc;
+        cudaStream_t s = (cudaStream_t)stream;
+        LAUNCH(TEE_K_EMBED, 0, 0, launch_positions(d_cu, n_texts, T, ctx->d_pos, ctx->d_rowtb, s));
+    }
     return step_attention(ctx, layer, d_qkv, d_cu, h_cu, n_texts, T, d_o, (cudaStream_t)stream);
 }
 

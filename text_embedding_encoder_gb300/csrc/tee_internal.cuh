@@ -56,6 +56,7 @@ struct tee_ctx {
     int32_t* d_ids = nullptr;
     int32_t* d_cu = nullptr;
     int32_t* d_pos = nullptr;
+    int2* d_rowtb = nullptr;                  // per token: {first token, one past the last} of its text
     float* x = nullptr;                 // residual stream, float [T*H]
     void* y = nullptr;                  // LayerNorm output, ACT [T*H]
     void* qkv = nullptr;                // ACT [T*3H]
@@ -143,7 +144,8 @@ void prof_end(tee_ctx* c, cudaStream_t s, int slot);
 cudaError_t launch_convert_f32_bf16(const float* src, bf16* dst, size_t n, cudaStream_t s);
 cudaError_t launch_embed(const void* emb, bool emb_bf16, const int32_t* ids, int T, int H, int V, float* x,
                          unsigned int* status, cudaStream_t s);
-cudaError_t launch_positions(const int32_t* cu, int n_texts, int T, int32_t* pos, cudaStream_t s);
+// pos[t] = t - cu[text(t)]; with row_tb non-NULL also row_tb[t] = {cu[text(t)], cu[text(t) + 1]}.
+cudaError_t launch_positions(const int32_t* cu, int n_texts, int T, int32_t* pos, int2* row_tb, cudaStream_t s);
 cudaError_t launch_layernorm(const float* x, const float* gamma, void* y, bool y_bf16, int T, int H, float eps,
                              cudaStream_t s);
 cudaError_t launch_rope(void* qkv, bool bf16_act, const int32_t* pos, const float* cos_t, const float* sin_t, int T,
@@ -168,9 +170,12 @@ cudaError_t launch_attention_simple(const void* qkv, bool bf16_act, const int32_
                                     int n_heads, bool is_global, int window, void* o, cudaStream_t s);
 
 // tcgen05 varlen attention over bf16 qkv [T, 3H]; items {q_start, q_len, k_lo, k_hi} per
-// (text, 128-query tile), one CTA per item and head.
+// 128-query tile (global layers: tiles of one text; window layers: tiles of the
+// packed sequence, each row's text bounds in row_tb), persistent CTAs over
+// (item, head) units.
 cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, const int4* d_items, int n_items,
-                                bool is_global, int window, void* o, unsigned int* status, cudaStream_t s);
+                                bool is_global, int window, const int2* row_tb, void* o, unsigned int* status,
+                                cudaStream_t s);
 
 // Self-test of the bounded waits: a wait on a barrier nothing completes, limited
 // to `limit_cycles`; its expiry sets TEE_STATUS_TIMEOUT in `status`.
