@@ -322,3 +322,53 @@ def test_geglu_epilogue_gelu_dense_range(lib):
     assert np.all(got[a == 0.0] == 0.0)
     # misaligned buffers are refused before any launch
     assert lib.tee_selftest_gelu(d_a.data_ptr() + 2, d_y.data_ptr(), 4, 0) == binding.TEE_EINVAL
+
+
+# ---------------------------------------------------------------------------
+# residual projection + the LayerNorm after it in one launch (hidden 768:
+# clusters of four CTAs own whole rows)
+# ---------------------------------------------------------------------------
+
+H768 = synth.Shape(n_layers=2, hidden=768, n_heads=12, head_dim=64, intermediate=1024, vocab=1000)
+
+
+@pytest.fixture(scope="module")
+def h768(lib):
+    w = synth.make_weights(H768, seed=31, std=0.05)
+    enc = make_encoder(H768, "bf16", w, max_tokens=8192, max_texts=64)
+    model = oracle.OracleModel(w, H768, "bf16")
+    yield w, enc, model
+    enc.close()
+
+
+@pytest.mark.parametrize("T", [1, 37, 128, 820, 5000])
+@pytest.mark.parametrize("op,name,K", [("tee_op_out_proj_ln", "wo", 768), ("tee_op_ffn_out_ln", "wo_ffn", 1024)])
+def test_residual_projection_with_layernorm(h768, T, op, name, K):
+    """x += A W^T, then y = LayerNorm(x) (the feed-forward gain of layer 0 after
+    the attention output projection; the attention gain of layer 1 after the
+    feed-forward output projection).  x against the oracle's projection of the
+    same bf16 inputs; y against the oracle's LayerNorm of the GPU's own x, and
+    against the separate projection + LayerNorm steps."""
+    w, enc, model = h768
+    H = H768.hidden
+    rng = np.random.default_rng(T + K)
+    a, a_np = _act(rng.standard_normal((T, K)).astype(np.float32), "bf16")
+    x0 = rng.standard_normal((T, H)).astype(np.float32)
+    x = dev(x0)
+    y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    enc.op(op, 0, a, x, y, T, 0)
+    torch.cuda.synchronize()
+    x_ref = x0.astype(np.float64) + model.linear(name, 0, a_np)
+    assert_step_close(to_np(x), x_ref, "fp32")
+    gamma = model.ln_mlp[0] if name == "wo" else model.ln_attn[1]
+    y_ref = oracle.layernorm(to_np(x), gamma, H768.ln_eps)
+    assert_step_close(to_np(y), y_ref, "bf16", bf16_rel=8e-3)
+    # the same two steps run separately
+    x2 = dev(x0)
+    y2 = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    enc.op("tee_op_out_proj" if name == "wo" else "tee_op_ffn_out", 0, a, x2, T, 0)
+    enc.op("tee_op_layernorm", 1 if name == "wo_ffn" else 0, 0 if name == "wo_ffn" else 1, x2, y2, T, 0)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(to_np(x), to_np(x2), rtol=0, atol=2e-5)
+    np.testing.assert_allclose(to_np(y), to_np(y2), rtol=0, atol=2 ** -7 * (np.abs(to_np(y2)).max() + 1e-30))
+    assert enc.device_status() == 0
