@@ -65,21 +65,21 @@ struct Params {
 // residual epilogue stages each warp's whole 32 x BN fp32 slice of the
 // residual (BN/32 boxes of 32 x 32): TMA-loaded, updated in place, TMA-stored.
 // Residual epilogue: 32-column staging boxes per warp (a ring over the warp's
-// chunks: 4 for BN = 128, 3 for BN = 192).
+// chunks: 4 for BN = 128 and 256, 3 for BN = 192 and for the fused LayerNorm).
 template <int BN, int EPI>
 __host__ __device__ constexpr int res_round_boxes() {
-    // the fused LayerNorm keeps a two-box ring so that its own staging fits beside four ring stages
-    return EPI == GEMM_EPI_ADD_F32_LN ? 2 : (BN / 32 <= 4 ? BN / 32 : BN / 64);
+    return EPI == GEMM_EPI_ADD_F32_LN ? 3 : (BN / 32 <= 4 ? BN / 32 : BN / 64);
 }
 
-// ADD_F32_LN adds, after the residual ring, one 4 KB bf16 staging box per warp
-// for the normalised rows and the row-statistics exchange of the cluster:
-// [2 tile slots][4 CTAs][128 rows] of (mean, M2).
+// ADD_F32_LN adds, after the residual ring, the row-statistics exchange of the
+// cluster: [2 tile slots][4 CTAs][128 rows] of (mean, M2).  Its normalised
+// bf16 rows are staged in the ring box of the tile's last chunk, which is free
+// from the read of that chunk's store until the next tile's first refill.
 constexpr uint32_t LN_XCH_BYTES = 2u * 4u * 128u * 8u;
 template <int BN, int EPI>
 constexpr uint32_t staging_bytes() {
     return EPI == GEMM_EPI_ADD_F32      ? 4u * res_round_boxes<BN, EPI>() * 4096u
-           : EPI == GEMM_EPI_ADD_F32_LN ? 4u * res_round_boxes<BN, EPI>() * 4096u + 4u * 4096u + LN_XCH_BYTES
+           : EPI == GEMM_EPI_ADD_F32_LN ? 4u * res_round_boxes<BN, EPI>() * 4096u + LN_XCH_BYTES
                                         : 4u * 2u * 4096u;
 }
 
@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // chunks ahead, as soon as the store that last used the box has read it
         constexpr int RB = res_round_boxes<BN, EPI>();
         constexpr int NC = BN / 32;
+        static_assert(RB >= 2 && RB <= 4, "a warp has four residual barriers and four ring boxes at most");
         uint8_t* rslice = smem + S::OUT_OFF + (warp - 2) * RB * 4096;
         int last_issued[4] = {-1, -1, -1, -1};                     // lane 0: last chunk loaded into each box
         int res_done = 0;                                          // chunks consumed by this warp
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const float mean_c = sh + a1 / (float)BN;
                     const float m2_c = fmaxf(a2 - a1 * (a1 / (float)BN), 0.f);
                     const int slot = it & 1;
-                    float2* xs = reinterpret_cast<float2*>(smem + S::OUT_OFF + 4 * RB * 4096 + 4 * 4096) + slot * 512;
+                    float2* xs = reinterpret_cast<float2*>(smem + S::OUT_OFF + 4 * RB * 4096) + slot * 512;
                     xs[crank * 128 + row_local] = make_float2(mean_c, m2_c);
                     const uint32_t mine = smem_u32(xs + crank * 128 + row_local);
 #pragma unroll
@@ -444,7 +445,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const float rstd = 1.0f / sqrtf(m2 / (float)(4 * BN) + p.eps);
                     // second pass: the updated values from TMEM, normalised,
                     // times the gain, as bf16 through this warp's staging box
-                    uint8_t* ybox = smem + S::OUT_OFF + 4 * RB * 4096 + (warp - 2) * 4096;
+                    uint8_t* ybox = rslice + ((it * NC + NC - 1) % RB) * 4096;   // the last chunk's box
                     const float4* g4 = reinterpret_cast<const float4*>(p.gamma + n_t * BN);
 #pragma unroll 1
                     for (int gcol = 0; gcol < BN / 64; ++gcol) {
@@ -458,7 +459,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             w[4 * j + 2] = (w[4 * j + 2] - mean) * rstd * gm.z;
                             w[4 * j + 3] = (w[4 * j + 3] - mean) * rstd * gm.w;
                         }
-                        if (lane == 0) bulk_wait_read<0>();   // the box's previous store has read it
+                        if (lane == 0) bulk_wait_read<0>();   // the box's previous store (residual, or y) has read it
                         __syncwarp();
                         stage_row_bf16x64(ybox, lane, w);
                         fence_proxy_async_smem();

@@ -659,7 +659,8 @@ int tee_load_weights(tee_ctx* ctx, const tee_weights* w) {
     carve_weights(ctx, ctx->weight_arena);
 
     const size_t H = g.hidden, V = g.vocab;
-    size_t stage_elems = std::max({V * H, (size_t)2 * g.intermediate * H, (size_t)g.proj_dim * H});
+    // the largest host tensor staged: token embeddings, Wqkv, Wi (Wo_ffn is half of Wi) or the projection
+    size_t stage_elems = std::max({V * H, 3 * H * H, (size_t)2 * g.intermediate * H, (size_t)g.proj_dim * H});
     float* stage = nullptr;
     if (g.dtype != TEE_F32) CK(cudaMalloc(&stage, stage_elems * sizeof(float)));
     cudaStream_t s = ctx->stream;
@@ -670,6 +671,7 @@ int tee_load_weights(tee_ctx* ctx, const tee_weights* w) {
             CK(cudaMemcpy(dst, src, n * sizeof(float), cudaMemcpyHostToDevice));
             return TEE_OK;
         }
+        if (n > stage_elems) return fail(ctx, TEE_EINVAL, "weight staging: tensor larger than the staging buffer");
         CK(cudaMemcpyAsync(stage, src, n * sizeof(float), cudaMemcpyHostToDevice, s));
         if (kind == 1) CK(launch_convert_f32_bf16(stage, (bf16*)dst, n, s));
         else CK(launch_quant_weight_blocks(stage, (int8_t*)dst, dscale, N, K, weight_bits(g), s));
