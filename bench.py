@@ -72,7 +72,7 @@ def peaks():
 # kernel sources with this digest; otherwise reported as null.
 GEMM_TRAFFIC_BYTES = 233.59e6
 GEMM_TRAFFIC_SOURCES = ['text_embedding_encoder_gb300/csrc/k_gemm_tc.cu', 'text_embedding_encoder_gb300/csrc/tc_ptx.cuh', 'text_embedding_encoder_gb300/csrc/gemm_tc.cuh']
-GEMM_TRAFFIC_DIGEST = "07919e3a10071759"
+GEMM_TRAFFIC_DIGEST = "903f52d1e5c5edbc"
 
 
 def gemm_traffic():

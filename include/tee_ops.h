@@ -5,8 +5,7 @@
  * asynchronously on `stream` (a cudaStream_t, NULL = legacy default stream),
  * using the weights already loaded into `ctx`.  They exist so each step can
  * be checked against the CPU oracle and timed on its own; tee_encode_device
- * runs exactly these steps in this order (the residual projections with the
- * LayerNorm after them: tee_op_out_proj_ln, tee_op_ffn_out_ln).
+ * runs exactly these steps in this order.
  *
  * Activation buffers use the context's activation type ACT:
  *   TEE_F32 and the integer-path (TEE_W8A8, TEE_W6A8, TEE_W4A8) contexts: float;
@@ -78,23 +77,6 @@ int tee_op_ffn_in(tee_ctx* ctx, int layer, const void* d_y, void* d_z, int T, vo
 
 /* x float[T*H] += z ACT[T*I] Wo_ffn^T */
 int tee_op_ffn_out(tee_ctx* ctx, int layer, const void* d_z, float* d_x, int T, void* stream);
-
-/* The residual projections together with the LayerNorm that follows each in
- * the pass (§何が動くか / エンコーダ: pre-norm blocks):
- *   tee_op_out_proj_ln  x += o Wo^T, then y ACT[T*H] = LayerNorm(x) with the
- *                       feed-forward gain of `layer`;
- *   tee_op_ffn_out_ln   x += z Wo_ffn^T, then y = LayerNorm(x) with the
- *                       attention gain of layer + 1 (layer + 1 < n_layers, else
- *                       TEE_EINVAL).
- * Same results as tee_op_out_proj / tee_op_ffn_out followed by
- * tee_op_layernorm.  TEE_BF16 contexts with hidden 512, 768 or 1024 run each as
- * one tensor-core launch (clusters of four CTAs own whole rows, exchange the
- * rows' statistics and write the normalised bf16 rows from the residual
- * epilogue); other contexts run the two steps.  tee_encode_device runs these
- * in place of the separate projection and LayerNorm steps (all but the first
- * LayerNorm). */
-int tee_op_out_proj_ln(tee_ctx* ctx, int layer, const void* d_o, float* d_x, void* d_y, int T, void* stream);
-int tee_op_ffn_out_ln(tee_ctx* ctx, int layer, const void* d_z, float* d_x, void* d_y, int T, void* stream);
 
 /* Generic bf16 projection on the tensor cores: C = A W^T with A bf16[M*K],
  * W bf16[N*K] (both K-contiguous), fp32 accumulation; epilogue 0 stores C as

@@ -3,7 +3,8 @@
 Shapes: the tiny encoder (hidden 256), an odd one (hidden 384, 6 heads,
 GeGLU width 640) whose projections exercise the 128-column GEMM tiles, and a
 wide one (GeGLU width 1280) whose long-K output projection runs on 192-column
-tiles; token
+tiles, and a narrow one (hidden 768, GeGLU width 1024) whose Wqkv is the
+largest weight staged on load; token
 counts are ragged (not multiples of the 128-row tiles) and texts straddle
 tile edges.
 """
@@ -21,15 +22,17 @@ pytestmark = pytest.mark.gpu
 ODD = synth.Shape(n_layers=2, hidden=384, n_heads=6, head_dim=64, intermediate=640, vocab=1000)
 # a long GeGLU width: the feed-forward output projection (K = 1280) runs on 192-column tiles
 WIDE = synth.Shape(n_layers=2, hidden=384, n_heads=6, head_dim=64, intermediate=1280, vocab=1000)
+# a GeGLU narrower than 1.5 x hidden: Wqkv is the largest weight staged on load
+NARROW = synth.Shape(n_layers=2, hidden=768, n_heads=12, head_dim=64, intermediate=1024, vocab=1000)
 LENGTHS = [1, 2, 63, 64, 65, 66, 129, 127, 3, 300]   # 820 tokens
 
 
 @pytest.fixture(scope="module", params=[("tiny", "fp32"), ("tiny", "bf16"), ("odd", "bf16"), ("odd", "fp32"),
-                                        ("wide", "bf16")],
+                                        ("wide", "bf16"), ("narrow", "bf16")],
                 ids=lambda p: f"{p[0]}-{p[1]}")
 def setup(request, lib):
     name, dt = request.param
-    shape = {"tiny": synth.TINY, "odd": ODD, "wide": WIDE}[name]
+    shape = {"tiny": synth.TINY, "odd": ODD, "wide": WIDE, "narrow": NARROW}[name]
     w = synth.make_weights(shape, seed=11, std=0.05)
     enc = make_encoder(shape, dt, w, max_tokens=1024, max_texts=64)
     model = oracle.OracleModel(w, shape, dt)
@@ -322,53 +325,3 @@ def test_geglu_epilogue_gelu_dense_range(lib):
     assert np.all(got[a == 0.0] == 0.0)
     # misaligned buffers are refused before any launch
     assert lib.tee_selftest_gelu(d_a.data_ptr() + 2, d_y.data_ptr(), 4, 0) == binding.TEE_EINVAL
-
-
-# ---------------------------------------------------------------------------
-# residual projection + the LayerNorm after it in one launch (hidden 768:
-# clusters of four CTAs own whole rows)
-# ---------------------------------------------------------------------------
-
-H768 = synth.Shape(n_layers=2, hidden=768, n_heads=12, head_dim=64, intermediate=1024, vocab=1000)
-
-
-@pytest.fixture(scope="module")
-def h768(lib):
-    w = synth.make_weights(H768, seed=31, std=0.05)
-    enc = make_encoder(H768, "bf16", w, max_tokens=8192, max_texts=64)
-    model = oracle.OracleModel(w, H768, "bf16")
-    yield w, enc, model
-    enc.close()
-
-
-@pytest.mark.parametrize("T", [1, 37, 128, 820, 5000])
-@pytest.mark.parametrize("op,name,K", [("tee_op_out_proj_ln", "wo", 768), ("tee_op_ffn_out_ln", "wo_ffn", 1024)])
-def test_residual_projection_with_layernorm(h768, T, op, name, K):
-    """x += A W^T, then y = LayerNorm(x) (the feed-forward gain of layer 0 after
-    the attention output projection; the attention gain of layer 1 after the
-    feed-forward output projection).  x against the oracle's projection of the
-    same bf16 inputs; y against the oracle's LayerNorm of the GPU's own x, and
-    against the separate projection + LayerNorm steps."""
-    w, enc, model = h768
-    H = H768.hidden
-    rng = np.random.default_rng(T + K)
-    a, a_np = _act(rng.standard_normal((T, K)).astype(np.float32), "bf16")
-    x0 = rng.standard_normal((T, H)).astype(np.float32)
-    x = dev(x0)
-    y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
-    enc.op(op, 0, a, x, y, T, 0)
-    torch.cuda.synchronize()
-    x_ref = x0.astype(np.float64) + model.linear(name, 0, a_np)
-    assert_step_close(to_np(x), x_ref, "fp32")
-    gamma = model.ln_mlp[0] if name == "wo" else model.ln_attn[1]
-    y_ref = oracle.layernorm(to_np(x), gamma, H768.ln_eps)
-    assert_step_close(to_np(y), y_ref, "bf16", bf16_rel=8e-3)
-    # the same two steps run separately
-    x2 = dev(x0)
-    y2 = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-    enc.op("tee_op_out_proj" if name == "wo" else "tee_op_ffn_out", 0, a, x2, T, 0)
-    enc.op("tee_op_layernorm", 1 if name == "wo_ffn" else 0, 0 if name == "wo_ffn" else 1, x2, y2, T, 0)
-    torch.cuda.synchronize()
-    np.testing.assert_allclose(to_np(x), to_np(x2), rtol=0, atol=2e-5)
-    np.testing.assert_allclose(to_np(y), to_np(y2), rtol=0, atol=2 ** -7 * (np.abs(to_np(y2)).max() + 1e-30))
-    assert enc.device_status() == 0

@@ -82,8 +82,6 @@ SIGNATURES = {
     "tee_op_out_proj": (_i, [_ctx, _i, _vp, _vp, _i, _vp]),
     "tee_op_ffn_in": (_i, [_ctx, _i, _vp, _vp, _i, _vp]),
     "tee_op_ffn_out": (_i, [_ctx, _i, _vp, _vp, _i, _vp]),
-    "tee_op_out_proj_ln": (_i, [_ctx, _i, _vp, _vp, _vp, _i, _vp]),
-    "tee_op_ffn_out_ln": (_i, [_ctx, _i, _vp, _vp, _vp, _i, _vp]),
     "tee_op_pool_l2": (_i, [_ctx, _vp, _vp, _vp, _i, _vp, _vp]),
     "tee_op_gemm_bf16": (_i, [_ctx, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "tee_op_quant_rows7": (_i, [_ctx, _vp, _i, _i, _vp, _vp, _vp]),

@@ -10,8 +10,6 @@
 #define GEMM_EPI_ROPE_BF16  2   // QKV: rotate-half RoPE on columns < 2*hidden, store bf16
 #define GEMM_EPI_GEGLU      3   // W rows interleaved per 256-row tile as [128 GELU inputs | 128 gates];
                                 // C bf16 [M, N/2] = GELU(a) * g
-#define GEMM_EPI_ADD_F32_LN 4   // C float [M, N] += acc, then Y bf16 [M, N] = LayerNorm(C row) * gamma
-                                // (bias-free; N = 512, 768 or 1024: four CTAs of a cluster own a row block)
 
 struct GemmTcArgs {
     const void* A;              // bf16 [M, K], row-major, 16-byte aligned rows
@@ -24,14 +22,7 @@ struct GemmTcArgs {
     const float* rope_sin;
     int hidden;                 // ROPE: q and k occupy columns [0, 2*hidden)
     unsigned int* status;       // device status word: bounded waits set a timeout bit
-    const float* gamma;         // ADD_F32_LN: LayerNorm gain [N]
-    void* Y;                    // ADD_F32_LN: bf16 [M, N], 16-byte aligned
-    float eps;                  // ADD_F32_LN: inside the square root
 };
-
-// Whether launch_gemm_tc fuses the LayerNorm (GEMM_EPI_ADD_F32_LN) for this
-// width: four 128-, 192- or 256-column tiles per row.
-inline bool gemm_tc_ln_fusable(int N) { return N == 512 || N == 768 || N == 1024; }
 
 cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s);
 

@@ -56,8 +56,6 @@ struct Params {
     const float* rope_sin;
     int hidden;
     unsigned int* status;
-    const float* gamma;   // ADD_F32_LN: LayerNorm gain [N]
-    float eps;
 };
 
 // bf16-output epilogues stage each warp's 32 rows x 64 columns in a 4 KB
@@ -65,22 +63,13 @@ struct Params {
 // residual epilogue stages each warp's whole 32 x BN fp32 slice of the
 // residual (BN/32 boxes of 32 x 32): TMA-loaded, updated in place, TMA-stored.
 // Residual epilogue: 32-column staging boxes per warp (a ring over the warp's
-// chunks: 4 for BN = 128 and 256, 3 for BN = 192 and for the fused LayerNorm).
-template <int BN, int EPI>
-__host__ __device__ constexpr int res_round_boxes() {
-    return EPI == GEMM_EPI_ADD_F32_LN ? 3 : (BN / 32 <= 4 ? BN / 32 : BN / 64);
-}
+// chunks: 4 for BN = 128, 3 for BN = 192).
+template <int BN>
+__host__ __device__ constexpr int res_round_boxes() { return BN / 32 <= 4 ? BN / 32 : BN / 64; }
 
-// ADD_F32_LN adds, after the residual ring, the row-statistics exchange of the
-// cluster: [2 tile slots][4 CTAs][128 rows] of (mean, M2).  Its normalised
-// bf16 rows are staged in the ring box of the tile's last chunk, which is free
-// from the read of that chunk's store until the next tile's first refill.
-constexpr uint32_t LN_XCH_BYTES = 2u * 4u * 128u * 8u;
 template <int BN, int EPI>
 constexpr uint32_t staging_bytes() {
-    return EPI == GEMM_EPI_ADD_F32      ? 4u * res_round_boxes<BN, EPI>() * 4096u
-           : EPI == GEMM_EPI_ADD_F32_LN ? 4u * res_round_boxes<BN, EPI>() * 4096u + LN_XCH_BYTES
-                                        : 4u * 2u * 4096u;
+    return EPI == GEMM_EPI_ADD_F32 ? 4u * res_round_boxes<BN>() * 4096u : 4u * 2u * 4096u;
 }
 
 // How CTAs share the work of a tile.
@@ -91,24 +80,19 @@ constexpr uint32_t staging_bytes() {
 //     rows of the accumulator in tensor memory.  A stage carries a third less
 //     data per CTA than a single CTA's (so the ring gets more stages), and the
 //     weight tile is read from L2 once per 256 rows.
-//   MODE_ROW4: clusters of four own whole rows (N == 4 BN): CTA r of a cluster
-//     computes the 128 x BN tile in column block r of every row block the
-//     cluster takes, so the four CTAs together hold complete rows (one CTA per
-//     tile otherwise, M = 128 MMAs).
-constexpr int MODE_SINGLE = 0, MODE_PAIR = 2, MODE_ROW4 = 4;
+constexpr int MODE_SINGLE = 0, MODE_PAIR = 2;
 constexpr uint32_t SMEM_LIMIT = 227 * 1024;
 
 template <int BN, int EPI, int MODE>
 struct Smem {
     static constexpr uint32_t B_BYTES = (MODE == MODE_PAIR ? BN / 2 : BN) * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int LN_BARS = EPI == GEMM_EPI_ADD_F32_LN ? 2 : 0;   // exchange arrivals, by tile slot
-    static constexpr uint32_t FIXED = staging_bytes<BN, EPI>() + (2 * 8 + 5 + 16 + LN_BARS) * 8 + 16 + 1024;
+    static constexpr uint32_t FIXED = staging_bytes<BN, EPI>() + (2 * 8 + 5 + 16) * 8 + 16 + 1024;
     static constexpr int STAGES_FIT = (int)((SMEM_LIMIT - FIXED) / STAGE_BYTES);
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;   // as many as fit, at most 8
     static constexpr uint32_t OUT_OFF = STAGES * STAGE_BYTES;
     static constexpr uint32_t BAR_OFF = OUT_OFF + staging_bytes<BN, EPI>();
-    static constexpr uint32_t N_BARS = 2 * STAGES + 5 + 16 + LN_BARS;   // + one residual barrier per staging box (4 x 4)
+    static constexpr uint32_t N_BARS = 2 * STAGES + 5 + 16;   // + one residual barrier per staging box (4 x 4)
     static constexpr uint32_t TOTAL = BAR_OFF + N_BARS * 8 + 16 + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;   // a power of two >= 2 * BN
     static_assert(TOTAL <= SMEM_LIMIT, "shared memory");
@@ -117,12 +101,9 @@ struct Smem {
 template <int BN, int EPI, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY, Params p) {
+                   const __grid_constant__ CUtensorMap tmC, Params p) {
     using S = Smem<BN, EPI, MODE>;
-    constexpr bool PAIR = MODE == MODE_PAIR, ROW4 = MODE == MODE_ROW4, CL = MODE != MODE_SINGLE;
-    constexpr int CS = PAIR ? 2 : (ROW4 ? 4 : 1);   // CTAs per cluster
-    constexpr bool LN = EPI == GEMM_EPI_ADD_F32_LN;
-    constexpr bool RESID = EPI == GEMM_EPI_ADD_F32 || LN;
+    constexpr bool PAIR = MODE == MODE_PAIR, CL = MODE != MODE_SINGLE;
     constexpr int CG = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -133,19 +114,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto bar = [&](int i) { return smem_u32(bars + i); };
     // barrier indices
     const int FULL = 0, EMPTY = S::STAGES, TFULL = 2 * S::STAGES, TEMPTY = 2 * S::STAGES + 2, MMA_DONE = 2 * S::STAGES + 4,
-              RES = 2 * S::STAGES + 5, XR = 2 * S::STAGES + 21;
+              RES = 2 * S::STAGES + 5;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_m = (p.M + BM - 1) / BM, num_n = p.N / BN, num_k = p.K / BK;
-    // work units: one tile, (pairs) a pair of vertically adjacent tiles per
-    // cluster, or (ROW4) a row block per cluster, this CTA taking column block
-    // `crank` of it
+    // work units: one tile, or (clustered) a pair of vertically adjacent tiles per cluster
     const uint32_t crank = CL ? cluster_ctarank() : 0;
-    const int num_units = ROW4 ? num_m : (PAIR ? (num_m + 1) / 2 : num_m) * num_n;
-    const int unit0 = blockIdx.x / CS;
-    const int ustride = gridDim.x / CS;
-    auto unit_m = [&](int u) { return ROW4 ? u : (PAIR ? 2 * (u / num_n) + (int)crank : u / num_n); };
-    auto unit_n = [&](int u) { return ROW4 ? (int)crank : u % num_n; };
+    const int num_units = (CL ? (num_m + 1) / 2 : num_m) * num_n;
+    const int unit0 = CL ? blockIdx.x / 2 : blockIdx.x;
+    const int ustride = CL ? gridDim.x / 2 : gridDim.x;
+    auto unit_m = [&](int u) { return CL ? 2 * (u / num_n) + (int)crank : u / num_n; };
     // PAIR: the even CTA's barriers that both CTAs' copies and epilogues signal
     auto lead_bar = [&](int i) { return mapa_shared(bar(i), 0); };
 
@@ -160,14 +138,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(bar(MMA_DONE), 1);
         for (int w = 0; w < 16; ++w) mbar_init(bar(RES + w), 1);
-        if constexpr (LN)   // each slot: 128 rows' statistics from each of the three other CTAs
-            for (int b = 0; b < 2; ++b) mbar_init(bar(XR + b), 3 * 128);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC)) : "memory");
-        if constexpr (LN) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmY)) : "memory");
     }
     if (warp == 1) tmem_alloc<CG>(smem_u32(tmem_slot), S::TMEM_COLS);   // PAIR: both CTAs, collectively
     tc_fence_before();
@@ -194,7 +169,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr int PF = S::STAGES + 4;
             constexpr bool PREFETCH = !PAIR;
             for (int u = unit0; u < num_units && ok; u += ustride) {
-                const int n_t = unit_n(u), m_t = unit_m(u);
+                const int n_t = u % num_n, m_t = unit_m(u);
                 if (PREFETCH && num_k > S::STAGES)
                     for (int j = S::STAGES; j < PF && j < num_k; ++j) tma_prefetch_l2_2d(&tmA, j * BK, m_t * BM);
                 for (int kb = 0; kb < num_k; ++kb, ++g) {
@@ -287,7 +262,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // residual epilogue: chunk g (32 columns; g counts this warp's chunks
         // over its tiles) is staged in box g % RB; lane 0 issues its load RB - 1
         // chunks ahead, as soon as the store that last used the box has read it
-        constexpr int RB = res_round_boxes<BN, EPI>();
+        constexpr int RB = res_round_boxes<BN>();
         constexpr int NC = BN / 32;
         static_assert(RB >= 2 && RB <= 4, "a warp has four residual barriers and four ring boxes at most");
         uint8_t* rslice = smem + S::OUT_OFF + (warp - 2) * RB * 4096;
@@ -300,7 +275,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (u >= num_units) return;
             const int b = g % RB;
             mbar_expect_tx(res_bar(b), 4096);
-            tma_load_2d(smem_u32(rslice + b * 4096), &tmC, unit_n(u) * BN + c * 32, unit_m(u) * BM + quad * 32,
+            tma_load_2d(smem_u32(rslice + b * 4096), &tmC, (u % num_n) * BN + c * 32, unit_m(u) * BM + quad * 32,
                         res_bar(b));
             last_issued[b] = g;
         };
@@ -321,7 +296,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int it = 0;
         for (int u = unit0; u < num_units; u += ustride, ++it) {
             const int acc = it & 1, use = it >> 1;
-            const int n_t = unit_n(u), m_t = unit_m(u);
+            const int n_t = u % num_n, m_t = unit_m(u);
             const int gr = m_t * BM + row_local;
             const bool valid = gr < p.M;
             const int y_box = m_t * BM + quad * 32;
@@ -336,7 +311,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld64(taddr + col, v);
                     store64(v, n_t * BN + col, y_box);
                 }
-            } else if constexpr (RESID) {
+            } else if constexpr (EPI == GEMM_EPI_ADD_F32) {
                 // this warp's 32 x BN slice of the residual, one 32-column box
                 // per chunk: the box was TMA-loaded ahead of time, is updated in
                 // place, TMA-stored, and then refilled with the chunk RB ahead
@@ -345,11 +320,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
                 tc_fence_after();
                 bool ok = true;
-                // LN: sums of the row's updated values, shifted by its first one
-                // in this tile (keeps the second moment well conditioned); the
-                // updated values go back into the accumulator columns for the
-                // normalising pass
-                float sh = 0.f, s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
                 // chunk c + 1's accumulator columns are loaded from TMEM while
                 // chunk c is added and stored (two register sets, loop unrolled)
                 float v[2][32];
@@ -377,22 +347,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         o.z += v[c & 1][4 * k + 2];
                         o.w += v[c & 1][4 * k + 3];
                         *q = o;
-                        if constexpr (LN) {
-                            v[c & 1][4 * k + 0] = o.x;
-                            v[c & 1][4 * k + 1] = o.y;
-                            v[c & 1][4 * k + 2] = o.z;
-                            v[c & 1][4 * k + 3] = o.w;
-                        }
-                    }
-                    if constexpr (LN) {
-                        if (c == 0) sh = v[0][0];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float d = v[c & 1][i] - sh;
-                            s1[i & 3] += d;
-                            s2[i & 3] = fmaf(d, d, s2[i & 3]);
-                        }
-                        tmem_st32(taddr + c * 32, v[c & 1]);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -406,70 +360,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                if constexpr (LN) {
-                    // The row's statistics over this tile's BN columns -- mean
-                    // and M2 = sum of squared deviations -- go to the other
-                    // three CTAs of the cluster (which hold the rest of the row)
-                    // and theirs come here; combined as equal-sized groups:
-                    // mean = average of the four means, M2 = sum of the M2 +
-                    // BN * sum of the squared offsets of the means.  A slot is
-                    // rewritten two tiles later, after every CTA of the cluster
-                    // has received this tile's statistics from all the others.
-                    const float a1 = (s1[0] + s1[1]) + (s1[2] + s1[3]), a2 = (s2[0] + s2[1]) + (s2[2] + s2[3]);
-                    const float mean_c = sh + a1 / (float)BN;
-                    const float m2_c = fmaxf(a2 - a1 * (a1 / (float)BN), 0.f);
-                    const int slot = it & 1;
-                    float2* xs = reinterpret_cast<float2*>(smem + S::OUT_OFF + 4 * RB * 4096) + slot * 512;
-                    xs[crank * 128 + row_local] = make_float2(mean_c, m2_c);
-                    const uint32_t mine = smem_u32(xs + crank * 128 + row_local);
-#pragma unroll
-                    for (uint32_t d = 1; d < 4; ++d) {
-                        const uint32_t peer = (crank + d) & 3u;
-                        const uint32_t raddr = mapa_shared(mine, peer);
-                        asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(raddr), "f"(mean_c), "f"(m2_c)
-                                     : "memory");
-                        mbar_arrive_cluster(mapa_shared(bar(XR + slot), peer));
-                    }
-                    if (!mbar_wait_cluster(bar(XR + slot), (it >> 1) & 1, abort_flag)) break;
-                    float mean = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) mean += xs[q * 128 + row_local].x;
-                    mean *= 0.25f;
-                    float m2 = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 st = xs[q * 128 + row_local];
-                        const float dm = st.x - mean;
-                        m2 += st.y + (float)BN * dm * dm;
-                    }
-                    const float rstd = 1.0f / sqrtf(m2 / (float)(4 * BN) + p.eps);
-                    // second pass: the updated values from TMEM, normalised,
-                    // times the gain, as bf16 through this warp's staging box
-                    uint8_t* ybox = rslice + ((it * NC + NC - 1) % RB) * 4096;   // the last chunk's box
-                    const float4* g4 = reinterpret_cast<const float4*>(p.gamma + n_t * BN);
-#pragma unroll 1
-                    for (int gcol = 0; gcol < BN / 64; ++gcol) {
-                        float w[64];
-                        tmem_ld64(taddr + gcol * 64, w);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float4 gm = __ldg(g4 + gcol * 16 + j);
-                            w[4 * j + 0] = (w[4 * j + 0] - mean) * rstd * gm.x;
-                            w[4 * j + 1] = (w[4 * j + 1] - mean) * rstd * gm.y;
-                            w[4 * j + 2] = (w[4 * j + 2] - mean) * rstd * gm.z;
-                            w[4 * j + 3] = (w[4 * j + 3] - mean) * rstd * gm.w;
-                        }
-                        if (lane == 0) bulk_wait_read<0>();   // the box's previous store (residual, or y) has read it
-                        __syncwarp();
-                        stage_row_bf16x64(ybox, lane, w);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmY, smem_u32(ybox), n_t * BN + gcol * 64, y_box);
-                            bulk_commit();
-                        }
-                    }
-                }
             } else if constexpr (EPI == GEMM_EPI_ROPE_BF16) {
                 // q and k tiles (columns < 2*hidden; 2*hidden is a multiple of
                 // the tile width) rotate every head with the row's cos/sin,
@@ -527,7 +417,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (PAIR) mbar_arrive_cluster(lead_bar(TEMPTY + acc));
             else mbar_arrive(bar(TEMPTY + acc));
         }
-        if (RESID && lane == 0)   // residual loads still in flight land before exit
+        if (EPI == GEMM_EPI_ADD_F32 && lane == 0)   // residual loads still in flight land before exit
             for (int b = 0; b < RB; ++b)
                 if (last_issued[b] >= res_done) mbar_wait_drain(res_bar(b), (last_issued[b] / RB) & 1);
         if (lane == 0) bulk_wait_all();   // stores complete before the CTA exits
@@ -590,10 +480,9 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, int K, int box_rows) 
 }
 
 template <int BN, int EPI, int MODE>
-cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const CUtensorMap& my,
-                     const Params& p, int units, int dev, int num_sms, cudaStream_t s) {
+cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const Params& p, int units,
+                     int dev, int num_sms, cudaStream_t s) {
     constexpr bool CL = MODE != MODE_SINGLE;
-    constexpr int CS = MODE == MODE_PAIR ? 2 : (MODE == MODE_ROW4 ? 4 : 1);   // CTAs per cluster
     // per device: CTAs that can be resident at once (a multiple of 2 when
     // clustered), set together with the kernel's shared-memory attribute
     static std::mutex mu;
@@ -603,7 +492,7 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.x = CL ? 2 : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
@@ -621,19 +510,20 @@ cudaError_t launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
             if (e != cudaSuccess) return e;
             if (CL) {
                 int clusters = 0;
-                cfg.gridDim = dim3(CS * (num_sms / CS));
+                cfg.gridDim = dim3(2 * num_sms);
                 e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
                 if (e != cudaSuccess) return e;
-                max_grid_of[dev] = CS * (clusters > 0 ? clusters : 1);
+                max_grid_of[dev] = 2 * (clusters > 0 ? clusters : 1);
             } else {
                 max_grid_of[dev] = num_sms;
             }
         }
         max_grid = max_grid_of[dev];
     }
-    const int grid = units * CS < max_grid ? units * CS : max_grid;
+    const int per_unit = CL ? 2 : 1;
+    const int grid = units * per_unit < max_grid ? units * per_unit : max_grid;
     cfg.gridDim = dim3(grid);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ma, mb, mc, my, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ma, mb, mc, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -685,31 +575,14 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     if (g_init_err != cudaSuccess) return g_init_err;
     if (a.M < 0 || a.N <= 0 || a.K <= 0 || a.N % 128 || a.K % BK) return cudaErrorInvalidValue;
     if (a.epi == GEMM_EPI_GEGLU && a.N % 256) return cudaErrorInvalidValue;
-    if (a.epi < GEMM_EPI_STORE_BF16 || a.epi > GEMM_EPI_ADD_F32_LN) return cudaErrorInvalidValue;
+    if (a.epi < GEMM_EPI_STORE_BF16 || a.epi > GEMM_EPI_GEGLU) return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.W) | reinterpret_cast<uintptr_t>(a.C)) & 15)
         return cudaErrorMisalignedAddress;
-    if (a.epi == GEMM_EPI_ADD_F32_LN &&
-        (!gemm_tc_ln_fusable(a.N) || !a.gamma || !a.Y ||
-         ((reinterpret_cast<uintptr_t>(a.Y) | reinterpret_cast<uintptr_t>(a.gamma)) & 15)))
-        return cudaErrorInvalidValue;
     if (a.M == 0) return cudaSuccess;
     int dev = 0, num_sms = 0;
     cudaError_t de = tee_current_device(&dev, &num_sms);
     if (de != cudaSuccess) return de;
     const int num_m = (a.M + BM - 1) / BM;
-    if (a.epi == GEMM_EPI_ADD_F32_LN) {
-        // residual add and LayerNorm: 4-CTA clusters, one row block per cluster
-        const int bn = a.N / 4;
-        CUtensorMap ma, mb, mc_map, my;
-        if (!make_map(&ma, a.A, a.M, a.K, BM) || !make_map(&mb, a.W, a.N, a.K, bn) ||
-            !make_out_map(&mc_map, a.C, a.M, a.N, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32) ||
-            !make_out_map(&my, a.Y, a.M, a.N, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64))
-            return cudaErrorInvalidValue;
-        Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status, a.gamma, a.eps};
-        if (bn == 128) return launch_t<128, GEMM_EPI_ADD_F32_LN, MODE_ROW4>(ma, mb, mc_map, my, p, num_m, dev, num_sms, s);
-        if (bn == 192) return launch_t<192, GEMM_EPI_ADD_F32_LN, MODE_ROW4>(ma, mb, mc_map, my, p, num_m, dev, num_sms, s);
-        return launch_t<256, GEMM_EPI_ADD_F32_LN, MODE_ROW4>(ma, mb, mc_map, my, p, num_m, dev, num_sms, s);
-    }
     int BN = 128, pair = 0;
     gemm_tc_choose_tiles(a.M, a.N, a.K, a.epi, num_sms, &BN, &pair);
     const int mode = pair ? MODE_PAIR : MODE_SINGLE;
@@ -722,11 +595,11 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64)) {
         return cudaErrorInvalidValue;
     }
-    Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status, nullptr, 0.f};
+    Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status};
     const int units = (mode != MODE_SINGLE ? (num_m + 1) / 2 : num_m) * (a.N / BN);
-#define TEE_GEMM_DISPATCH(BN_, EPI_)                                                                          \
-    return mode == MODE_PAIR ? launch_t<BN_, EPI_, MODE_PAIR>(ma, mb, mc_map, mc_map, p, units, dev, num_sms, s) \
-                             : launch_t<BN_, EPI_, MODE_SINGLE>(ma, mb, mc_map, mc_map, p, units, dev, num_sms, s)
+#define TEE_GEMM_DISPATCH(BN_, EPI_)                                                                  \
+    return mode == MODE_PAIR ? launch_t<BN_, EPI_, MODE_PAIR>(ma, mb, mc_map, p, units, dev, num_sms, s)  \
+                             : launch_t<BN_, EPI_, MODE_SINGLE>(ma, mb, mc_map, p, units, dev, num_sms, s)
     if (a.epi == GEMM_EPI_ADD_F32 && BN == 256) TEE_GEMM_DISPATCH(256, GEMM_EPI_ADD_F32);
     if (a.epi == GEMM_EPI_ADD_F32 && BN == 192) TEE_GEMM_DISPATCH(192, GEMM_EPI_ADD_F32);
     if (BN == 256) {

@@ -361,41 +361,6 @@ int step_linear(tee_ctx* ctx, int layer, int which, const void* A, void* C, int 
     return TEE_OK;
 }
 
-// x += A W^T for projection `which` (TEE_W_OUT or TEE_W_FFN_OUT) of `layer`, then
-// y = LayerNorm(x) with gain `gamma`.  bf16 contexts whose hidden width splits
-// into four tiles run both in one tensor-core launch (the residual epilogue of
-// 4-CTA clusters that own whole rows normalises them); otherwise the two
-// steps run one after the other.
-int step_linear_ln(tee_ctx* ctx, int layer, int which, const void* A, float* x, const float* gamma, void* y, int T,
-                   cudaStream_t s) {
-    const tee_config& g = ctx->cfg;
-    int N, K;
-    wshape(g, which, &N, &K);
-    if (g.dtype == TEE_BF16 && gemm_tc_ln_fusable(N)) {
-        GemmTcArgs a{};
-        a.A = A;
-        a.W = ctx->layers[layer].w[which];
-        a.C = x;
-        a.M = T;
-        a.N = N;
-        a.K = K;
-        a.epi = GEMM_EPI_ADD_F32_LN;
-        a.hidden = g.hidden;
-        a.status = ctx->d_status;
-        a.gamma = gamma;
-        a.Y = y;
-        a.eps = g.ln_eps;
-        const double bytes = (double)T * K * 2 + (double)N * K * 2 + (double)T * N * (8 + 2);
-        LAUNCH(TEE_K_GEMM, 2.0 * T * N * K, bytes, launch_gemm_tc(a, s));
-        return TEE_OK;
-    }
-    int rc = step_linear(ctx, layer, which, A, x, T, 1, GEMM_EPI_ADD_F32, nullptr, s);
-    if (rc) return rc;
-    const double bytes = (double)T * g.hidden * (4 + act_size(ctx)) + g.hidden * 4.0;
-    LAUNCH(TEE_K_LAYERNORM, 0, bytes, launch_layernorm(x, gamma, y, act_is_bf16(ctx), T, g.hidden, g.ln_eps, s));
-    return TEE_OK;
-}
-
 int step_qkv(tee_ctx* ctx, int layer, const void* y, const int32_t* pos, void* qkv, int T, cudaStream_t s) {
     const tee_config& g = ctx->cfg;
     if (g.dtype == TEE_BF16) return step_linear(ctx, layer, TEE_W_QKV, y, qkv, T, 0, GEMM_EPI_ROPE_BF16, pos, s);
@@ -484,23 +449,14 @@ int run_layers(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const in
     LAUNCH(TEE_K_EMBED, 0, (double)T * g.hidden * (4.0 + (act_is_bf16(ctx) ? 2 : 4)) + T * 4.0,
            launch_embed(ctx->emb, act_is_bf16(ctx), d_ids, T, g.hidden, g.vocab, ctx->x, ctx->d_status, s));
     if (g.emb_norm && (rc = step_norm_in_place(ctx, ctx->ln_emb, T, s))) return rc;
-    // Each LayerNorm but the first runs with the residual projection before it
-    // (step_linear_ln): the attention LayerNorm of layer l + 1 with the
-    // feed-forward output projection of layer l, the feed-forward LayerNorm of
-    // layer l with its attention output projection.
-    if ((rc = step_layernorm(ctx, 0, TEE_LN_ATTN, ctx->x, ctx->y, T, s))) return rc;
     for (int l = 0; l < g.n_layers; ++l) {
-        const LayerWeights& L = ctx->layers[l];
+        if ((rc = step_layernorm(ctx, l, TEE_LN_ATTN, ctx->x, ctx->y, T, s))) return rc;
         if ((rc = step_qkv(ctx, l, ctx->y, ctx->d_pos, ctx->qkv, T, s))) return rc;
         if ((rc = step_attention(ctx, l, ctx->qkv, d_cu, h_cu, n_texts, T, ctx->o, s))) return rc;
-        if ((rc = step_linear_ln(ctx, l, TEE_W_OUT, ctx->o, ctx->x, L.ln_mlp, ctx->y, T, s))) return rc;
+        if ((rc = step_linear(ctx, l, TEE_W_OUT, ctx->o, ctx->x, T, 1, GEMM_EPI_ADD_F32, nullptr, s))) return rc;
+        if ((rc = step_layernorm(ctx, l, TEE_LN_MLP, ctx->x, ctx->y, T, s))) return rc;
         if ((rc = step_ffn_in(ctx, l, ctx->y, ctx->z, T, s))) return rc;
-        if (l + 1 < g.n_layers) {
-            if ((rc = step_linear_ln(ctx, l, TEE_W_FFN_OUT, ctx->z, ctx->x, ctx->layers[l + 1].ln_attn, ctx->y, T, s)))
-                return rc;
-        } else if ((rc = step_linear(ctx, l, TEE_W_FFN_OUT, ctx->z, ctx->x, T, 1, GEMM_EPI_ADD_F32, nullptr, s))) {
-            return rc;
-        }
+        if ((rc = step_linear(ctx, l, TEE_W_FFN_OUT, ctx->z, ctx->x, T, 1, GEMM_EPI_ADD_F32, nullptr, s))) return rc;
     }
     if (g.final_norm && (rc = step_norm_in_place(ctx, ctx->ln_final, T, s))) return rc;
     return TEE_OK;
@@ -957,26 +913,6 @@ int tee_op_ffn_out(tee_ctx* ctx, int layer, const void* d_z, float* d_x, int T, 
     if ((rc = check_dev(ctx, T, 16, {d_z, d_x}))) return rc;
     ON_DEVICE(ctx);
     return step_linear(ctx, layer, TEE_W_FFN_OUT, d_z, d_x, T, 1, GEMM_EPI_ADD_F32, nullptr, (cudaStream_t)stream);
-}
-
-int tee_op_out_proj_ln(tee_ctx* ctx, int layer, const void* d_o, float* d_x, void* d_y, int T, void* stream) {
-    int rc = check_ready(ctx);
-    if (rc || (rc = check_layer(ctx, layer))) return rc;
-    if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
-    if ((rc = check_dev(ctx, T, 16, {d_o, d_x, d_y}))) return rc;
-    ON_DEVICE(ctx);
-    return step_linear_ln(ctx, layer, TEE_W_OUT, d_o, d_x, ctx->layers[layer].ln_mlp, d_y, T, (cudaStream_t)stream);
-}
-
-int tee_op_ffn_out_ln(tee_ctx* ctx, int layer, const void* d_z, float* d_x, void* d_y, int T, void* stream) {
-    int rc = check_ready(ctx);
-    if (rc || (rc = check_layer(ctx, layer))) return rc;
-    if (layer + 1 >= ctx->cfg.n_layers) return fail(ctx, TEE_EINVAL, "the last layer has no next attention LayerNorm");
-    if (T < 0 || T > ctx->cfg.max_tokens) return fail(ctx, TEE_EINVAL, "bad T");
-    if ((rc = check_dev(ctx, T, 16, {d_z, d_x, d_y}))) return rc;
-    ON_DEVICE(ctx);
-    return step_linear_ln(ctx, layer, TEE_W_FFN_OUT, d_z, d_x, ctx->layers[layer + 1].ln_attn, d_y, T,
-                          (cudaStream_t)stream);
 }
 
 int tee_op_gemm_bf16(tee_ctx* ctx, const void* d_a, const void* d_w, void* d_c, int M, int N, int K, int epilogue,
