@@ -30,7 +30,10 @@
 //                   32-lane TMEM quadrant, so warps w and w+4 share one and
 //                   split the 128 key columns, and the 64 output dimensions,
 //                   in halves): one 64-column TMEM load of S, the mask as a
-//                   per-row interval of visible keys, the tile's row maximum
+//                   per-row interval of visible keys (on window layers first
+//                   decided for the whole warp per 32-column block: a block
+//                   that no row sees is skipped, one that every row sees is
+//                   not masked), the tile's row maximum
 //                   exchanged through shared memory with a pair barrier, the
 //                   softmax in fp32 with exp2 (scale folded into one FMA)
 //                   against a reference maximum that moves only when a tile's
@@ -81,7 +84,6 @@ struct AttnParams {
     int n_units;            // items x heads
     int n_heads;
     int hidden;
-    int is_global;
     int window;
     float scale_log2;       // log2(e) / sqrt(64)
     bf16* o;                // [T, hidden]
@@ -90,6 +92,38 @@ struct AttnParams {
 
 __device__ __forceinline__ int n_kv_tiles(const int4& it) { return (it.w - it.z + BKV - 1) / BKV; }
 
+// Row maximum of columns [B, E) of a thread's 64 scores, as eight partial
+// maxima (short dependency chains).
+template <int B, int E>
+__device__ __forceinline__ void max8(const float* v, float* m8) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m8[k] = v[B + k];
+#pragma unroll
+    for (int i = B + 8; i < E; ++i) m8[i & 7] = fmaxf(m8[i & 7], v[i]);
+}
+
+// p = 2^(s * scale_log2 - m) over columns [B, E): added to eight partial row
+// sums and packed as bf16 pairs (pk[c] holds columns 2c, 2c + 1).
+template <int B, int E>
+__device__ __forceinline__ void exp_pack(float* v, float sl2, float m, float* s8, uint32_t* pk) {
+#pragma unroll
+    for (int i = B; i < E; ++i) {
+        v[i] = ex2_approx(fmaf(v[i], sl2, -m));
+        s8[i & 7] += v[i];
+    }
+#pragma unroll
+    for (int c = B / 2; c < E / 2; ++c) pk[c] = pack_bf16(v[2 * c], v[2 * c + 1]);
+}
+
+template <int B, int E>
+__device__ __forceinline__ void zero_pack(uint32_t* pk) {
+#pragma unroll
+    for (int c = B / 2; c < E / 2; ++c) pk[c] = 0u;
+}
+
+// WINDOW: the ±window layers (per-row text bounds, 32-column block skipping);
+// otherwise the global layers, whose rows all see the same keys.
+template <bool WINDOW>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm, AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -303,11 +337,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             return true;
         };
 
+        // Work items are read two units ahead and (window layers) the row's
+        // text bounds one unit ahead, so neither load's latency lands on a
+        // unit's first tile.
+        auto row_bounds = [&](const int4& x) -> int2 {
+            return (WINDOW && r < x.y) ? p.row_tb[x.x + r] : make_int2(0, 0);
+        };
         int ui = 0;
         int4 it_next = p.items[blockIdx.x / p.n_heads];
+        int4 it_next2 = blockIdx.x + gridDim.x < p.n_units ? p.items[(blockIdx.x + gridDim.x) / p.n_heads]
+                                                           : make_int4(0, 0, 0, 0);
+        int2 tb_next = row_bounds(it_next);
         for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
             const int4 it = it_next;
-            if (u + gridDim.x < p.n_units) it_next = p.items[(u + gridDim.x) / p.n_heads];
+            const int2 tb = tb_next;
+            it_next = it_next2;
+            if (u + gridDim.x < p.n_units) tb_next = row_bounds(it_next);
+            if (u + 2 * gridDim.x < p.n_units) it_next2 = p.items[(u + 2 * gridDim.x) / p.n_heads];
             const int head = u % p.n_heads;
             const int q_start = it.x, q_len = it.y, k_lo = it.z, k_hi = it.w;
             const int nk = n_kv_tiles(it);
@@ -317,9 +363,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // layers, the window inside the row's own text otherwise (nothing
             // for rows past the end of the sequence)
             int vis_lo = k_lo, vis_hi = k_hi;
-            if (!p.is_global) {
+            if constexpr (WINDOW) {
                 if (r < q_len) {
-                    const int2 tb = p.row_tb[qg];
                     vis_lo = max(tb.x, qg - p.window);
                     vis_hi = min(tb.y, qg + p.window + 1);
                 } else {
@@ -329,6 +374,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float m_ref = -INFINITY, l = 0.f;
             for (int kt = 0; kt < nk; ++kt, ++t) {
                 const int sb = t % SP_BUFS;
+                const int key0 = k_lo + kt * BKV + half * 64;
+                const int lo = vis_lo - key0, hi = vis_hi - key0;   // visible columns [lo, hi)
+                // Window layers: the warp's 64 columns as two 32-column blocks,
+                // each decided for the whole warp (before S is ready: the
+                // decision needs no score): no row sees a key of it (skipped:
+                // no maximum, no exponentials, P = 0), every row sees all of it
+                // (no mask), or a mixed block (masked per element).  The band
+                // crosses one mixed block per pair of warps and tile.  Global
+                // layers: every block counts as seen (a tile past the text's
+                // end is masked per element).
+                bool any0 = true, any1 = true, all0 = true, all1 = true;
+                if constexpr (WINDOW) {
+                    any0 = __any_sync(0xffffffffu, lo < hi && lo < 32 && hi > 0);
+                    any1 = __any_sync(0xffffffffu, lo < hi && lo < 64 && hi > 32);
+                    all0 = __all_sync(0xffffffffu, lo <= 0 && hi >= 32);
+                    all1 = __all_sync(0xffffffffu, lo <= 32 && hi >= 64);
+                }
                 if (!mbar_wait(bar(B_SF + sb), (t / SP_BUFS) & 1, abort_flag)) {
                     ok = false;
                     break;
@@ -336,9 +398,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 float v[64];
                 tmem_ld64(tmem_base + lane_off + TM_S + sb * BKV + half * 64, v);
-                const int key0 = k_lo + kt * BKV + half * 64;
-                const int lo = vis_lo - key0, hi = vis_hi - key0;   // visible columns [lo, hi)
-                if (lo > 0 || hi < 64) {
+                if constexpr (WINDOW) {
+                    if (any0 && !all0) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < lo || i >= hi) v[i] = -INFINITY;
+                    }
+                    if (any1 && !all1) {
+#pragma unroll
+                        for (int i = 32; i < 64; ++i)
+                            if (i < lo || i >= hi) v[i] = -INFINITY;
+                    }
+                } else if (lo > 0 || hi < 64) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
                         if (i < lo || i >= hi) v[i] = -INFINITY;
@@ -346,10 +417,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // row maximum and (below) row sum over eight independent
                 // partials: short dependency chains for the latency-bound warps
                 float m8[8];
+                if (any0 && any1) {
+                    max8<0, 64>(v, m8);
+                } else if (any0) {
+                    max8<0, 32>(v, m8);
+                } else if (any1) {
+                    max8<32, 64>(v, m8);
+                } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) m8[k] = v[k];
-#pragma unroll
-                for (int i = 8; i < 64; ++i) m8[i & 7] = fmaxf(m8[i & 7], v[i]);
+                    for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+                }
                 float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 float* red_t = red + (t & 1) * 256;
@@ -385,20 +462,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
                 float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    v[i] = ex2_approx(fmaf(v[i], sl2, -m_use));
-                    s8[i & 7] += v[i];
-                }
-                const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
                 // P as bf16 pairs over the tile's first 64 S columns (the A
                 // operand of P V): this half's 64 keys are columns [32 * half,
                 // +32).  Both warps of the pair have read their S (the row
                 // maximum exchange above), so overwriting the other half's S
                 // columns is safe.
                 uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(v[2 * c], v[2 * c + 1]);
+                if (any0 && any1) {   // one loop over all 64 columns: the common case on global layers
+                    exp_pack<0, 64>(v, sl2, m_use, s8, pk);
+                } else {
+                    if (any0) exp_pack<0, 32>(v, sl2, m_use, s8, pk);
+                    else zero_pack<0, 32>(pk);
+                    if (any1) exp_pack<32, 64>(v, sl2, m_use, s8, pk);
+                    else zero_pack<32, 64>(pk);
+                }
+                const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
                 tmem_st32_u(tmem_base + lane_off + TM_S + sb * BKV + half * 32, pk);
                 tc_fence_before();
                 mbar_arrive(bar(B_PF + sb));
@@ -471,17 +549,21 @@ cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, cons
     {
         std::lock_guard<std::mutex> lock(g_attr_mu);
         if (!g_attr_set[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)SMEM_TOTAL);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_TOTAL);
             if (e != cudaSuccess) return e;
             g_attr_set[dev] = true;
         }
     }
     const int n_units = n_items * n_heads;
-    AttnParams p{d_items, row_tb, n_units, n_heads, H, is_global ? 1 : 0, window, 1.4426950408889634f / 8.0f,
+    AttnParams p{d_items, row_tb, n_units, n_heads, H, window, 1.4426950408889634f / 8.0f,
                  (bf16*)o, status};
     const int grid = n_units < num_sms ? n_units : num_sms;
-    cudaError_t e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_TOTAL, s, tm, p);
+    cudaError_t e = is_global ? launch_pdl(attn_tc_kernel<false>, dim3(grid), dim3(NUM_THREADS), SMEM_TOTAL, s, tm, p)
+                              : launch_pdl(attn_tc_kernel<true>, dim3(grid), dim3(NUM_THREADS), SMEM_TOTAL, s, tm, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
