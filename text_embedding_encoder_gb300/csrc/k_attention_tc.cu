@@ -93,26 +93,49 @@ struct AttnParams {
 __device__ __forceinline__ int n_kv_tiles(const int4& it) { return (it.w - it.z + BKV - 1) / BKV; }
 
 // Row maximum of columns [B, E) of a thread's 64 scores, as eight partial
-// maxima (short dependency chains).
+// maxima (partial k over the columns = k mod 8; short dependency chains),
+// three scores per max instruction.
 template <int B, int E>
 __device__ __forceinline__ void max8(const float* v, float* m8) {
+    static_assert((E - B) % 16 == 0, "whole groups of two per partial");
 #pragma unroll
-    for (int k = 0; k < 8; ++k) m8[k] = v[B + k];
+    for (int k = 0; k < 8; ++k) {
+        float m = fmaxf(v[B + k], v[B + k + 8]);
 #pragma unroll
-    for (int i = B + 8; i < E; ++i) m8[i & 7] = fmaxf(m8[i & 7], v[i]);
+        for (int i = B + k + 16; i < E; i += 16) m = fmax3(m, v[i], v[i + 8]);
+        m8[k] = m;
+    }
 }
 
-// p = 2^(s * scale_log2 - m) over columns [B, E): added to eight partial row
+// Eight partial row sums as four fp32x2 pairs: pair c & 3 takes columns 2c and
+// 2c + 1, so partial k again sums the columns = k mod 8.
+struct RowSum8 {
+    uint64_t s[4];
+    __device__ void zero() {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s[k] = 0ull;
+    }
+    __device__ float total() const {
+        float a[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) f2_unpack(s[k], a[2 * k], a[2 * k + 1]);
+        return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+    }
+};
+
+// p = 2^(s * scale_log2 - m) over columns [B, E): added to the partial row
 // sums and packed as bf16 pairs (pk[c] holds columns 2c, 2c + 1).
 template <int B, int E>
-__device__ __forceinline__ void exp_pack(float* v, float sl2, float m, float* s8, uint32_t* pk) {
+__device__ __forceinline__ void exp_pack(float* v, uint64_t sl2x2, uint64_t negm2, RowSum8& rs, uint32_t* pk) {
 #pragma unroll
-    for (int i = B; i < E; ++i) {
-        v[i] = ex2_approx(fmaf(v[i], sl2, -m));
-        s8[i & 7] += v[i];
+    for (int c = B / 2; c < E / 2; ++c) {
+        float a, b;
+        f2_unpack(f2_fma(f2_pack(v[2 * c], v[2 * c + 1]), sl2x2, negm2), a, b);
+        a = ex2_approx(a);
+        b = ex2_approx(b);
+        rs.s[c & 3] = f2_add(rs.s[c & 3], f2_pack(a, b));
+        pk[c] = pack_bf16(a, b);
     }
-#pragma unroll
-    for (int c = B / 2; c < E / 2; ++c) pk[c] = pack_bf16(v[2 * c], v[2 * c + 1]);
 }
 
 template <int B, int E>
@@ -303,6 +326,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float* red_l = reinterpret_cast<float*>(smem + OFF_REDL);   // [2][128]
         const uint32_t pair_bar = 1 + quad;             // named barrier of warps (w, w + 4)
         const float sl2 = p.scale_log2;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
         uint32_t t = 0;
         bool ok = true;
 
@@ -427,8 +451,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
                 }
-                float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                 float* red_t = red + (t & 1) * 256;
                 red_t[half * 128 + r] = mx;
                 pair_sync();
@@ -461,7 +484,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                const uint64_t negm2 = f2_pack(-m_use, -m_use);
+                RowSum8 rs;
+                rs.zero();
                 // P as bf16 pairs over the tile's first 64 S columns (the A
                 // operand of P V): this half's 64 keys are columns [32 * half,
                 // +32).  Both warps of the pair have read their S (the row
@@ -469,14 +494,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // columns is safe.
                 uint32_t pk[32];
                 if (any0 && any1) {   // one loop over all 64 columns: the common case on global layers
-                    exp_pack<0, 64>(v, sl2, m_use, s8, pk);
+                    exp_pack<0, 64>(v, sl2x2, negm2, rs, pk);
                 } else {
-                    if (any0) exp_pack<0, 32>(v, sl2, m_use, s8, pk);
+                    if (any0) exp_pack<0, 32>(v, sl2x2, negm2, rs, pk);
                     else zero_pack<0, 32>(pk);
-                    if (any1) exp_pack<32, 64>(v, sl2, m_use, s8, pk);
+                    if (any1) exp_pack<32, 64>(v, sl2x2, negm2, rs, pk);
                     else zero_pack<32, 64>(pk);
                 }
-                const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+                const float sum = rs.total();
                 tmem_st32_u(tmem_base + lane_off + TM_S + sb * BKV + half * 32, pk);
                 tc_fence_before();
                 mbar_arrive(bar(B_PF + sb));

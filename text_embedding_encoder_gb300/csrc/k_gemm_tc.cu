@@ -342,10 +342,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int k = 0; k < 8; ++k) {
                         float4* q = reinterpret_cast<float4*>(rp + ((k ^ (lane & 7)) << 4));
                         float4 o = *q;
-                        o.x += v[c & 1][4 * k + 0];
-                        o.y += v[c & 1][4 * k + 1];
-                        o.z += v[c & 1][4 * k + 2];
-                        o.w += v[c & 1][4 * k + 3];
+                        f2_unpack(f2_add(f2_pack(o.x, o.y), f2_pack(v[c & 1][4 * k + 0], v[c & 1][4 * k + 1])), o.x, o.y);
+                        f2_unpack(f2_add(f2_pack(o.z, o.w), f2_pack(v[c & 1][4 * k + 2], v[c & 1][4 * k + 3])), o.z, o.w);
                         *q = o;
                     }
                     fence_proxy_async_smem();
@@ -385,12 +383,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     float v[64];   // one head: v[j] pairs with v[j + 32]
                     tmem_ld64(taddr + col, v);
                     if (rope) {
+                        // two rotation pairs per packed fp32x2 step
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float a = v[j] * cs[j] - v[j + 32] * sn[j];
-                            const float b = v[j + 32] * cs[j] + v[j] * sn[j];
-                            v[j] = a;
-                            v[j + 32] = b;
+                        for (int j = 0; j < 32; j += 2) {
+                            const uint64_t A = f2_pack(v[j], v[j + 1]), B = f2_pack(v[j + 32], v[j + 33]);
+                            const uint64_t C = f2_pack(cs[j], cs[j + 1]);
+                            f2_unpack(f2_fma(A, C, f2_mul(B, f2_pack(-sn[j], -sn[j + 1]))), v[j], v[j + 1]);
+                            f2_unpack(f2_fma(B, C, f2_mul(A, f2_pack(sn[j], sn[j + 1]))), v[j + 32], v[j + 33]);
                         }
                     }
                     store64(v, n_t * BN + col, y_box);
@@ -409,7 +408,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_tie64(a);
                     tmem_tie64(gt);
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) a[j] = gelu_as(a[j]) * gt[j];
+                    for (int j = 0; j < 64; j += 2) gelu_mul2(a[j], a[j + 1], gt[j], gt[j + 1], a[j], a[j + 1]);
                     store64(a, n_t * (BN / 2) + col, y_box);
                 }
             }

@@ -468,6 +468,65 @@ __device__ __forceinline__ float gelu_as(float a) {
     return fmaf(-(x * t) * poly, e, fmaxf(a, 0.0f));
 }
 
+// Two fp32 lanes in one 64-bit register pair, for the packed fp32x2 FMA and
+// add of sm_100-class SMs (one instruction for two scores).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// GELU(a) * g for two lanes at once: gelu_as above, step for step and with
+// the same roundings, on the packed fp32x2 FMA and multiply (the sign of the
+// correction term folded into the negated, exactly halved coefficients).
+__device__ __forceinline__ void gelu_mul2(float a0, float a1, float g0, float g1, float& y0, float& y1) {
+    constexpr float P = 0.3275911f * 0.70710678118654752f;
+    constexpr float N1 = -0.5f * 0.254829592f, N2 = -0.5f * -0.284496736f, N3 = -0.5f * 1.421413741f,
+                    N4 = -0.5f * -1.453152027f, N5 = -0.5f * 1.061405429f;   // -a1/2 .. -a5/2
+    constexpr float NEG_HALF_LOG2E = -0.72134752044448170f;
+    const float x0 = fabsf(a0), x1 = fabsf(a1);
+    const uint64_t X = f2_pack(x0, x1), A = f2_pack(a0, a1);
+    float u0, u1;
+    f2_unpack(f2_fma(X, f2_pack(P, P), f2_pack(1.0f, 1.0f)), u0, u1);
+    float t0, t1;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t0) : "f"(u0));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t1) : "f"(u1));
+    float w0, w1;
+    f2_unpack(f2_mul(f2_mul(A, A), f2_pack(NEG_HALF_LOG2E, NEG_HALF_LOG2E)), w0, w1);
+    const uint64_t E = f2_pack(ex2_approx(w0), ex2_approx(w1));
+    const uint64_t T = f2_pack(t0, t1);
+    uint64_t q = f2_fma(T, f2_pack(N5, N5), f2_pack(N4, N4));
+    q = f2_fma(T, q, f2_pack(N3, N3));
+    q = f2_fma(T, q, f2_pack(N2, N2));
+    q = f2_fma(T, q, f2_pack(N1, N1));                   // -poly
+    q = f2_mul(f2_mul(X, T), q);                         // -(|a| t) poly
+    const uint64_t R = f2_fma(q, E, f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)));
+    f2_unpack(f2_mul(R, f2_pack(g0, g1)), y0, y1);
+}
+
 }  // namespace tc
 
 namespace tc {
