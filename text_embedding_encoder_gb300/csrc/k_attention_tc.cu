@@ -73,8 +73,8 @@ constexpr int SP_BUFS = 3;   // TMEM S/P buffers: tile t uses buffer t % 3
 constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = B_KVF + KV_STAGES, B_SF = B_KVE + KV_STAGES,
               B_PF = B_SF + SP_BUFS, B_OF = B_PF + SP_BUFS, B_OE = B_OF + 2, B_DONE = B_OE + 2, N_BARS = B_DONE + 1;
 constexpr uint32_t OFF_RED = OFF_BAR + N_BARS * 8 + 16;       // row-maximum exchange: [2 tiles][2 halves][128 rows]
-constexpr uint32_t OFF_REDL = OFF_RED + 2 * 2 * 128 * 4;       // row-sum exchange: [2 halves][128 rows]
-constexpr uint32_t SMEM_TOTAL = OFF_REDL + 2 * 128 * 4 + 1024;
+constexpr uint32_t OFF_REDL = OFF_RED + 2 * 2 * 128 * 4;       // row-sum exchange: [2 units][2 halves][128 rows]
+constexpr uint32_t SMEM_TOTAL = OFF_REDL + 2 * 2 * 128 * 4 + 1024;
 constexpr uint32_t TMEM_COLS = 512;                 // S/P: 3 x 128 columns (by tile), O: 2 x 64 (by unit)
 constexpr uint32_t TM_S = 0, TM_O = SP_BUFS * BKV;
 
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int r = quad * 32 + lane;                 // query row of the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         float* red = reinterpret_cast<float*>(smem + OFF_RED);   // [2][2][128]
-        float* red_l = reinterpret_cast<float*>(smem + OFF_REDL);   // [2][128]
+        float* red_l = reinterpret_cast<float*>(smem + OFF_REDL);   // [2][2][128]
         const uint32_t pair_bar = 1 + quad;             // named barrier of warps (w, w + 4)
         const float sl2 = p.scale_log2;
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
@@ -334,25 +334,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         // The previous unit's output, deferred past the next unit's first
         // softmax: wait for its last P V, read this warp's 32 columns of O,
-        // release the buffer, combine the row sum with the partner, store.
+        // release the buffer, store O / l.  The pair's two halves of the row
+        // sum l travel with the next unit's first row-maximum exchange (slot
+        // by the unit's O buffer, so a slot is rewritten only after both warps
+        // have passed a later exchange); the last unit exchanges them itself.
         bool pend = false;
-        float l_p = 0.f;
+        float l_p = 0.f, l_tot_p = 0.f;
         uint32_t t_p = 0;
         int ub_p = 0;
         bf16* dst_p = nullptr;
-        auto finalize = [&]() -> bool {
+        auto finalize = [&](bool exchanged) -> bool {
             if (!mbar_wait(bar(B_OF + (t_p & 1)), (t_p >> 1) & 1, abort_flag)) return false;
             tc_fence_after();
             float o[32];
             tmem_ld32(tmem_base + lane_off + TM_O + ub_p * HD + half * 32, o);
             tc_fence_before();
             mbar_arrive(bar(B_OE + ub_p));
-            red_l[half * 128 + r] = l_p;
-            pair_sync();
-            const float l_tot = l_p + red_l[(half ^ 1) * 128 + r];
-            pair_sync();
+            if (!exchanged) {
+                red_l[(ub_p * 2 + half) * 128 + r] = l_p;
+                pair_sync();
+                l_tot_p = l_p + red_l[(ub_p * 2 + (half ^ 1)) * 128 + r];
+            }
             if (dst_p) {
-                const float inv = 1.0f / l_tot;
+                const float inv = 1.0f / l_tot_p;
 #pragma unroll
                 for (int d = 0; d < 32; ++d) o[d] *= inv;
                 store_bf16x32(dst_p, o);
@@ -454,8 +458,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                 float* red_t = red + (t & 1) * 256;
                 red_t[half * 128 + r] = mx;
+                const bool carry_l = kt == 0 && pend;   // the previous unit's row sum rides along
+                if (carry_l) red_l[(ub_p * 2 + half) * 128 + r] = l_p;
                 pair_sync();
                 mx = fmaxf(mx, red_t[(half ^ 1) * 128 + r]) * sl2;
+                if (carry_l) l_tot_p = l_p + red_l[(ub_p * 2 + (half ^ 1)) * 128 + r];
                 if (kt == 0) {
                     m_ref = mx;
                 } else {
@@ -507,7 +514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_arrive(bar(B_PF + sb));
                 l += sum;
                 // the previous unit's output, once this tile's P is handed over
-                if (kt == 0 && pend && !finalize()) {
+                if (kt == 0 && pend && !finalize(true)) {
                     ok = false;
                     break;
                 }
@@ -519,7 +526,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             dst_p = r < q_len ? p.o + (size_t)qg * p.hidden + head * HD + half * 32 : nullptr;
             pend = true;
         }
-        if (ok && pend) finalize();
+        if (ok && pend) finalize(false);
     }
 
     tc_fence_before();
