@@ -178,10 +178,15 @@ int tee_selftest_gelu(const float* d_a, float* d_y, long long n, void* stream);
  * §エンコーダ: the whole text on global layers, +-window tokens otherwise), each
  * {q_start, q_len, k_lo, k_hi}: a tile of up to 128 queries and the key range
  * [k_lo, k_hi) that any of its queries may see.
- *   is_global != 0: one item per (text j, 128-query tile) -- q_start = cu[j] +
- *     128 i, q_len = min(128, cu[j+1] - q_start), [k_lo, k_hi) = [cu[j],
- *     cu[j+1]) -- ordered by q_len * (k_hi - k_lo), largest first, ties in text
- *     order.
+ *   is_global != 0: a text longer than 128 tokens gives one item per
+ *     128-query tile -- q_start = cu[j] + 128 i, q_len = min(128, cu[j+1] -
+ *     q_start), [k_lo, k_hi) = [cu[j], cu[j+1]); texts of at most 128 tokens
+ *     are taken in text order and grouped greedily, each group the longest run
+ *     of consecutive such texts spanning at most 128 tokens, one item per group
+ *     with q_start = k_lo = its first token, k_hi = its end, q_len = k_hi -
+ *     k_lo.  Ordered by q_len * (k_hi - k_lo), largest first, ties in text
+ *     order.  (Where texts share an item, the kernel masks each row to its
+ *     own text.)
  *   is_global == 0: one item per 128-query tile of the packed sequence itself
  *     (q_start = 128 i, q_len = min(128, T - q_start), T = cu[n_texts]), tiles
  *     shared by consecutive texts; k_lo = max(start of the text holding row

@@ -1,8 +1,9 @@
 """Host-side planning of a pass, checked without a GPU through the C ABI.
 
 tee_plan_attention: the attention work items (global layers: one per text
-and 128-query tile; window layers: one per 128-row tile of the packed
-sequence) with the key range the tile's queries may see, compared with a
+and 128-query tile, consecutive texts spanning at most 128 tokens sharing one;
+window layers: one per 128-row tile of the packed sequence) with the key range
+the tile's queries may see, compared with a
 brute force over every query row of the tile (whole text on global layers,
 |i - j| <= window inside the text otherwise).  tee_plan_gemm: the tensor-core
 GEMM's tile shapes for the projections of the 310m shape, pinned to values
@@ -63,10 +64,21 @@ def _brute_force_items(cu, window, is_global):
         items.append((q0, ql, int(cols.min()), int(cols.max()) + 1))
 
     if is_global:
-        for j in range(len(cu) - 1):
+        n = len(cu) - 1
+        j = 0
+        while j < n:
             s0, s1 = int(cu[j]), int(cu[j + 1])
-            for q0 in range(s0, s1, 128):
-                add(q0, min(128, s1 - q0))
+            if s1 - s0 <= 128:
+                # consecutive texts of <= 128 tokens share a tile while their span fits
+                k = j + 1
+                while k < n and int(cu[k + 1]) - s0 <= 128:
+                    k += 1
+                add(s0, int(cu[k]) - s0)
+                j = k
+            else:
+                for q0 in range(s0, s1, 128):
+                    add(q0, min(128, s1 - q0))
+                j += 1
         items = sorted(items, key=lambda it: -it[1] * (it[3] - it[2]))   # most work first, stable
     else:
         T = int(cu[-1])

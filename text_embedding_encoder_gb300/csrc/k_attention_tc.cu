@@ -7,9 +7,10 @@
 //
 // Work unit = (128-query tile, head).  The host lists the query tiles with
 // their key range [k_lo, k_hi): on global layers the tiles of each text (keys =
-// the text), longest first; on window layers the tiles of the packed sequence
-// itself, so short texts share a tile instead of padding one each, with every
-// row masked to its own text through the per-token text bounds row_tb.  The
+// the text), with consecutive texts that together span at most 128 tokens
+// sharing one tile, longest first; on window layers the tiles of the packed
+// sequence itself.  Where texts share a tile, every row is masked to its own
+// text through the per-token text bounds row_tb.  The
 // kernel is persistent: one CTA per SM walks the units u = blockIdx.x,
 // blockIdx.x + gridDim.x, ...  Ten warps:
 //   warp 0 lane 0   TMA: each unit's Q tile (double-buffered, so the next
@@ -80,7 +81,7 @@ constexpr uint32_t TM_S = 0, TM_O = SP_BUFS * BKV;
 
 struct AttnParams {
     const int4* items;      // {q_start, q_len, k_lo, k_hi} per query tile
-    const int2* row_tb;     // per token: {start, end} of its text (window layers)
+    const int2* row_tb;     // per token: {start, end} of its text
     int n_units;            // items x heads
     int n_heads;
     int hidden;
@@ -365,11 +366,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             return true;
         };
 
-        // Work items are read two units ahead and (window layers) the row's
-        // text bounds one unit ahead, so neither load's latency lands on a
-        // unit's first tile.
+        // Work items are read two units ahead and the row's text bounds one
+        // unit ahead, so neither load's latency lands on a unit's first tile.
         auto row_bounds = [&](const int4& x) -> int2 {
-            return (WINDOW && r < x.y) ? p.row_tb[x.x + r] : make_int2(0, 0);
+            return r < x.y ? p.row_tb[x.x + r] : make_int2(0, 0);
         };
         int ui = 0;
         int4 it_next = p.items[blockIdx.x / p.n_heads];
@@ -387,9 +387,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int nk = n_kv_tiles(it);
             const int qg = q_start + r;
             const int ub = ui & 1;
-            // keys visible to this row: [vis_lo, vis_hi) -- the text on global
-            // layers, the window inside the row's own text otherwise (nothing
-            // for rows past the end of the sequence)
+            // keys visible to this row: [vis_lo, vis_hi) -- the row's text on
+            // global layers, the window inside the row's own text otherwise
+            // (nothing for window rows past the end of the sequence)
             int vis_lo = k_lo, vis_hi = k_hi;
             if constexpr (WINDOW) {
                 if (r < q_len) {
@@ -398,6 +398,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 } else {
                     vis_hi = vis_lo;
                 }
+            } else if (r < q_len) {   // a tile shared by short texts: the row's own text
+                vis_lo = max(k_lo, tb.x);
+                vis_hi = min(k_hi, tb.y);
             }
             float m_ref = -INFINITY, l = 0.f;
             for (int kt = 0; kt < nk; ++kt, ++t) {
@@ -565,7 +568,7 @@ cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, cons
     if (n_items == 0 || T == 0) return cudaSuccess;
     if (H != n_heads * HD || (reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(o) & 15))
         return cudaErrorInvalidValue;
-    if (!is_global && !row_tb) return cudaErrorInvalidValue;
+    if (!row_tb) return cudaErrorInvalidValue;
     CUtensorMap tm;
     cuuint64_t dims[2] = {(cuuint64_t)3 * H, (cuuint64_t)T};
     cuuint64_t strides[1] = {(cuuint64_t)3 * H * 2};

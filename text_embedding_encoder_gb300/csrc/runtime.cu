@@ -224,9 +224,20 @@ double attention_pairs(const int32_t* h_cu, int n_texts, bool is_global, int w) 
 // its own text in the kernel.
 void plan_attention_items(const int32_t* h_cu, int n_texts, int w, std::vector<int4> (&items)[2]) {
     for (int b = 0; b < 2; ++b) items[b].clear();
-    for (int j = 0; j < n_texts; ++j) {
+    // global layers: a text's 128-query tiles, keys = the text; consecutive
+    // texts that together span at most 128 tokens share one tile (keys = their
+    // span; the kernel masks each row to its own text)
+    for (int j = 0; j < n_texts;) {
         const int s0 = h_cu[j], s1 = h_cu[j + 1];
+        if (s1 - s0 <= 128) {
+            int k = j + 1;
+            while (k < n_texts && h_cu[k + 1] - s0 <= 128) ++k;
+            items[0].push_back(make_int4(s0, h_cu[k] - s0, s0, h_cu[k]));
+            j = k;
+            continue;
+        }
         for (int q0 = s0; q0 < s1; q0 += 128) items[0].push_back(make_int4(q0, std::min(128, s1 - q0), s0, s1));
+        ++j;
     }
     std::stable_sort(items[0].begin(), items[0].end(), [](const int4& a, const int4& b) {
         const long long ca = (long long)a.y * (a.w - a.z), cb = (long long)b.y * (b.w - b.z);
