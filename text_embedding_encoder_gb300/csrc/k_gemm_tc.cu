@@ -63,9 +63,10 @@ struct Params {
 // residual epilogue stages each warp's whole 32 x BN fp32 slice of the
 // residual (BN/32 boxes of 32 x 32): TMA-loaded, updated in place, TMA-stored.
 // Residual epilogue: 32-column staging boxes per warp (a ring over the warp's
-// chunks: 4 for BN = 128, 3 for BN = 192).
+// chunks: 4 for BN = 128, 192 and 256).
+constexpr int RES_BOXES_MAX = 4;   // residual ring boxes (and barriers) per epilogue warp, at most
 template <int BN>
-__host__ __device__ constexpr int res_round_boxes() { return BN / 32 <= 4 ? BN / 32 : BN / 64; }
+__host__ __device__ constexpr int res_round_boxes() { return BN / 32 <= 4 ? BN / 32 : (BN == 192 ? 4 : BN / 64); }
 
 template <int BN, int EPI>
 constexpr uint32_t staging_bytes() {
@@ -87,12 +88,12 @@ template <int BN, int EPI, int MODE>
 struct Smem {
     static constexpr uint32_t B_BYTES = (MODE == MODE_PAIR ? BN / 2 : BN) * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t FIXED = staging_bytes<BN, EPI>() + (2 * 8 + 5 + 16) * 8 + 16 + 1024;
+    static constexpr uint32_t FIXED = staging_bytes<BN, EPI>() + (2 * 8 + 5 + 4 * RES_BOXES_MAX) * 8 + 16 + 1024;
     static constexpr int STAGES_FIT = (int)((SMEM_LIMIT - FIXED) / STAGE_BYTES);
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;   // as many as fit, at most 8
     static constexpr uint32_t OUT_OFF = STAGES * STAGE_BYTES;
     static constexpr uint32_t BAR_OFF = OUT_OFF + staging_bytes<BN, EPI>();
-    static constexpr uint32_t N_BARS = 2 * STAGES + 5 + 16;   // + one residual barrier per staging box (4 x 4)
+    static constexpr uint32_t N_BARS = 2 * STAGES + 5 + 4 * RES_BOXES_MAX;   // + a residual barrier per staging box
     static constexpr uint32_t TOTAL = BAR_OFF + N_BARS * 8 + 16 + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;   // a power of two >= 2 * BN
     static_assert(TOTAL <= SMEM_LIMIT, "shared memory");
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(TEMPTY + a), PAIR ? 256 : 128);   // every epilogue thread of the tile's CTAs
         }
         mbar_init(bar(MMA_DONE), 1);
-        for (int w = 0; w < 16; ++w) mbar_init(bar(RES + w), 1);
+        for (int w = 0; w < 4 * RES_BOXES_MAX; ++w) mbar_init(bar(RES + w), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -264,11 +265,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // chunks ahead, as soon as the store that last used the box has read it
         constexpr int RB = res_round_boxes<BN>();
         constexpr int NC = BN / 32;
-        static_assert(RB >= 2 && RB <= 4, "a warp has four residual barriers and four ring boxes at most");
+        static_assert(RB >= 2 && RB <= RES_BOXES_MAX, "a warp has RES_BOXES_MAX residual barriers and ring boxes");
         uint8_t* rslice = smem + S::OUT_OFF + (warp - 2) * RB * 4096;
-        int last_issued[4] = {-1, -1, -1, -1};                     // lane 0: last chunk loaded into each box
+        int last_issued[RES_BOXES_MAX];                            // lane 0: last chunk loaded into each box
+#pragma unroll
+        for (int b = 0; b < RES_BOXES_MAX; ++b) last_issued[b] = -1;
         int res_done = 0;                                          // chunks consumed by this warp
-        auto res_bar = [&](int b) { return bar(RES + (warp - 2) * 4 + b); };
+        auto res_bar = [&](int b) { return bar(RES + (warp - 2) * RES_BOXES_MAX + b); };
         auto issue_res_load = [&](int g) {                         // lane 0; box g % RB is free
             const int k = g / NC, c = g % NC;
             const int u = unit0 + k * ustride;
