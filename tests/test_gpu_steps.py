@@ -8,6 +8,8 @@ largest weight staged on load; token
 counts are ragged (not multiples of the 128-row tiles) and texts straddle
 tile edges.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -250,7 +252,8 @@ def test_gemm_residual_short_k_tile_choices(lib, M):
 @pytest.mark.parametrize("M", [2048, 8192, 20000])
 def test_gemm_residual_long_k_tile_choices(lib, M):
     # the FFN out-projection shape at row counts whose wave model picks single
-    # CTAs on 128 columns (2048), CTA pairs on 192 (8192) and on 256 (20000)
+    # CTAs on 128 columns (2048; every tile split into 3 parts of K), CTA pairs
+    # on 192 (8192) and on 256 (20000; the last 9 tiles split into 8 parts)
     N, K = 768, 3072
     enc = binding.Encoder(synth.TINY, "bf16", max_tokens=16, max_texts=4)
     rng = np.random.default_rng(M)
@@ -261,6 +264,30 @@ def test_gemm_residual_long_k_tile_choices(lib, M):
     enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 1, 0)
     ref = to_np(a) @ to_np(w).T
     np.testing.assert_allclose(to_np(c), c0.astype(np.float64) + ref, atol=2e-3 * max(1.0, np.abs(ref).max()))
+    enc.close()
+
+
+def test_gemm_residual_split_tail_full_size(lib):
+    """The FFN out-projection at 32768 rows: 384 CTA-pair tiles, of which the
+    last 4 (a round of 4 on 76 SM pairs) are split into 12 parts of K that add
+    into the residual; every row against an fp64 product on the GPU."""
+    M, N, K = 32768, 768, 3072
+    st = ctypes.c_int(-1)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    parts = lib.tee_plan_gemm_ksplit(M, N, K, 1, sms, ctypes.byref(st))
+    if sms == 152:
+        assert (parts, st.value) == (12, 4)
+    enc = binding.Encoder(synth.TINY, "bf16", max_tokens=16, max_texts=4)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    a = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    w = (torch.randn(N, K, device="cuda", generator=g) * 0.05).to(torch.bfloat16)
+    c0 = torch.randn(M, N, device="cuda", generator=g)
+    c = c0.clone()
+    enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 1, 0)
+    torch.cuda.synchronize()
+    ref = c0.double() + a.double() @ w.double().T
+    err = (c.double() - ref).abs().max().item()
+    assert err <= 2e-3 * max(1.0, (ref - c0.double()).abs().max().item()), err
     enc.close()
 
 

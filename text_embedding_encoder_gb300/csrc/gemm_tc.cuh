@@ -33,9 +33,10 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s);
 // arguments as launch_gemm_tc accepts them).
 void gemm_tc_choose_tiles(int M, int N, int K, int epi, int num_sms, int* bn, int* pair);
 
-// Parts of K that launch_gemm_tc splits a residual-add product into (1 = no
-// split; > 1 only when the tiles leave SMs idle), host only.
-int gemm_tc_choose_ksplit(int M, int N, int K, int epi, int num_sms);
+// Parts of K into which launch_gemm_tc splits the last *split_tiles tiles of a
+// residual-add product (1 and 0 = no split; only where tiles would leave SMs
+// idle), host only.
+int gemm_tc_choose_split(int M, int N, int K, int epi, int num_sms, int* split_tiles);
 
 // Row permutation of Wi used by GEMM_EPI_GEGLU: stored row r holds original row
 // geglu_source_row(r, I).

@@ -56,7 +56,8 @@ struct Params {
     const float* rope_sin;
     int hidden;
     unsigned int* status;
-    int ksplit;       // ADD_F32: K is split into ksplit equal parts, each added into C by its own unit
+    int n_full;       // ADD_F32: tiles [0, n_full) take all of K; each later tile is split into
+    int parts;        //   `parts` equal parts of K, each a unit that adds its share into C
 };
 
 // bf16-output epilogues stage each warp's 32 rows x 64 columns in a 4 KB
@@ -121,18 +122,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_m = (p.M + BM - 1) / BM, num_n = p.N / BN, num_k = p.K / BK;
     // work units: one tile, or (clustered) a pair of vertically adjacent tiles
-    // per cluster; with a split K, (tile, part) -- unit u takes tile u %
-    // num_tiles and k-blocks [kc * (u / num_tiles), +kc)
+    // per cluster.  ADD_F32 may split the tiles from n_full on into `parts`
+    // parts of K: unit u < n_full is tile u; later units are (tile, part),
+    // parts of a tile consecutive, each with num_k / parts k-blocks.
     const uint32_t crank = CL ? cluster_ctarank() : 0;
     const int num_tiles = (CL ? (num_m + 1) / 2 : num_m) * num_n;
-    const int ksplit = EPI == GEMM_EPI_ADD_F32 ? p.ksplit : 1;
-    const int kc = num_k / ksplit;
-    const int num_units = num_tiles * ksplit;
+    const int parts = EPI == GEMM_EPI_ADD_F32 ? p.parts : 1;
+    const int n_full = EPI == GEMM_EPI_ADD_F32 ? p.n_full : num_tiles;
+    const int kc_part = num_k / parts;
+    const int num_units = n_full + (num_tiles - n_full) * parts;
     const int unit0 = CL ? blockIdx.x / 2 : blockIdx.x;
     const int ustride = CL ? gridDim.x / 2 : gridDim.x;
-    auto unit_n = [&](int u) { return (u % num_tiles) % num_n; };
-    auto unit_m = [&](int u) { return CL ? 2 * ((u % num_tiles) / num_n) + (int)crank : (u % num_tiles) / num_n; };
-    auto unit_k0 = [&](int u) { return kc * (u / num_tiles); };
+    auto unit_tile = [&](int u) { return u < n_full ? u : n_full + (u - n_full) / parts; };
+    auto unit_n = [&](int u) { return unit_tile(u) % num_n; };
+    auto unit_m = [&](int u) { return CL ? 2 * (unit_tile(u) / num_n) + (int)crank : unit_tile(u) / num_n; };
+    auto unit_k0 = [&](int u) { return u < n_full ? 0 : ((u - n_full) % parts) * kc_part; };
+    auto unit_kc = [&](int u) { return u < n_full ? num_k : kc_part; };
     // PAIR: the even CTA's barriers that both CTAs' copies and epilogues signal
     auto lead_bar = [&](int i) { return mapa_shared(bar(i), 0); };
 
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr int PF = S::STAGES + 4;
             constexpr bool PREFETCH = !PAIR;
             for (int u = unit0; u < num_units && ok; u += ustride) {
-                const int n_t = unit_n(u), m_t = unit_m(u), kb0 = unit_k0(u), kb1 = kb0 + kc;
+                const int n_t = unit_n(u), m_t = unit_m(u), kc = unit_kc(u), kb0 = unit_k0(u), kb1 = kb0 + kc;
                 if (PREFETCH && kc > S::STAGES)
                     for (int j = S::STAGES; j < PF && j < kc; ++j) tma_prefetch_l2_2d(&tmA, (kb0 + j) * BK, m_t * BM);
                 for (int kb = kb0; kb < kb1; ++kb, ++g) {
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                const int kb0 = unit_k0(u), kb1 = kb0 + kc;
+                const int kb0 = unit_k0(u), kb1 = kb0 + unit_kc(u);
                 for (int kb = kb0; kb < kb1; ++kb, ++g) {
                     const int s = g % S::STAGES;
                     const uint32_t r = g / S::STAGES;
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         auto issue_res_load = [&](int g) {                         // lane 0; box g % RB is free
             const int k = g / NC, c = g % NC;
             const int u = unit0 + k * ustride;
-            if (u >= num_units) return;
+            if (u >= num_units || u >= n_full) return;   // a split unit adds, loading no residual
             const int b = g % RB;
             mbar_expect_tx(res_bar(b), 4096);
             tma_load_2d(smem_u32(rslice + b * 4096), &tmC, unit_n(u) * BN + c * 32, unit_m(u) * BM + quad * 32,
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     store64(v, n_t * BN + col, y_box);
                 }
             } else if constexpr (EPI == GEMM_EPI_ADD_F32) {
-                if (ksplit > 1) {
+                if (u >= n_full) {
                     // a part of a split K: its share of A W^T is added into the
                     // residual in L2 by TMA reduce-adds, 32 columns at a time
                     // through the same ring of staging boxes (no residual load)
@@ -614,29 +619,42 @@ void gemm_tc_choose_tiles(int M, int N, int K, int epi, int num_sms, int* bn, in
     *pair = mode == MODE_PAIR;
 }
 
-int gemm_tc_choose_ksplit(int M, int N, int K, int epi, int num_sms) {
-    // Residual add with fewer units than the SMs (or SM pairs) can hold at
-    // once: split K into equal parts (at least 4 k-blocks each, at most 8
-    // parts) so that more SMs work, each part adding its share into the
-    // residual.  The part count minimises rounds of units over the slots per
-    // unit of K -- ceil(units * parts / slots) / parts -- fewest parts on a
-    // tie, and must cut that cost by at least a fifth against no split (the
-    // reduce-adds cost more per tile than the fused residual update).
+int gemm_tc_choose_split(int M, int N, int K, int epi, int num_sms, int* split_tiles) {
+    // Residual add: tiles that would leave most slots (SMs, or SM pairs) idle
+    // in the last round of units are split into equal parts of K (at least 4
+    // k-blocks each), each part a unit that adds its share into the residual.
+    // Fewer tiles than slots: every tile is split, into the part count (2..8)
+    // that minimises rounds of units per unit of K -- ceil(tiles * parts /
+    // slots) / parts -- fewest parts on a tie, if that cost is at most 0.8
+    // (the reduce-adds cost more per tile than the fused residual update).
+    // Otherwise, a last round that fills at most half the slots: its tiles are
+    // split into the most parts (2..16) that still fit in one round.
+    *split_tiles = 0;
     if (epi != GEMM_EPI_ADD_F32 || M <= 0) return 1;
     int bn = 128, pair = 0;
     gemm_tc_choose_tiles(M, N, K, epi, num_sms, &bn, &pair);
     const int num_m = (M + BM - 1) / BM, num_k = K / BK;
-    const long units = (long)(pair ? (num_m + 1) / 2 : num_m) * (N / bn);
+    const long tiles = (long)(pair ? (num_m + 1) / 2 : num_m) * (N / bn);
     const long slots = pair ? num_sms / 2 : num_sms;
-    if (units >= slots) return 1;
     int best_parts = 1;
-    double best = 1.0;
-    for (int parts = 2; parts <= 8; ++parts) {
-        if (num_k % parts || num_k / parts < 4) continue;
-        const double c = (double)((units * parts + slots - 1) / slots) / parts;
-        if (c < best - 1e-9 && c <= 0.8) best = c, best_parts = parts;
+    if (tiles < slots) {
+        double best = 1.0;
+        for (int parts = 2; parts <= 8; ++parts) {
+            if (num_k % parts || num_k / parts < 4) continue;
+            const double c = (double)((tiles * parts + slots - 1) / slots) / parts;
+            if (c < best - 1e-9 && c <= 0.8) best = c, best_parts = parts;
+        }
+        if (best_parts > 1) *split_tiles = (int)tiles;
+        return best_parts;
     }
-    return best_parts;
+    const long tail = tiles % slots;
+    if (tail == 0 || 2 * tail > slots) return 1;
+    for (int parts = 16; parts >= 2; --parts) {
+        if (num_k % parts || num_k / parts < 4 || tail * parts > slots) continue;
+        *split_tiles = (int)tail;
+        return parts;
+    }
+    return 1;
 }
 
 cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
@@ -664,9 +682,11 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64)) {
         return cudaErrorInvalidValue;
     }
-    const int ksplit = gemm_tc_choose_ksplit(a.M, a.N, a.K, a.epi, num_sms);
-    Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status, ksplit};
-    const int units = (mode != MODE_SINGLE ? (num_m + 1) / 2 : num_m) * (a.N / BN) * ksplit;
+    int split_tiles = 0;
+    const int parts = gemm_tc_choose_split(a.M, a.N, a.K, a.epi, num_sms, &split_tiles);
+    const int tiles = (mode != MODE_SINGLE ? (num_m + 1) / 2 : num_m) * (a.N / BN);
+    Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status, tiles - split_tiles, parts};
+    const int units = tiles - split_tiles + split_tiles * parts;
 #define TEE_GEMM_DISPATCH(BN_, EPI_)                                                                  \
     return mode == MODE_PAIR ? launch_t<BN_, EPI_, MODE_PAIR>(ma, mb, mc_map, p, units, dev, num_sms, s)  \
                              : launch_t<BN_, EPI_, MODE_SINGLE>(ma, mb, mc_map, p, units, dev, num_sms, s)
