@@ -206,23 +206,6 @@ int tee_plan_attention(const int32_t* h_cu, int n_texts, int window, int is_glob
  * K % 64 == 0, num_sms >= 2. */
 int tee_plan_gemm(int M, int N, int K, int epi, int num_sms, int* bn, int* pair);
 
-/* How the bf16 tensor-core projection splits K for the same product
- * (arguments as tee_plan_gemm): returns the part count P and writes to
- * *split_tiles how many of its tiles -- the last ones in launch order -- are
- * split into P equal parts of K (1 and 0: no split).  Only the fp32 residual
- * add (epi 1) splits, with slots = num_sms (num_sms / 2 with *pair):
- *   fewer tiles than slots: every tile, into the P in 2..8 dividing K / 64
- *     with at least 4 blocks of 64 per part that minimises ceil(tiles * P /
- *     slots) / P, fewest parts on a tie, if that cost is at most 0.8;
- *   else, when the last round of tiles (tiles mod slots, nonzero) fills at
- *     most half the slots: those tiles, into the largest P in 2..16 dividing
- *     K / 64 with at least 4 blocks per part and tail * P <= slots.
- * Each part adds its share of A W^T into the residual with TMA reduce-adds,
- * so the order of those fp32 additions -- and the last bits of the result --
- * may differ between runs.  split_tiles must not be NULL.  TEE_EINVAL for
- * arguments tee_plan_gemm rejects. */
-int tee_plan_gemm_ksplit(int M, int N, int K, int epi, int num_sms, int* split_tiles);
-
 /* Synchronise the context's device status word: TEE_OK, or TEE_EINVAL if a
  * kernel met an out-of-range token id since the last call (the word is then
  * cleared), or TEE_ETIMEOUT if a bounded device wait gave up. */

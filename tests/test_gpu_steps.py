@@ -8,8 +8,6 @@ largest weight staged on load; token
 counts are ragged (not multiples of the 128-row tiles) and texts straddle
 tile edges.
 """
-import ctypes
-
 import numpy as np
 import pytest
 
@@ -232,63 +230,49 @@ def test_gemm_bf16_shapes(lib, M, N, K, epi):
     enc.close()
 
 
+# a context of the 310m widths (one layer)
+W768 = synth.Shape(n_layers=1, hidden=768, n_heads=12, head_dim=64, intermediate=3072, vocab=16)
+
+
+def _residual_gemm_twice(M, N, K, seed):
+    """C += A W^T through tee_op_gemm_bf16 in a W768 context, twice from the
+    same C: the two results must be bit-identical (every output element is
+    summed in one fixed order).  Returns (result, A, W, C0) as torch tensors."""
+    enc = binding.Encoder(W768, "bf16", max_tokens=M, max_texts=4)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    a = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    w = (torch.randn(N, K, device="cuda", generator=g) * 0.05).to(torch.bfloat16)
+    c0 = torch.randn(M, N, device="cuda", generator=g)
+    outs = []
+    for _ in range(2):
+        c = c0.clone()
+        enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 1, 0)
+        torch.cuda.synchronize()
+        outs.append(c)
+    enc.close()
+    assert torch.equal(outs[0], outs[1])
+    return outs[0], a, w, c0
+
+
+def _check_residual(c, a, w, c0):
+    ref = c0.double() + a.double() @ w.double().T
+    err = (c.double() - ref).abs().max().item()
+    assert err <= 2e-3 * max(1.0, (ref - c0.double()).abs().max().item()), err
+
+
 @pytest.mark.parametrize("M", [2048, 24000, 32768])
 def test_gemm_residual_short_k_tile_choices(lib, M):
     # the attention out-projection shape at row counts whose wave model picks
     # 128-column tiles (2048) and 192-column tiles (24000, 32768), one CTA each
-    N, K = 768, 768
-    enc = binding.Encoder(synth.TINY, "bf16", max_tokens=16, max_texts=4)
-    rng = np.random.default_rng(M + 1)
-    a = dev(rng.standard_normal((M, K)).astype(np.float32), torch.bfloat16)
-    w = dev((rng.standard_normal((N, K)) * 0.05).astype(np.float32), torch.bfloat16)
-    c0 = rng.standard_normal((M, N)).astype(np.float32)
-    c = dev(c0)
-    enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 1, 0)
-    ref = to_np(a) @ to_np(w).T
-    np.testing.assert_allclose(to_np(c), c0.astype(np.float64) + ref, atol=2e-3 * max(1.0, np.abs(ref).max()))
-    enc.close()
+    _check_residual(*_residual_gemm_twice(M, 768, 768, M + 1))
 
 
-@pytest.mark.parametrize("M", [2048, 8192, 20000])
+@pytest.mark.parametrize("M", [2048, 8192, 20000, 32768])
 def test_gemm_residual_long_k_tile_choices(lib, M):
     # the FFN out-projection shape at row counts whose wave model picks single
-    # CTAs on 128 columns (2048; every tile split into 3 parts of K), CTA pairs
-    # on 192 (8192) and on 256 (20000; the last 9 tiles split into 8 parts)
-    N, K = 768, 3072
-    enc = binding.Encoder(synth.TINY, "bf16", max_tokens=16, max_texts=4)
-    rng = np.random.default_rng(M)
-    a = dev(rng.standard_normal((M, K)).astype(np.float32), torch.bfloat16)
-    w = dev((rng.standard_normal((N, K)) * 0.05).astype(np.float32), torch.bfloat16)
-    c0 = rng.standard_normal((M, N)).astype(np.float32)
-    c = dev(c0)
-    enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 1, 0)
-    ref = to_np(a) @ to_np(w).T
-    np.testing.assert_allclose(to_np(c), c0.astype(np.float64) + ref, atol=2e-3 * max(1.0, np.abs(ref).max()))
-    enc.close()
-
-
-def test_gemm_residual_split_tail_full_size(lib):
-    """The FFN out-projection at 32768 rows: 384 CTA-pair tiles, of which the
-    last 4 (a round of 4 on 76 SM pairs) are split into 12 parts of K that add
-    into the residual; every row against an fp64 product on the GPU."""
-    M, N, K = 32768, 768, 3072
-    st = ctypes.c_int(-1)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    parts = lib.tee_plan_gemm_ksplit(M, N, K, 1, sms, ctypes.byref(st))
-    if sms == 152:
-        assert (parts, st.value) == (12, 4)
-    enc = binding.Encoder(synth.TINY, "bf16", max_tokens=16, max_texts=4)
-    g = torch.Generator(device="cuda").manual_seed(7)
-    a = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
-    w = (torch.randn(N, K, device="cuda", generator=g) * 0.05).to(torch.bfloat16)
-    c0 = torch.randn(M, N, device="cuda", generator=g)
-    c = c0.clone()
-    enc.op("tee_op_gemm_bf16", a, w, c, M, N, K, 1, 0)
-    torch.cuda.synchronize()
-    ref = c0.double() + a.double() @ w.double().T
-    err = (c.double() - ref).abs().max().item()
-    assert err <= 2e-3 * max(1.0, (ref - c0.double()).abs().max().item()), err
-    enc.close()
+    # CTAs on 128 columns (2048), CTA pairs on 192 (8192) and on 256 (20000,
+    # 32768: 384 pair tiles, the pass's own launch)
+    _check_residual(*_residual_gemm_twice(M, 768, 3072, M))
 
 
 def test_step_entry_points_reject_unaligned_and_null_buffers(lib):

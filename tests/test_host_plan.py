@@ -177,30 +177,6 @@ def test_gemm_tile_invariants(built_lib):
                         assert bn == 256
 
 
-@pytest.mark.parametrize("M,N,K,want", [
-    (2048, 768, 3072, (3, 96)),    # 310m FFN out-projection, 2048 tokens: 96 single-CTA tiles, 48 k-blocks
-    (2048, 768, 768, (3, 96)),     # 310m attention out-projection, 2048 tokens: 96 tiles, 12 k-blocks (4 per part)
-    (4096, 768, 3072, (1, 0)),     # 64 CTA-pair tiles of 76 slots: the best split (8 parts) saves only 1/8
-    (8192, 768, 3072, (1, 0)),     # 128 pair tiles: the last round (52) fills more than half of 76
-    (20480, 768, 3072, (6, 12)),   # 240 pair tiles: a last round of 12, split into 6 parts of 8 k-blocks
-    (32768, 768, 3072, (12, 4)),   # 384 pair tiles: a last round of 4, 12 parts of 4 k-blocks
-    (32768, 768, 768, (1, 0)),     # 1024 single-CTA tiles: a last round of 112 of 152
-    (100, 384, 1280, (5, 3)),      # 3 tiles, 20 k-blocks: 5 parts of 4
-    (820, 256, 512, (2, 14)),      # 14 tiles, 8 k-blocks: 2 parts of 4
-])
-def test_gemm_ksplit_choices(built_lib, M, N, K, want):
-    """The residual projection's split of K, worked out by hand from the rule
-    in the header (152 SMs; the tile choice of tee_plan_gemm)."""
-    st = ctypes.c_int(-1)
-    assert (built_lib.tee_plan_gemm_ksplit(M, N, K, 1, 152, ctypes.byref(st)), st.value) == want
-    for epi in (0, 2, 3):   # other epilogues never split
-        if epi == 3 and N % 256:
-            continue
-        assert (built_lib.tee_plan_gemm_ksplit(M, N, K, epi, 152, ctypes.byref(st)), st.value) == (1, 0)
-    assert built_lib.tee_plan_gemm_ksplit(M, N + 1, K, 1, 152, ctypes.byref(st)) == binding.TEE_EINVAL
-    assert built_lib.tee_plan_gemm_ksplit(M, N, K, 1, 152, None) == binding.TEE_EINVAL
-
-
 def test_gemm_plan_rejects_bad_shapes(built_lib):
     for args in ((0, 768, 768, 0), (64, 100, 768, 0), (64, 768, 100, 0), (64, 384, 768, 3), (64, 768, 768, 4)):
         rc, _, _ = _plan_gemm(built_lib, *args)

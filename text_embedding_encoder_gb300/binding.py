@@ -98,7 +98,6 @@ SIGNATURES = {
     "tee_unigram_destroy": (None, [_vp]),
     "tee_similarity": (_i, [_vp, _i, _i, _vp]),
     "tee_plan_gemm": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
-    "tee_plan_gemm_ksplit": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_i)]),
 }
 
 _LIB = None

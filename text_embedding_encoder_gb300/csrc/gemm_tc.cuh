@@ -6,8 +6,7 @@
 
 // Epilogues of C = A W^T (A bf16 [M, K], W bf16 [N, K], fp32 accumulation in TMEM).
 #define GEMM_EPI_STORE_BF16 0   // C bf16 [M, N]
-#define GEMM_EPI_ADD_F32    1   // C float [M, N] += acc (residual stream; with a split K each part adds its
-                                // share by TMA reduce-adds, in no fixed order)
+#define GEMM_EPI_ADD_F32    1   // C float [M, N] += acc (residual stream)
 #define GEMM_EPI_ROPE_BF16  2   // QKV: rotate-half RoPE on columns < 2*hidden, store bf16
 #define GEMM_EPI_GEGLU      3   // W rows interleaved per 256-row tile as [128 GELU inputs | 128 gates];
                                 // C bf16 [M, N/2] = GELU(a) * g
@@ -32,11 +31,6 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s);
 // [M, N] x K product with epilogue `epi` on a GPU of num_sms SMs (host only;
 // arguments as launch_gemm_tc accepts them).
 void gemm_tc_choose_tiles(int M, int N, int K, int epi, int num_sms, int* bn, int* pair);
-
-// Parts of K into which launch_gemm_tc splits the last *split_tiles tiles of a
-// residual-add product (1 and 0 = no split; only where tiles would leave SMs
-// idle), host only.
-int gemm_tc_choose_split(int M, int N, int K, int epi, int num_sms, int* split_tiles);
 
 // Row permutation of Wi used by GEMM_EPI_GEGLU: stored row r holds original row
 // geglu_source_row(r, I).

@@ -56,8 +56,6 @@ struct Params {
     const float* rope_sin;
     int hidden;
     unsigned int* status;
-    int n_full;       // ADD_F32: tiles [0, n_full) take all of K; each later tile is split into
-    int parts;        //   `parts` equal parts of K, each a unit that adds its share into C
 };
 
 // bf16-output epilogues stage each warp's 32 rows x 64 columns in a 4 KB
@@ -121,23 +119,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_m = (p.M + BM - 1) / BM, num_n = p.N / BN, num_k = p.K / BK;
-    // work units: one tile, or (clustered) a pair of vertically adjacent tiles
-    // per cluster.  ADD_F32 may split the tiles from n_full on into `parts`
-    // parts of K: unit u < n_full is tile u; later units are (tile, part),
-    // parts of a tile consecutive, each with num_k / parts k-blocks.
+    // work units: one tile, or (clustered) a pair of vertically adjacent tiles per cluster
     const uint32_t crank = CL ? cluster_ctarank() : 0;
-    const int num_tiles = (CL ? (num_m + 1) / 2 : num_m) * num_n;
-    const int parts = EPI == GEMM_EPI_ADD_F32 ? p.parts : 1;
-    const int n_full = EPI == GEMM_EPI_ADD_F32 ? p.n_full : num_tiles;
-    const int kc_part = num_k / parts;
-    const int num_units = n_full + (num_tiles - n_full) * parts;
+    const int num_units = (CL ? (num_m + 1) / 2 : num_m) * num_n;
     const int unit0 = CL ? blockIdx.x / 2 : blockIdx.x;
     const int ustride = CL ? gridDim.x / 2 : gridDim.x;
-    auto unit_tile = [&](int u) { return u < n_full ? u : n_full + (u - n_full) / parts; };
-    auto unit_n = [&](int u) { return unit_tile(u) % num_n; };
-    auto unit_m = [&](int u) { return CL ? 2 * (unit_tile(u) / num_n) + (int)crank : unit_tile(u) / num_n; };
-    auto unit_k0 = [&](int u) { return u < n_full ? 0 : ((u - n_full) % parts) * kc_part; };
-    auto unit_kc = [&](int u) { return u < n_full ? num_k : kc_part; };
+    auto unit_m = [&](int u) { return CL ? 2 * (u / num_n) + (int)crank : u / num_n; };
     // PAIR: the even CTA's barriers that both CTAs' copies and epilogues signal
     auto lead_bar = [&](int i) { return mapa_shared(bar(i), 0); };
 
@@ -183,13 +170,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr int PF = S::STAGES + 4;
             constexpr bool PREFETCH = !PAIR;
             for (int u = unit0; u < num_units && ok; u += ustride) {
-                const int n_t = unit_n(u), m_t = unit_m(u), kc = unit_kc(u), kb0 = unit_k0(u), kb1 = kb0 + kc;
-                if (PREFETCH && kc > S::STAGES)
-                    for (int j = S::STAGES; j < PF && j < kc; ++j) tma_prefetch_l2_2d(&tmA, (kb0 + j) * BK, m_t * BM);
-                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                const int n_t = u % num_n, m_t = unit_m(u);
+                if (PREFETCH && num_k > S::STAGES)
+                    for (int j = S::STAGES; j < PF && j < num_k; ++j) tma_prefetch_l2_2d(&tmA, j * BK, m_t * BM);
+                for (int kb = 0; kb < num_k; ++kb, ++g) {
                     const int s = g % S::STAGES;
                     const uint32_t r = g / S::STAGES;
-                    if (PREFETCH && kc > S::STAGES && kb + PF < kb1)
+                    if (PREFETCH && num_k > S::STAGES && kb + PF < num_k)
                         tma_prefetch_l2_2d(&tmA, (kb + PF) * BK, m_t * BM);
                     if (!mbar_wait(bar(EMPTY + s), (r & 1) ^ 1, abort_flag)) {
                         ok = false;
@@ -236,8 +223,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                const int kb0 = unit_k0(u), kb1 = kb0 + unit_kc(u);
-                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                for (int kb = 0; kb < num_k; ++kb, ++g) {
                     const int s = g % S::STAGES;
                     const uint32_t r = g / S::STAGES;
                     if (!(PAIR ? mbar_wait_cluster(bar(FULL + s), r & 1, abort_flag)
@@ -251,8 +237,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t bdesc = sw128_desc(sa + A_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        if constexpr (PAIR) mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, kb != kb0 || k != 0);
-                        else mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, kb != kb0 || k != 0);
+                        if constexpr (PAIR) mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                        else mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
                     }
                     if constexpr (PAIR) mma_commit_pair(bar(EMPTY + s), 0x3);   // both CTAs' stage s
                     else mma_commit(bar(EMPTY + s));
@@ -289,10 +275,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         auto issue_res_load = [&](int g) {                         // lane 0; box g % RB is free
             const int k = g / NC, c = g % NC;
             const int u = unit0 + k * ustride;
-            if (u >= num_units || u >= n_full) return;   // a split unit adds, loading no residual
+            if (u >= num_units) return;
             const int b = g % RB;
             mbar_expect_tx(res_bar(b), 4096);
-            tma_load_2d(smem_u32(rslice + b * 4096), &tmC, unit_n(u) * BN + c * 32, unit_m(u) * BM + quad * 32,
+            tma_load_2d(smem_u32(rslice + b * 4096), &tmC, (u % num_n) * BN + c * 32, unit_m(u) * BM + quad * 32,
                         res_bar(b));
             last_issued[b] = g;
         };
@@ -313,7 +299,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int it = 0;
         for (int u = unit0; u < num_units; u += ustride, ++it) {
             const int acc = it & 1, use = it >> 1;
-            const int n_t = unit_n(u), m_t = unit_m(u);
+            const int n_t = u % num_n, m_t = unit_m(u);
             const int gr = m_t * BM + row_local;
             const bool valid = gr < p.M;
             const int y_box = m_t * BM + quad * 32;
@@ -329,85 +315,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     store64(v, n_t * BN + col, y_box);
                 }
             } else if constexpr (EPI == GEMM_EPI_ADD_F32) {
-                if (u >= n_full) {
-                    // a part of a split K: its share of A W^T is added into the
-                    // residual in L2 by TMA reduce-adds, 32 columns at a time
-                    // through the same ring of staging boxes (no residual load)
-                    if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
-                    tc_fence_after();
-                    float v[2][32];
-                    tmem_ld32_issue(taddr, v[0]);
+                // this warp's 32 x BN slice of the residual, one 32-column box
+                // per chunk: the box was TMA-loaded ahead of time, is updated in
+                // place, TMA-stored, and then refilled with the chunk RB ahead
+                if (it == 0 && lane == 0)
+                    for (int g = 0; g < RB; ++g) issue_res_load(g);
+                if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
+                tc_fence_after();
+                bool ok = true;
+                // chunk c + 1's accumulator columns are loaded from TMEM while
+                // chunk c is added and stored (two register sets, loop unrolled)
+                float v[2][32];
+                tmem_ld32_issue(taddr, v[0]);
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        const int g = it * NC + c;
-                        const int b = g % RB;
+                for (int c = 0; c < NC; ++c) {
+                    const int g = it * NC + c;
+                    const int b = g % RB;
+                    if (!mbar_wait(res_bar(b), (g / RB) & 1, abort_flag)) {
                         tmem_wait_ld();
-                        tmem_tie32(v[c & 1]);
-                        if (c + 1 < NC) tmem_ld32_issue(taddr + (c + 1) * 32, v[(c + 1) & 1]);
-                        // box b last held chunk g - RB: its reduce has read it
-                        if (lane == 0 && g >= RB) bulk_wait_read<RB - 1>();
-                        __syncwarp();
-                        uint8_t* rp = rslice + b * 4096 + lane * 128;
+                        ok = false;
+                        break;
+                    }
+                    res_done = g + 1;
+                    tmem_wait_ld();
+                    tmem_tie32(v[c & 1]);
+                    if (c + 1 < NC) tmem_ld32_issue(taddr + (c + 1) * 32, v[(c + 1) & 1]);
+                    uint8_t* rp = rslice + b * 4096 + lane * 128;
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            *reinterpret_cast<float4*>(rp + ((k ^ (lane & 7)) << 4)) =
-                                make_float4(v[c & 1][4 * k + 0], v[c & 1][4 * k + 1], v[c & 1][4 * k + 2],
-                                            v[c & 1][4 * k + 3]);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_reduce_add_2d(&tmC, smem_u32(rslice + b * 4096), n_t * BN + c * 32, y_box);
-                            bulk_commit();
+                    for (int k = 0; k < 8; ++k) {
+                        float4* q = reinterpret_cast<float4*>(rp + ((k ^ (lane & 7)) << 4));
+                        float4 o = *q;
+                        f2_unpack(f2_add(f2_pack(o.x, o.y), f2_pack(v[c & 1][4 * k + 0], v[c & 1][4 * k + 1])), o.x, o.y);
+                        f2_unpack(f2_add(f2_pack(o.z, o.w), f2_pack(v[c & 1][4 * k + 2], v[c & 1][4 * k + 3])), o.z, o.w);
+                        *q = o;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, smem_u32(rslice + b * 4096), n_t * BN + c * 32, y_box);
+                        bulk_commit();
+                        if (g >= 1) {
+                            bulk_wait_read<1>();           // the store of chunk g - 1 has read its box
+                            issue_res_load(g - 1 + RB);
                         }
                     }
-                } else {
-                    // this warp's 32 x BN slice of the residual, one 32-column box
-                    // per chunk: the box was TMA-loaded ahead of time, is updated in
-                    // place, TMA-stored, and then refilled with the chunk RB ahead
-                    if (it == 0 && lane == 0)
-                        for (int g = 0; g < RB; ++g) issue_res_load(g);
-                    if (!mbar_wait(bar(TFULL + acc), use & 1, abort_flag)) break;
-                    tc_fence_after();
-                    bool ok = true;
-                    // chunk c + 1's accumulator columns are loaded from TMEM while
-                    // chunk c is added and stored (two register sets, loop unrolled)
-                    float v[2][32];
-                    tmem_ld32_issue(taddr, v[0]);
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        const int g = it * NC + c;
-                        const int b = g % RB;
-                        if (!mbar_wait(res_bar(b), (g / RB) & 1, abort_flag)) {
-                            tmem_wait_ld();
-                            ok = false;
-                            break;
-                        }
-                        res_done = g + 1;
-                        tmem_wait_ld();
-                        tmem_tie32(v[c & 1]);
-                        if (c + 1 < NC) tmem_ld32_issue(taddr + (c + 1) * 32, v[(c + 1) & 1]);
-                        uint8_t* rp = rslice + b * 4096 + lane * 128;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            float4* q = reinterpret_cast<float4*>(rp + ((k ^ (lane & 7)) << 4));
-                            float4 o = *q;
-                            f2_unpack(f2_add(f2_pack(o.x, o.y), f2_pack(v[c & 1][4 * k + 0], v[c & 1][4 * k + 1])), o.x, o.y);
-                            f2_unpack(f2_add(f2_pack(o.z, o.w), f2_pack(v[c & 1][4 * k + 2], v[c & 1][4 * k + 3])), o.z, o.w);
-                            *q = o;
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmC, smem_u32(rslice + b * 4096), n_t * BN + c * 32, y_box);
-                            bulk_commit();
-                            if (g >= 1) {
-                                bulk_wait_read<1>();           // the store of chunk g - 1 has read its box
-                                issue_res_load(g - 1 + RB);
-                            }
-                        }
-                    }
-                    if (!ok) break;
                 }
+                if (!ok) break;
             } else if constexpr (EPI == GEMM_EPI_ROPE_BF16) {
                 // q and k tiles (columns < 2*hidden; 2*hidden is a multiple of
                 // the tile width) rotate every head with the row's cos/sin,
@@ -619,44 +572,6 @@ void gemm_tc_choose_tiles(int M, int N, int K, int epi, int num_sms, int* bn, in
     *pair = mode == MODE_PAIR;
 }
 
-int gemm_tc_choose_split(int M, int N, int K, int epi, int num_sms, int* split_tiles) {
-    // Residual add: tiles that would leave most slots (SMs, or SM pairs) idle
-    // in the last round of units are split into equal parts of K (at least 4
-    // k-blocks each), each part a unit that adds its share into the residual.
-    // Fewer tiles than slots: every tile is split, into the part count (2..8)
-    // that minimises rounds of units per unit of K -- ceil(tiles * parts /
-    // slots) / parts -- fewest parts on a tie, if that cost is at most 0.8
-    // (the reduce-adds cost more per tile than the fused residual update).
-    // Otherwise, a last round that fills at most half the slots: its tiles are
-    // split into the most parts (2..16) that still fit in one round.
-    *split_tiles = 0;
-    if (epi != GEMM_EPI_ADD_F32 || M <= 0) return 1;
-    int bn = 128, pair = 0;
-    gemm_tc_choose_tiles(M, N, K, epi, num_sms, &bn, &pair);
-    const int num_m = (M + BM - 1) / BM, num_k = K / BK;
-    const long tiles = (long)(pair ? (num_m + 1) / 2 : num_m) * (N / bn);
-    const long slots = pair ? num_sms / 2 : num_sms;
-    int best_parts = 1;
-    if (tiles < slots) {
-        double best = 1.0;
-        for (int parts = 2; parts <= 8; ++parts) {
-            if (num_k % parts || num_k / parts < 4) continue;
-            const double c = (double)((tiles * parts + slots - 1) / slots) / parts;
-            if (c < best - 1e-9 && c <= 0.8) best = c, best_parts = parts;
-        }
-        if (best_parts > 1) *split_tiles = (int)tiles;
-        return best_parts;
-    }
-    const long tail = tiles % slots;
-    if (tail == 0 || 2 * tail > slots) return 1;
-    for (int parts = 16; parts >= 2; --parts) {
-        if (num_k % parts || num_k / parts < 4 || tail * parts > slots) continue;
-        *split_tiles = (int)tail;
-        return parts;
-    }
-    return 1;
-}
-
 cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
     std::call_once(g_once, init_once);
     if (g_init_err != cudaSuccess) return g_init_err;
@@ -682,11 +597,8 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, cudaStream_t s) {
                              CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64)) {
         return cudaErrorInvalidValue;
     }
-    int split_tiles = 0;
-    const int parts = gemm_tc_choose_split(a.M, a.N, a.K, a.epi, num_sms, &split_tiles);
-    const int tiles = (mode != MODE_SINGLE ? (num_m + 1) / 2 : num_m) * (a.N / BN);
-    Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status, tiles - split_tiles, parts};
-    const int units = tiles - split_tiles + split_tiles * parts;
+    Params p{a.C, a.M, a.N, a.K, a.pos, a.rope_cos, a.rope_sin, a.hidden, a.status};
+    const int units = (mode != MODE_SINGLE ? (num_m + 1) / 2 : num_m) * (a.N / BN);
 #define TEE_GEMM_DISPATCH(BN_, EPI_)                                                                  \
     return mode == MODE_PAIR ? launch_t<BN_, EPI_, MODE_PAIR>(ma, mb, mc_map, p, units, dev, num_sms, s)  \
                              : launch_t<BN_, EPI_, MODE_SINGLE>(ma, mb, mc_map, p, units, dev, num_sms, s)

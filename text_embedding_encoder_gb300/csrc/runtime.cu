@@ -811,14 +811,6 @@ int tee_plan_gemm(int M, int N, int K, int epi, int num_sms, int* bn, int* pair)
     return TEE_OK;
 }
 
-int tee_plan_gemm_ksplit(int M, int N, int K, int epi, int num_sms, int* split_tiles) {
-    if (!split_tiles) return tee_set_global_error(TEE_EINVAL, "plan_gemm_ksplit: NULL output");
-    if (M < 1 || N < 128 || N % 128 || K < 64 || K % 64 || epi < GEMM_EPI_STORE_BF16 || epi > GEMM_EPI_GEGLU ||
-        (epi == GEMM_EPI_GEGLU && N % 256) || num_sms < 2)
-        return tee_set_global_error(TEE_EINVAL, "plan_gemm_ksplit: shape, epilogue or SM count out of range");
-    return gemm_tc_choose_split(M, N, K, epi, num_sms, split_tiles);
-}
-
 int tee_profile_enable(tee_ctx* ctx, int on) {
     if (!ctx) return TEE_EINVAL;
     ctx->profiling = on != 0;
