@@ -529,7 +529,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             dst_p = r < q_len ? p.o + (size_t)qg * p.hidden + head * HD + half * 32 : nullptr;
             pend = true;
         }
-        if (ok && pend) finalize(false);
+        if (ok && pend) ok = finalize(false);
+        // A warp that gave up on a bounded wait leaves with one arrival on its
+        // pair barrier, so a partner already waiting there is released (and
+        // next sees the abort flag at its next, bounded, wait: every path
+        // between two pair barriers passes one).  Unawaited, it is harmless.
+        if (!ok) asm volatile("bar.arrive %0, 64;" ::"r"(pair_bar) : "memory");
     }
 
     tc_fence_before();
