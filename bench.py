@@ -72,7 +72,7 @@ def peaks():
 # kernel sources with this digest; otherwise reported as null.
 GEMM_TRAFFIC_BYTES = 233.97e6
 GEMM_TRAFFIC_SOURCES = ['text_embedding_encoder_gb300/csrc/k_gemm_tc.cu', 'text_embedding_encoder_gb300/csrc/tc_ptx.cuh', 'text_embedding_encoder_gb300/csrc/gemm_tc.cuh']
-GEMM_TRAFFIC_DIGEST = "96fe365d314a9385"
+GEMM_TRAFFIC_DIGEST = "79dbd9b2c7257d5b"
 
 
 def gemm_traffic():
