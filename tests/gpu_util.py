@@ -10,7 +10,7 @@ For single steps on bf16 activations the GPU rounds its output to bf16
 import numpy as np
 import torch
 
-from text_embedding_encoder_gb300 import binding, synth
+from text_embedding_encoder_gb300 import binding
 import oracle
 
 FP32_ABS = 1e-4
