@@ -72,7 +72,7 @@ constexpr uint32_t OFF_BAR = OFF_V + KV_STAGES * TILE_BYTES;
 // barrier indices
 constexpr int SP_BUFS = 3;   // TMEM S/P buffers: tile t uses buffer t % 3
 constexpr int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = B_KVF + KV_STAGES, B_SF = B_KVE + KV_STAGES,
-              B_PF = B_SF + SP_BUFS, B_OF = B_PF + SP_BUFS, B_OE = B_OF + 2, B_DONE = B_OE + 2, N_BARS = B_DONE + 1;
+              B_PF = B_SF + SP_BUFS, B_OE = B_PF + SP_BUFS, B_DONE = B_OE + 2, N_BARS = B_DONE + 1;
 constexpr uint32_t OFF_RED = OFF_BAR + N_BARS * 8 + 16;       // row-maximum exchange: [2 tiles][2 halves][128 rows]
 constexpr uint32_t OFF_REDL = OFF_RED + 2 * 2 * 128 * 4;       // row-sum exchange: [2 units][2 halves][128 rows]
 constexpr uint32_t SMEM_TOTAL = OFF_REDL + 2 * 2 * 128 * 4 + 1024;
@@ -164,7 +164,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_QF + b), 1);
             mbar_init(bar(B_QE + b), 1);
-            mbar_init(bar(B_OF + b), 1);
             mbar_init(bar(B_OE + b), SM_THREADS);
         }
         for (int b = 0; b < SP_BUFS; ++b) {
@@ -240,7 +239,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // tile of a unit overwrites it once the softmax warps have read the
             // unit two back out of that buffer
             auto issue_pv = [&](uint32_t tt, bool first, int ub, uint32_t uuse) -> bool {
-                const int pb = tt & 1, sb = tt % SP_BUFS, st = tt % KV_STAGES;
+                const int sb = tt % SP_BUFS, st = tt % KV_STAGES;
                 if (!mbar_wait(bar(B_PF + sb), (tt / SP_BUFS) & 1, abort_flag)) return false;
                 if (first && !mbar_wait(bar(B_OE + ub), (uuse & 1) ^ 1, abort_flag)) return false;
                 tc_fence_after();
@@ -251,7 +250,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t vdesc = sw128_desc_mn(vbase + s * 2048);
                     mma_bf16_ts(tmem_base + TM_O + ub * HD, pbase + 8 * s, vdesc, idesc_pv, !(first && s == 0));
                 }
-                mma_commit(bar(B_OF + pb));
+                // one commit frees the K/V stage and tells the softmax warps
+                // that P_tt V_tt is in O
                 mma_commit(bar(B_KVE + st));
                 return true;
             };
@@ -332,6 +332,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
 
         auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+        // P_tt V_tt is in O once tile tt's K/V stage is released (the commit
+        // after that P V).  The wait's parity cannot alias: it is asked for
+        // after the S of tile tt was seen ready, and that S was issued after
+        // the P V of tile tt - 3, so the stage's previous phase (tile tt - 5)
+        // is complete; its next phase needs the P of tile tt + 5, which these
+        // warps have not yet written.
+        auto pv_done = [&](uint32_t tt) -> bool {
+            return mbar_wait(bar(B_KVE + tt % KV_STAGES), (tt / KV_STAGES) & 1, abort_flag);
+        };
 
         // The previous unit's output, deferred past the next unit's first
         // softmax: wait for its last P V, read this warp's 32 columns of O,
@@ -345,7 +354,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int ub_p = 0;
         bf16* dst_p = nullptr;
         auto finalize = [&](bool exchanged) -> bool {
-            if (!mbar_wait(bar(B_OF + (t_p & 1)), (t_p >> 1) & 1, abort_flag)) return false;
+            if (!pv_done(t_p)) return false;
             tc_fence_after();
             float o[32];
             tmem_ld32(tmem_base + lane_off + TM_O + ub_p * HD + half * 32, o);
@@ -475,7 +484,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (__any_sync(0xffffffffu, need)) {
                         const float corr = need ? ex2_approx(m_ref - mx) : 1.0f;
                         // P V of the previous tile must be in O before it is rescaled
-                        if (!mbar_wait(bar(B_OF + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag)) {
+                        if (!pv_done(t - 1)) {
                             ok = false;
                             break;
                         }
