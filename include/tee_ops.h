@@ -198,6 +198,20 @@ int tee_selftest_gelu(const float* d_a, float* d_y, long long n, void* stream);
  * of items (TEE_ETOOLONG if it exceeds max_items). */
 int tee_plan_attention(const int32_t* h_cu, int n_texts, int window, int is_global, int32_t* items, int max_items);
 
+/* How the attention kernel's `grid` persistent CTAs share the units (item,
+ * head) of a list of n_items work items (as tee_plan_attention gives them) and
+ * n_heads heads.  Units are taken in order of decreasing work -- work = 2 x
+ * ceil((k_hi - k_lo) / 128) + 1 -- ties in unit order (item by item, heads in
+ * order), and each goes to the CTA with the least work so far, ties to the
+ * lower CTA index.  slots: host int32[4 * n_items * n_heads], each CTA's units
+ * in the order it takes them, CTA 0 first, each as {q_start, q_len | head <<
+ * 16, k_lo, k_hi}; slot_off: host int32[grid + 1], CTA c holding slots
+ * slot_off[c] .. slot_off[c + 1].  Requires 1 <= n_heads <= 32767, 1 <= grid
+ * <= 1024 and items with 0 <= q_len <= 65535 and k_lo <= k_hi.  Returns
+ * n_items * n_heads, TEE_EINVAL, or TEE_ETOOLONG past 2^29 units. */
+int tee_plan_attention_schedule(const int32_t* items, int n_items, int n_heads, int grid, int32_t* slots,
+                                int32_t* slot_off);
+
 /* Tile shape of the bf16 tensor-core projection C[M, N] = A[M, K] W^T: *bn =
  * tile width in columns (128, 192 or 256), *pair = 1 when 2-CTA clusters
  * compute 256-row tiles, 0 for one CTA per 128-row tile, as the library

@@ -92,6 +92,7 @@ SIGNATURES = {
     "tee_selftest_wait_timeout": (_i, [_ctx, ctypes.c_longlong, _vp]),
     "tee_selftest_gelu": (_i, [_vp, _vp, ctypes.c_longlong, _vp]),
     "tee_plan_attention": (_i, [_vp, _i, _i, _i, _vp, _i]),
+    "tee_plan_attention_schedule": (_i, [_vp, _i, _i, _i, _vp, _vp]),
     "tee_unigram_create": (_i, [ctypes.POINTER(ctypes.c_char_p), _vp, _i, _i, ctypes.c_float, _i, _i,
                                 ctypes.POINTER(_vp)]),
     "tee_unigram_encode": (_i, [_vp, ctypes.c_char_p, _i, _vp, _i]),

@@ -80,10 +80,9 @@ constexpr uint32_t TMEM_COLS = 512;                 // S/P: 3 x 128 columns (by 
 constexpr uint32_t TM_S = 0, TM_O = SP_BUFS * BKV;
 
 struct AttnParams {
-    const int4* items;      // {q_start, q_len, k_lo, k_hi} per query tile
+    const int4* slots;      // {q_start, q_len | head << 16, k_lo, k_hi} per unit, CTA after CTA
+    const int* slot_off;    // CTA c takes slots slot_off[c] .. slot_off[c + 1]
     const int2* row_tb;     // per token: {start, end} of its text
-    int n_units;            // items x heads
-    int n_heads;
     int hidden;
     int window;
     float scale_log2;       // log2(e) / sqrt(64)
@@ -196,11 +195,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t g = 0;   // KV tiles issued
             int ui = 0;
             bool ok = true;
-            int4 it_next = p.items[blockIdx.x / p.n_heads];   // work items are read a unit ahead
-            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
+            const int i0 = p.slot_off[blockIdx.x], i1 = p.slot_off[blockIdx.x + 1];
+            int4 it_next = i0 < i1 ? p.slots[i0] : make_int4(0, 0, 0, 0);   // units are read one ahead
+            for (int i = i0; i < i1 && ok; ++i, ++ui) {
                 const int4 it = it_next;
-                if (u + gridDim.x < p.n_units) it_next = p.items[(u + gridDim.x) / p.n_heads];
-                const int head = u % p.n_heads;
+                if (i + 1 < i1) it_next = p.slots[i + 1];
+                const int head = it.y >> 16;
                 const int nk = n_kv_tiles(it);
                 const int qb = ui & 1;
                 if (!mbar_wait(bar(B_QE + qb), ((ui >> 1) & 1) ^ 1, abort_flag)) break;
@@ -265,10 +265,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t t = 0;          // tiles whose S has been issued (global)
             bool ok = true;
             int ui = 0;
-            int4 it_next = p.items[blockIdx.x / p.n_heads];
-            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
+            const int i0 = p.slot_off[blockIdx.x], i1 = p.slot_off[blockIdx.x + 1];
+            int4 it_next = i0 < i1 ? p.slots[i0] : make_int4(0, 0, 0, 0);
+            for (int i = i0; i < i1 && ok; ++i, ++ui) {
                 const int nk = n_kv_tiles(it_next);
-                if (u + gridDim.x < p.n_units) it_next = p.items[(u + gridDim.x) / p.n_heads];
+                if (i + 1 < i1) it_next = p.slots[i + 1];
                 const int qb = ui & 1;
                 if (!mbar_wait(bar(B_QF + qb), (ui >> 1) & 1, abort_flag)) break;
                 const uint64_t qdesc = sw128_desc(sbase + OFF_Q + qb * TILE_BYTES);
@@ -378,21 +379,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Work items are read two units ahead and the row's text bounds one
         // unit ahead, so neither load's latency lands on a unit's first tile.
         auto row_bounds = [&](const int4& x) -> int2 {
-            return r < x.y ? p.row_tb[x.x + r] : make_int2(0, 0);
+            return r < (x.y & 0xffff) ? p.row_tb[x.x + r] : make_int2(0, 0);
         };
         int ui = 0;
-        int4 it_next = p.items[blockIdx.x / p.n_heads];
-        int4 it_next2 = blockIdx.x + gridDim.x < p.n_units ? p.items[(blockIdx.x + gridDim.x) / p.n_heads]
-                                                           : make_int4(0, 0, 0, 0);
+        const int i0 = p.slot_off[blockIdx.x], i1 = p.slot_off[blockIdx.x + 1];
+        int4 it_next = i0 < i1 ? p.slots[i0] : make_int4(0, 0, 0, 0);
+        int4 it_next2 = i0 + 1 < i1 ? p.slots[i0 + 1] : make_int4(0, 0, 0, 0);
         int2 tb_next = row_bounds(it_next);
-        for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++ui) {
+        for (int i = i0; i < i1 && ok; ++i, ++ui) {
             const int4 it = it_next;
             const int2 tb = tb_next;
             it_next = it_next2;
-            if (u + gridDim.x < p.n_units) tb_next = row_bounds(it_next);
-            if (u + 2 * gridDim.x < p.n_units) it_next2 = p.items[(u + 2 * gridDim.x) / p.n_heads];
-            const int head = u % p.n_heads;
-            const int q_start = it.x, q_len = it.y, k_lo = it.z, k_hi = it.w;
+            if (i + 1 < i1) tb_next = row_bounds(it_next);
+            if (i + 2 < i1) it_next2 = p.slots[i + 2];
+            const int head = it.y >> 16;
+            const int q_start = it.x, q_len = it.y & 0xffff, k_lo = it.z, k_hi = it.w;
             const int nk = n_kv_tiles(it);
             const int qg = q_start + r;
             const int ub = ui & 1;
@@ -574,15 +575,15 @@ void init_once() {
 
 }  // namespace
 
-cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, const int4* d_items, int n_items,
-                                bool is_global, int window, const int2* row_tb, void* o, unsigned int* status,
-                                cudaStream_t s) {
+cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, const int4* d_slots,
+                                const int32_t* d_slot_off, int grid, bool is_global, int window, const int2* row_tb,
+                                void* o, unsigned int* status, cudaStream_t s) {
     std::call_once(g_once, init_once);
     if (g_init_err != cudaSuccess) return g_init_err;
-    if (n_items == 0 || T == 0) return cudaSuccess;
+    if (grid == 0 || T == 0) return cudaSuccess;
     if (H != n_heads * HD || (reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(o) & 15))
         return cudaErrorInvalidValue;
-    if (!row_tb) return cudaErrorInvalidValue;
+    if (!row_tb || !d_slots || !d_slot_off || grid < 0) return cudaErrorInvalidValue;
     CUtensorMap tm;
     cuuint64_t dims[2] = {(cuuint64_t)3 * H, (cuuint64_t)T};
     cuuint64_t strides[1] = {(cuuint64_t)3 * H * 2};
@@ -607,10 +608,7 @@ cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, cons
             g_attr_set[dev] = true;
         }
     }
-    const int n_units = n_items * n_heads;
-    AttnParams p{d_items, row_tb, n_units, n_heads, H, window, 1.4426950408889634f / 8.0f,
-                 (bf16*)o, status};
-    const int grid = n_units < num_sms ? n_units : num_sms;
+    AttnParams p{d_slots, d_slot_off, row_tb, H, window, 1.4426950408889634f / 8.0f, (bf16*)o, status};
     cudaError_t e = is_global ? launch_pdl(attn_tc_kernel<false>, dim3(grid), dim3(NUM_THREADS), SMEM_TOTAL, s, tm, p)
                               : launch_pdl(attn_tc_kernel<true>, dim3(grid), dim3(NUM_THREADS), SMEM_TOTAL, s, tm, p);
     if (e != cudaSuccess) return e;

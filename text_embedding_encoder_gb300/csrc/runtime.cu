@@ -124,7 +124,10 @@ size_t carve_workspace(tee_ctx* c, void* base) {
     }
     c->d_status = cv.take<unsigned int>(4);
     c->max_items = (int)(T / 128 + g.max_texts + 1);   // bounds both lists
-    for (int b = 0; b < 2; ++b) c->d_items[b] = cv.take<int4>(c->max_items);
+    for (int b = 0; b < 2; ++b) {
+        c->d_slots[b] = cv.take<int4>((size_t)c->max_items * g.n_heads);
+        c->d_slot_off[b] = cv.take<int32_t>(TEE_ATTN_MAX_GRID + 1);
+    }
     c->max_chunks = (int)(T / POOL_CHUNK_FUSED + g.max_texts + 1);
     c->d_chunk_off = cv.take<int32_t>(g.max_texts + 1);
     c->pool_partial = cv.take<float>((size_t)c->max_chunks * H);
@@ -253,12 +256,85 @@ void plan_attention_items(const int32_t* h_cu, int n_texts, int w, std::vector<i
     }
 }
 
-int prepare_attention_items(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cudaStream_t s) {
+// The attention kernel's persistent CTAs over (item, head) units.  Units are
+// taken in order of decreasing work (stable: item order, then head) and each
+// goes to the CTA with the least work so far, ties to the lower index (longest
+// processing time first); a unit's work is counted as 2 x its 128-key tiles +
+// 1 (a tile, and the per-unit output pass at about half a tile).  slots gets
+// each CTA's units in the order it takes them, CTA after CTA, as the item with
+// y = q_len | head << 16; off[c] .. off[c + 1] are CTA c's slots.
+//
+// The least-loaded CTA comes from a bucket queue: loads are integers, the least
+// load never falls, and no load is more than the largest unit's work above it,
+// so a ring of (largest work + 1) buckets, each a bitset of the CTAs with that
+// load, finds it in amortised constant time (lowest set bit = lowest index).
+void schedule_attention_units(const std::vector<int4>& items, int n_heads, int grid, std::vector<int4>& slots,
+                              std::vector<int32_t>& off) {
+    const int n_items = (int)items.size();
+    std::vector<int> wk(n_items), order(n_items);
+    int w_max = 1;
+    for (int i = 0; i < n_items; ++i) {
+        wk[i] = 2 * ((items[i].w - items[i].z + 127) / 128) + 1;
+        w_max = std::max(w_max, wk[i]);
+        order[i] = i;
+    }
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return wk[a] > wk[b]; });
+    const int words = (grid + 63) / 64, ring = w_max + 1;
+    std::vector<uint64_t> bits((size_t)ring * words, 0);
+    for (int c = 0; c < grid; ++c) bits[c >> 6] |= 1ull << (c & 63);
+    std::vector<int> cta((size_t)n_items * n_heads);
+    off.assign(grid + 1, 0);
+    int lb = 0;   // bucket of the least load (that load modulo ring)
+    size_t k = 0;
+    for (int i : order) {
+        for (int h = 0; h < n_heads; ++h, ++k) {
+            int c = -1;
+            while (c < 0) {
+                uint64_t* b = &bits[(size_t)lb * words];
+                for (int q = 0; q < words && c < 0; ++q)
+                    if (b[q]) {
+                        const int bit = __builtin_ctzll(b[q]);
+                        b[q] &= b[q] - 1;
+                        c = q * 64 + bit;
+                    }
+                if (c < 0 && ++lb == ring) lb = 0;
+            }
+            cta[k] = c;
+            ++off[c + 1];
+            int nb = lb + wk[i];   // wk[i] < ring
+            if (nb >= ring) nb -= ring;
+            bits[(size_t)nb * words + (c >> 6)] |= 1ull << (c & 63);
+        }
+    }
+    for (int c = 0; c < grid; ++c) off[c + 1] += off[c];
+    std::vector<int32_t> fill(off.begin(), off.end() - 1);
+    slots.resize((size_t)n_items * n_heads);
+    k = 0;
+    for (int i : order)
+        for (int h = 0; h < n_heads; ++h, ++k) {
+            int4 it = items[i];
+            it.y |= h << 16;
+            slots[fill[cta[k]]++] = it;
+        }
+}
+
+// Plans both lists and uploads the schedule of list `only` (0 global, 1
+// window layers), or of both when only < 0.
+int prepare_attention_items(tee_ctx* ctx, const int32_t* h_cu, int n_texts, cudaStream_t s, int only = -1) {
     plan_attention_items(h_cu, n_texts, ctx->cfg.window, ctx->h_items);
+    int dev = 0, num_sms = 0;
+    CK(tee_current_device(&dev, &num_sms));
     for (int b = 0; b < 2; ++b) {
+        if (only >= 0 && b != only) continue;
         if ((int)ctx->h_items[b].size() > ctx->max_items)
             return fail(ctx, TEE_ETOOLONG, "too many attention work items");
-        CK(cudaMemcpyAsync(ctx->d_items[b], ctx->h_items[b].data(), ctx->h_items[b].size() * sizeof(int4),
+        const int n_units = (int)ctx->h_items[b].size() * ctx->cfg.n_heads;
+        ctx->attn_grid[b] = std::min(std::min(n_units, num_sms), TEE_ATTN_MAX_GRID);
+        schedule_attention_units(ctx->h_items[b], ctx->cfg.n_heads, ctx->attn_grid[b], ctx->h_slots[b],
+                                 ctx->h_slot_off[b]);
+        CK(cudaMemcpyAsync(ctx->d_slots[b], ctx->h_slots[b].data(), ctx->h_slots[b].size() * sizeof(int4),
+                           cudaMemcpyHostToDevice, s));
+        CK(cudaMemcpyAsync(ctx->d_slot_off[b], ctx->h_slot_off[b].data(), ctx->h_slot_off[b].size() * sizeof(int32_t),
                            cudaMemcpyHostToDevice, s));
     }
     return TEE_OK;
@@ -393,8 +469,8 @@ int step_attention(tee_ctx* ctx, int layer, const void* qkv, const int32_t* d_cu
     if (g.dtype == TEE_BF16) {
         const int b = is_g ? 0 : 1;
         LAUNCH(TEE_K_ATTENTION, flops, bytes,
-               launch_attention_tc(qkv, T, g.hidden, g.n_heads, ctx->d_items[b], (int)ctx->h_items[b].size(), is_g,
-                                   g.window, ctx->d_rowtb, o, ctx->d_status, s));
+               launch_attention_tc(qkv, T, g.hidden, g.n_heads, ctx->d_slots[b], ctx->d_slot_off[b], ctx->attn_grid[b],
+                                   is_g, g.window, ctx->d_rowtb, o, ctx->d_status, s));
         return TEE_OK;
     }
     LAUNCH(TEE_K_ATTENTION, flops, bytes,
@@ -454,7 +530,6 @@ int run_layers(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const in
                cudaStream_t s) {
     const tee_config& g = ctx->cfg;
     int rc;
-    if (g.dtype == TEE_BF16 && (rc = prepare_attention_items(ctx, h_cu, n_texts, s))) return rc;
     LAUNCH(TEE_K_EMBED, 0, (double)T * 4 * 4,
            launch_positions(d_cu, n_texts, T, ctx->d_pos, ctx->d_rowtb, s));
     LAUNCH(TEE_K_EMBED, 0, (double)T * g.hidden * (4.0 + (act_is_bf16(ctx) ? 2 : 4)) + T * 4.0,
@@ -463,6 +538,9 @@ int run_layers(tee_ctx* ctx, const int32_t* d_ids, const int32_t* d_cu, const in
     for (int l = 0; l < g.n_layers; ++l) {
         if ((rc = step_layernorm(ctx, l, TEE_LN_ATTN, ctx->x, ctx->y, T, s))) return rc;
         if ((rc = step_qkv(ctx, l, ctx->y, ctx->d_pos, ctx->qkv, T, s))) return rc;
+        // the attention work items and their schedule are planned on the host
+        // while the kernels queued so far run
+        if (l == 0 && g.dtype == TEE_BF16 && (rc = prepare_attention_items(ctx, h_cu, n_texts, s))) return rc;
         if ((rc = step_attention(ctx, l, ctx->qkv, d_cu, h_cu, n_texts, T, ctx->o, s))) return rc;
         if ((rc = step_linear(ctx, l, TEE_W_OUT, ctx->o, ctx->x, T, 1, GEMM_EPI_ADD_F32, nullptr, s))) return rc;
         if ((rc = step_layernorm(ctx, l, TEE_LN_MLP, ctx->x, ctx->y, T, s))) return rc;
@@ -802,6 +880,32 @@ int tee_plan_attention(const int32_t* h_cu, int n_texts, int window, int is_glob
     return (int)v.size();
 }
 
+int tee_plan_attention_schedule(const int32_t* items, int n_items, int n_heads, int grid, int32_t* slots,
+                                int32_t* slot_off) {
+    if (n_items < 0 || (n_items > 0 && !items)) return tee_set_global_error(TEE_EINVAL, "plan_schedule: bad items");
+    if (n_heads < 1 || n_heads > 32767) return tee_set_global_error(TEE_EINVAL, "plan_schedule: n_heads out of range");
+    if (grid < 1 || grid > TEE_ATTN_MAX_GRID) return tee_set_global_error(TEE_EINVAL, "plan_schedule: grid out of range");
+    if (!slots || !slot_off) return tee_set_global_error(TEE_EINVAL, "plan_schedule: output is NULL");
+    if ((long long)n_items * n_heads > INT32_MAX / 4) return tee_set_global_error(TEE_ETOOLONG, "plan_schedule: too many units");
+    std::vector<int4> v(n_items);
+    for (int i = 0; i < n_items; ++i) {
+        v[i] = make_int4(items[4 * i], items[4 * i + 1], items[4 * i + 2], items[4 * i + 3]);
+        if (v[i].y < 0 || v[i].y > 0xffff || v[i].w < v[i].z)
+            return tee_set_global_error(TEE_EINVAL, "plan_schedule: bad item");
+    }
+    std::vector<int4> sl;
+    std::vector<int32_t> off;
+    schedule_attention_units(v, n_heads, grid, sl, off);
+    for (size_t i = 0; i < sl.size(); ++i) {
+        slots[4 * i + 0] = sl[i].x;
+        slots[4 * i + 1] = sl[i].y;
+        slots[4 * i + 2] = sl[i].z;
+        slots[4 * i + 3] = sl[i].w;
+    }
+    for (int c = 0; c <= grid; ++c) slot_off[c] = off[c];
+    return (int)sl.size();
+}
+
 int tee_plan_gemm(int M, int N, int K, int epi, int num_sms, int* bn, int* pair) {
     if (!bn || !pair) return tee_set_global_error(TEE_EINVAL, "plan_gemm: NULL output");
     if (M < 1 || N < 128 || N % 128 || K < 64 || K % 64 || epi < GEMM_EPI_STORE_BF16 || epi > GEMM_EPI_GEGLU ||
@@ -892,7 +996,9 @@ int tee_op_attention(tee_ctx* ctx, int layer, const void* d_qkv, const int32_t* 
     ON_DEVICE(ctx);
     if (ctx->cfg.dtype == TEE_BF16) {
         // the work items, and the per-row text bounds the window layers' masks take
-        if ((rc = prepare_attention_items(ctx, h_cu, n_texts, (cudaStream_t)stream))) return rc;
+        if ((rc = prepare_attention_items(ctx, h_cu, n_texts, (cudaStream_t)stream,
+                                          layer_is_global(ctx, layer) ? 0 : 1)))
+            return rc;
         cudaStream_t s = (cudaStream_t)stream;
         LAUNCH(TEE_K_EMBED, 0, 0, launch_positions(d_cu, n_texts, T, ctx->d_pos, ctx->d_rowtb, s));
     }

@@ -67,7 +67,8 @@ struct tee_ctx {
     int8_t* qa = nullptr;               // W8A8 activation codes [T*max(H,I)]
     float* qs = nullptr;                // W8A8 activation scales [T]
     unsigned int* d_status = nullptr;   // device status word
-    int4* d_items[2] = {nullptr, nullptr};   // attention work items (global, window layers)
+    int4* d_slots[2] = {nullptr, nullptr};        // attention units per CTA (global, window layers)
+    int32_t* d_slot_off[2] = {nullptr, nullptr};  // each CTA's first slot [grid + 1]
     int32_t* d_chunk_off = nullptr;     // pool: first chunk of each text [max_texts + 1]
     float* pool_partial = nullptr;      // pool: partial sums [max_chunks * H]
     unsigned int* pool_counters = nullptr;   // pool: chunks finished per text [max_texts], zero between launches
@@ -75,6 +76,9 @@ struct tee_ctx {
     std::vector<int32_t> h_chunk_off;
     int max_items = 0;
     std::vector<int4> h_items[2];
+    std::vector<int4> h_slots[2];
+    std::vector<int32_t> h_slot_off[2];
+    int attn_grid[2] = {0, 0};
 
     cudaStream_t stream = nullptr;      // the context's own stream (tee_encode)
     std::vector<int32_t> h_cu_scratch;
@@ -133,6 +137,8 @@ int tee_set_global_error(int code, const char* msg);
 // attributes, occupancy-derived grid sizes -- is kept per device index, under
 // a lock.  Device indices must be below TEE_MAX_DEVICES.
 #define TEE_MAX_DEVICES 64
+// Upper bound of the attention kernel's grid (one CTA per SM).
+#define TEE_ATTN_MAX_GRID 1024
 // The current device's index and SM count (looked up once per device).
 cudaError_t tee_current_device(int* dev, int* num_sms);
 
@@ -169,13 +175,15 @@ cudaError_t launch_l2_rows(float* x, int M, int D, cudaStream_t s);
 cudaError_t launch_attention_simple(const void* qkv, bool bf16_act, const int32_t* cu, int n_texts, int T, int H,
                                     int n_heads, bool is_global, int window, void* o, cudaStream_t s);
 
-// tcgen05 varlen attention over bf16 qkv [T, 3H]; items {q_start, q_len, k_lo, k_hi} per
-// 128-query tile (global layers: tiles of one text; window layers: tiles of the
-// packed sequence, each row's text bounds in row_tb), persistent CTAs over
-// (item, head) units.
-cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, const int4* d_items, int n_items,
-                                bool is_global, int window, const int2* row_tb, void* o, unsigned int* status,
-                                cudaStream_t s);
+// tcgen05 varlen attention over bf16 qkv [T, 3H]: `grid` persistent CTAs, CTA c
+// taking slots d_slot_off[c] .. d_slot_off[c + 1] of d_slots, each a work item
+// {q_start, q_len | head << 16, k_lo, k_hi} -- a tile of up to 128 queries of
+// one head and the keys it may see (global layers: one text, or consecutive
+// short texts; window layers: a tile of the packed sequence) -- with each
+// row's text bounds in row_tb.
+cudaError_t launch_attention_tc(const void* qkv, int T, int H, int n_heads, const int4* d_slots,
+                                const int32_t* d_slot_off, int grid, bool is_global, int window, const int2* row_tb,
+                                void* o, unsigned int* status, cudaStream_t s);
 
 // Self-test of the bounded waits: a wait on a barrier nothing completes, limited
 // to `limit_cycles`; its expiry sets TEE_STATUS_TIMEOUT in `status`.
