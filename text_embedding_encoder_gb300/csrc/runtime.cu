@@ -411,7 +411,7 @@ int step_layernorm(tee_ctx* ctx, int layer, int which, const float* x, void* y, 
 int step_linear(tee_ctx* ctx, int layer, int which, const void* A, void* C, int T, int epi, int tc_epi,
                 const int32_t* pos, cudaStream_t s) {
     const tee_config& g = ctx->cfg;
-    int N, K;
+    int N = 0, K = 0;
     wshape(g, which, &N, &K);
     const LayerWeights& L = ctx->layers[layer];
     const double flops = 2.0 * T * N * K;
