@@ -11,8 +11,8 @@
 // sharing one tile, longest first; on window layers the tiles of the packed
 // sequence itself.  Where texts share a tile, every row is masked to its own
 // text through the per-token text bounds row_tb.  The
-// kernel is persistent: one CTA per SM walks the units u = blockIdx.x,
-// blockIdx.x + gridDim.x, ...  Ten warps:
+// kernel is persistent: one CTA per SM walks its own list of units, which the
+// host balances (longest first, each to the least-loaded CTA).  Ten warps:
 //   warp 0 lane 0   TMA: each unit's Q tile (double-buffered, so the next
 //                   unit's Q arrives early), then its K and V tiles (128 keys)
 //                   into a KV_STAGES-deep ring, straight from the packed qkv

@@ -217,9 +217,9 @@ double attention_pairs(const int32_t* h_cu, int n_texts, bool is_global, int w) 
 }
 
 // Attention work items of one pass, each a 128-query tile with the key range
-// its queries may see.  List 0 (global layers): the tiles of each text (a
-// tile never holds two texts, so its keys are exactly the text), the most
-// work (queries x keys) first so the heavy CTAs start early.  List 1 (window
+// its queries may see.  List 0 (global layers): the tiles of each text (keys =
+// the text), consecutive texts that together span at most 128 tokens sharing
+// one tile (keys = their span), the most work (queries x keys) first.  List 1 (window
 // layers): the tiles of the packed sequence itself, ignoring text boundaries,
 // so short texts share tiles instead of padding one each; a tile's key range
 // runs from the first key its first row may see (the window clipped to that
