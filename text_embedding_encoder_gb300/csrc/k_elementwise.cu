@@ -93,9 +93,12 @@ template <typename TY>
 __global__ void layernorm_kernel(const float* x, const float* __restrict__ gamma, TY* y, int T, int H, float eps) {
     pdl_wait();
     pdl_trigger();
-    int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    int lane = threadIdx.x & 31;
-    if (warp >= T) return;
+    // Rows are taken last first: the kernel before this one (a residual
+    // projection, or the embedding) writes them first to last, so the rows it
+    // wrote last are read while they are still in L2.
+    const int warp = T - 1 - (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp < 0) return;
     const float4* row = reinterpret_cast<const float4*>(x + (size_t)warp * H);
     const int nv = H / 128;   // float4 per lane
     float4 v[8];
